@@ -1,0 +1,134 @@
+"""Seeded synthetic inputs for the Q1_0 GEMV: weights, activations, raw quants.
+
+This module draws random numbers and lays them out in the input formats; it
+holds none of the product's arithmetic.  Both the CUDA path and the CPU oracle
+receive exactly the arrays made here.
+
+Input formats:
+  Q1_0 weight blocks  uint8 [rows, n/128, 18]: bytes 0-1 the block scale d0 as
+                      little-endian IEEE binary16, bytes 2-17 the 128 sign bits
+                      (element j in byte 2 + j//8, bit j%8; 1 = +d0, 0 = -d0).
+  activations         float32 [B, n]
+  raw q8_0 quants     int8 [B, n] and binary16 scale bits uint16 [B, n/32]
+
+Distributions (the shapes of the workloads the pages and the benchmark name):
+  sign bits           Bernoulli(0.5), i.e. uniform random bytes
+  d0 "halfnormal"     |N(0, 0.02)| rounded to binary16 (about 0.24 % of blocks
+                      land in the binary16 subnormal range)
+  d0 "lognormal"      exp(N(ln 0.02, 1)) rounded to binary16 (scales that vary
+                      per block over several binades: the "layer-shaped" regime)
+  activations         N(0, 1) float32, optionally with 1 % outliers of
+                      magnitude 20 at positions drawn without replacement
+"""
+from __future__ import annotations
+
+import numpy as np
+
+QK1 = 128          # weights per Q1_0 block
+QK8 = 32           # activation values per q8_0 scale
+BLOCK_BYTES = 18
+
+# Llama-3-8B-shaped decode step: per layer q, k, v, o, gate, up, down; then lm_head.
+LLAMA3_8B_LAYER = (
+    ("q", 4096, 4096),
+    ("k", 1024, 4096),
+    ("v", 1024, 4096),
+    ("o", 4096, 4096),
+    ("gate", 14336, 4096),
+    ("up", 14336, 4096),
+    ("down", 4096, 14336),
+)
+LLAMA3_8B_LAYERS = 32
+LLAMA3_8B_LM_HEAD = ("lm_head", 128256, 4096)
+
+
+def decode_set_shapes():
+    """The 225 (name, rows, n) products of one Llama-3-8B-shaped decode step."""
+    out = []
+    for layer in range(LLAMA3_8B_LAYERS):
+        for name, rows, n in LLAMA3_8B_LAYER:
+            out.append((f"L{layer}.{name}", rows, n))
+    out.append(LLAMA3_8B_LM_HEAD)
+    return out
+
+
+def rng_for(*keys: int) -> np.random.Generator:
+    """A generator seeded from a tuple of non-negative integers."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(k) for k in keys])))
+
+
+def fp16_bits(values: np.ndarray) -> np.ndarray:
+    """Binary16 bit patterns of `values` (numpy's own float16 rounding)."""
+    return np.asarray(values, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def block_scales(rng: np.random.Generator, shape, kind: str = "halfnormal") -> np.ndarray:
+    """Binary16 bits of block scales with the named distribution."""
+    if kind == "halfnormal":
+        v = np.abs(rng.standard_normal(shape)) * 0.02
+    elif kind == "lognormal":
+        v = np.exp(rng.standard_normal(shape) + np.log(0.02))
+    elif kind == "ones":
+        v = np.ones(shape)
+    elif kind == "signed":
+        v = rng.standard_normal(shape) * 0.02
+    else:
+        raise ValueError(f"unknown scale distribution {kind!r}")
+    return fp16_bits(v)
+
+
+def assemble_blocks(scale_bits: np.ndarray, sign_bytes: np.ndarray) -> np.ndarray:
+    """Lay out [rows, nb] scale bits and [rows, nb, 16] sign bytes as 18-byte blocks."""
+    rows, nb = scale_bits.shape
+    if sign_bytes.shape != (rows, nb, 16):
+        raise ValueError("sign bytes must be [rows, nb, 16]")
+    blocks = np.empty((rows, nb, BLOCK_BYTES), dtype=np.uint8)
+    s = np.ascontiguousarray(scale_bits, dtype=np.uint16)
+    blocks[:, :, 0] = (s & 0xFF).astype(np.uint8)
+    blocks[:, :, 1] = (s >> 8).astype(np.uint8)
+    blocks[:, :, 2:] = sign_bytes
+    return blocks
+
+
+def weight_blocks(rng: np.random.Generator, rows: int, n: int, scale: str = "halfnormal") -> np.ndarray:
+    """Random Q1_0 weight blocks uint8 [rows, n/128, 18]."""
+    if n % QK1:
+        raise ValueError("n must be a multiple of 128")
+    nb = n // QK1
+    signs = rng.integers(0, 256, size=(rows, nb, 16), dtype=np.uint8)
+    scales = block_scales(rng, (rows, nb), scale)
+    return assemble_blocks(scales, signs)
+
+
+def sign_bytes_from_bits(bits: np.ndarray) -> np.ndarray:
+    """Pack a {0,1} array [..., 128] into the block's 16 sign bytes (bit j%8 of byte j//8)."""
+    bits = np.asarray(bits, dtype=np.uint8)
+    return np.packbits(bits.reshape(bits.shape[:-1] + (16, 8)), axis=-1, bitorder="little")[..., 0]
+
+
+def activations(rng: np.random.Generator, nvec: int, n: int, outliers: float = 0.0,
+                outlier_value: float = 20.0) -> np.ndarray:
+    """float32 [nvec, n] N(0,1) activations; a fraction `outliers` of positions
+    per vector (drawn without replacement) set to +-outlier_value."""
+    x = rng.standard_normal((nvec, n)).astype(np.float32)
+    k = int(round(outliers * n))
+    for v in range(nvec if k else 0):
+        pos = rng.choice(n, size=k, replace=False)
+        sgn = np.where(rng.integers(0, 2, size=k) == 1, 1.0, -1.0)
+        x[v, pos] = (sgn * outlier_value).astype(np.float32)
+    return x
+
+
+def raw_quants(rng: np.random.Generator, nvec: int, n: int, scale: str = "lognormal",
+               m128_frac: float = 0.02):
+    """Raw q8_0 activations not produced by the quantizer: quants uniform over
+    [-128, 127] with a further fraction `m128_frac` forced to -128, and binary16
+    scale bits from `scale`.  Returns (q int8 [nvec, n], d uint16 [nvec, n/32])."""
+    if n % QK8:
+        raise ValueError("n must be a multiple of 32")
+    q = rng.integers(-128, 128, size=(nvec, n), dtype=np.int16)
+    if m128_frac > 0:
+        mask = rng.random((nvec, n)) < m128_frac
+        q[mask] = -128
+    d = block_scales(rng, (nvec, n // QK8), scale)
+    return q.astype(np.int8), d
