@@ -1,0 +1,366 @@
+"""Benchmark: the Llama-3-8B-shaped 1-bit (Q1_0) decode matmul set, batch 1.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole hot path over the 225 products of a decode
+token (32 layers x q, k, v, o, gate, up, down + lm_head): q8_0 quantization of
+each product's f32 activation, then the Q1_0 matrix-vector product, captured
+once as a CUDA graph with programmatic dependent launch and replayed.  Weights
+(1.055 GB of Q1_0 blocks) are packed once and stay resident; every step streams
+all of them, more than the 126 MB L2, so no step reuses another's cached bytes.
+
+Printed (rank 0, one JSON line):
+  value       whole-job weight GB/s = n_gpus * weight bytes / max-over-ranks step time
+  us_per_set  microseconds per decode matmul set on one GPU
+  roofline    the product kernel alone (its 225 launches captured as one graph,
+              timed with CUDA events): algorithmic bytes / time vs measured HBM peak
+  e2e         same metric with the activations copied in from pinned host memory
+              and the outputs copied back inside every timed step
+  cpu_baseline  the CPU oracle timed on a bounded sample (rank 0, N = 1 only)
+Multi-GPU: independent replicas (the product shards by rows, but this workload
+is one GPU's; N GPUs run N copies), scaling "weak".
+
+--impl reference times the CPU oracle (the definition the CUDA path must match
+bit for bit) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("Q1_0 GEMV weight GB/s and % of HBM peak; µs per 8B-shaped decode matmul set")
+WORKLOAD = "llama3-8b-shaped Q1_0 decode matmul set, batch 1 (225 products)"
+
+
+# ------------------------------------------------------------- helpers ----
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("decode_q1_gemv_gb300/csrc/gemv.cu", "decode_q1_gemv_gb300/csrc/common.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the product kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged (else None)."""
+    path = os.path.join(ROOT, "profiles", "q1_0_gemv_decode_set_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch_avg")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU works."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- CPU baseline --
+def cpu_oracle_sample(layers: int, budget_s: float, threads: int, seed: int = 3):
+    """Time the threaded CPU oracle (q8_0 quantization + product) on the first
+    products of the decode set until about `budget_s` of work, returns
+    (weight GB/s, description, threads)."""
+    import numpy as np
+
+    import oracle
+    from decode_q1_gemv_gb300 import synth
+
+    oracle.build()
+    shapes = synth.decode_set_shapes()
+    done_bytes, elapsed, count = 0, 0.0, 0
+    for i, (name, rows, n) in enumerate(shapes[:7 * layers]):
+        blocks = synth.weight_blocks(synth.rng_for(seed, i, 0), rows, n)
+        x = synth.activations(synth.rng_for(seed, i, 1), 1, n)
+        t0 = time.perf_counter()
+        q, d = oracle.q8_quantize(x)
+        out, _ = oracle.gemv_threaded(blocks, q[0], d[0], threads)
+        elapsed += time.perf_counter() - t0
+        done_bytes += rows * n * 18 // 128
+        count += 1
+        if elapsed >= budget_s:
+            break
+    gbs = done_bytes / elapsed / 1e9
+    desc = (f"first {count} products of the decode set ({done_bytes / 1e6:.1f} MB of weights), "
+            f"q8_0 quantization + threaded oracle product, {threads} threads, {elapsed:.1f} s")
+    return gbs, desc, threads
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from decode_q1_gemv_gb300 import synth
+
+    oracle.build()
+    threads = os.cpu_count() or 1
+    shapes = synth.decode_set_shapes()[:7]  # layer 0: q, k, v, o, gate, up, down
+    inputs = []
+    for i, (name, rows, n) in enumerate(shapes):
+        blocks = synth.weight_blocks(synth.rng_for(3, i, 0), rows, n)
+        x = synth.activations(synth.rng_for(3, i, 1), 1, n)
+        inputs.append((blocks, x))
+    sample_bytes = sum(rows * n * 18 // 128 for _, rows, n in shapes)
+
+    def one_step():
+        for blocks, x in inputs:
+            q, d = oracle.q8_quantize(x)
+            oracle.gemv_threaded(blocks, q[0], d[0], threads)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = sample_bytes / dt / 1e9
+    desc = (f"each step: layer 0 of the decode set (7 products, {sample_bytes / 1e6:.1f} MB of weights), "
+            f"q8_0 quantization + threaded oracle product, {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "layer 0 (7 products)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- ours -----
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+
+    from decode_q1_gemv_gb300 import binding
+    from decode_q1_gemv_gb300.decode_set import DecodeSet
+
+    binding.load()
+    ds = DecodeSet(seed=3, device=str(dev))
+    graph = ds.capture()
+    prod_graph = ds.capture_products()
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- main timed region: K decode steps (graph replays), clocks sampled around it
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_pre = time.time()
+    while time.time() - t_pre < 0.6:  # load the GPU so the sampler sees loaded clocks
+        for _ in range(50):
+            graph.replay()
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    step_ms = e0.elapsed_time(e1) / args.steps
+    t_post = time.time()
+    while time.time() - t_post < 0.6:
+        for _ in range(50):
+            graph.replay()
+        torch.cuda.synchronize()
+    sampler.stop()
+    step_ms = max_over_ranks(step_ms)
+
+    # ---- the product kernel alone: its 225 launches as one graph
+    reps = max(args.steps, 50)
+    for _ in range(3):
+        prod_graph.replay()
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(reps):
+        prod_graph.replay()
+    p1.record(stream)
+    torch.cuda.synchronize()
+    prod_ms = p0.elapsed_time(p1) / reps
+
+    # ---- end to end through the public API with host buffers
+    host_x = ds.x_all.cpu().pin_memory()
+    host_out = torch.empty(ds.out_all.shape, dtype=ds.out_all.dtype, pin_memory=True)
+    for _ in range(3):
+        ds.x_all.copy_(host_x, non_blocking=True)
+        graph.replay()
+        host_out.copy_(ds.out_all, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        ds.x_all.copy_(host_x, non_blocking=True)
+        graph.replay()
+        host_out.copy_(ds.out_all, non_blocking=True)
+        stream.synchronize()  # the step's result is on the host
+    x1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps)
+
+    wb = ds.weight_bytes
+    peak, peak_kind = measured_peaks()
+    value = world * wb / (step_ms * 1e-3) / 1e9
+    prod_bytes = wb + ds.activation_bytes // 4 + ds.activation_bytes // 64 + ds.output_bytes
+    achieved = prod_bytes / (prod_ms * 1e-3) / 1e9
+    traffic = recorded_traffic()
+    clocks = sampler.summary()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, desc, cores = cpu_oracle_sample(layers=32, budget_s=args.cpu_budget, threads=os.cpu_count() or 1)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "products": len(ds.shapes), "batch": 1,
+                       "weight_bytes": wb, "l2": "inputs larger than L2: each step streams 1.055 GB of weights",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_set": round(step_ms * 1e3, 2),
+            "hbm_frac_of_measured": round(value / world / peak, 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "k_q1_prod (q1_0_gemv)", "launches": len(ds.shapes),
+                         "avg_launch_us": round(prod_ms * 1e3 / len(ds.shapes), 3),
+                         "algorithmic_bytes_per_launch_avg": prod_bytes // len(ds.shapes),
+                         "peak_source": peak_kind},
+            "e2e": {"value": round(world * wb / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": int(host_x.numel() * 4), "d2h_bytes_per_step": int(host_out.numel() * 4),
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": ds.launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU-oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

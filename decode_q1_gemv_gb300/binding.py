@@ -1,0 +1,210 @@
+"""Thin Python binding of libq1gemv.so (see include/q1gemv.h).
+
+Argument marshalling only: every function checks tensor dtypes, devices and
+shapes, passes raw device pointers and the current CUDA stream to the C ABI,
+and raises ``Q1Error`` with the library's message when a call fails.  All
+arithmetic runs in the library's CUDA kernels; there is no fallback.
+
+Tensors:
+  blocks  torch.uint8  [rows, n/128, 18]  Q1_0 blocks (see q1_0_pack)
+  packed  torch.uint8  [q1_0_packed_bytes(rows, n)]
+  x       torch.float32 [nvec, n]
+  q       torch.int8   [nvec, n] (or [n])
+  d       torch.int16/uint16 [nvec, n/32] (fp16 bit patterns; torch.float16 accepted)
+  out     torch.float32 [nvec, rows] (or [rows])
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+Q1_OK = 0
+Q1_ERR_ARG = -1
+Q1_ERR_CUDA = -2
+Q1_ERR_NOMEM = -3
+Q1_MISMATCH = 2
+
+# Every symbol include/q1gemv.h declares (checked by the tests).
+EXPORTS = ("q1_last_error", "q1_0_packed_bytes", "q1_0_pack", "q1_0_unpack", "q8_quantize_act",
+           "q1_0_gemv", "q1_0_gemm_small", "q1_0_verify")
+
+
+class Q1Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libq1gemv.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libq1gemv.so not found at {path}")
+        lib = ctypes.CDLL(path)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.q1_last_error.argtypes = []
+        lib.q1_last_error.restype = ctypes.c_char_p
+        lib.q1_0_packed_bytes.argtypes = [I64, I64]
+        lib.q1_0_packed_bytes.restype = I64
+        lib.q1_0_pack.argtypes = [P, I64, I64, P, P]
+        lib.q1_0_pack.restype = I
+        lib.q1_0_unpack.argtypes = [P, I64, I64, P, P]
+        lib.q1_0_unpack.restype = I
+        lib.q8_quantize_act.argtypes = [P, I64, I64, P, P, P]
+        lib.q8_quantize_act.restype = I
+        lib.q1_0_gemv.argtypes = [P, I64, I64, P, P, P, P]
+        lib.q1_0_gemv.restype = I
+        lib.q1_0_gemm_small.argtypes = [P, I64, I64, I64, P, P, P, P]
+        lib.q1_0_gemm_small.restype = I
+        lib.q1_0_verify.argtypes = [I, ctypes.c_char_p, ctypes.c_size_t]
+        lib.q1_0_verify.restype = I
+        _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().q1_last_error().decode(errors="replace")
+
+
+def _check(rc: int, what: str):
+    if rc != Q1_OK:
+        raise Q1Error(rc, f"{what}: {last_error()}")
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtypes) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+_SCALE_DTYPES = (torch.int16, torch.float16) + ((torch.uint16,) if hasattr(torch, "uint16") else ())
+
+
+# ------------------------------------------------------------------ calls --
+def packed_bytes(rows: int, n: int) -> int:
+    v = load().q1_0_packed_bytes(int(rows), int(n))
+    if v < 0:
+        raise Q1Error(int(v), last_error())
+    return int(v)
+
+
+def pack(blocks: torch.Tensor, rows: int, n: int, packed: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    nbytes = packed_bytes(rows, n)
+    if blocks.numel() != rows * (n // 128) * 18:
+        raise ValueError("blocks must hold rows*(n/128) 18-byte blocks")
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=blocks.device)
+    if packed.numel() * packed.element_size() < nbytes:
+        raise ValueError("packed buffer too small")
+    _check(load().q1_0_pack(_dev(blocks, "blocks", (torch.uint8,)), rows, n,
+                            _dev(packed, "packed", (torch.uint8,)), _stream_ptr(stream)), "q1_0_pack")
+    return packed
+
+
+def unpack(packed: torch.Tensor, rows: int, n: int, blocks: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    packed_bytes(rows, n)
+    if blocks is None:
+        blocks = torch.empty((rows, n // 128, 18), dtype=torch.uint8, device=packed.device)
+    if blocks.numel() != rows * (n // 128) * 18:
+        raise ValueError("blocks must hold rows*(n/128) 18-byte blocks")
+    _check(load().q1_0_unpack(_dev(packed, "packed", (torch.uint8,)), rows, n,
+                              _dev(blocks, "blocks", (torch.uint8,)), _stream_ptr(stream)), "q1_0_unpack")
+    return blocks
+
+
+def quantize(x: torch.Tensor, q: torch.Tensor | None = None, d: torch.Tensor | None = None, stream=None):
+    """q8_0 quantization of x [nvec, n] (or [n]).  Returns (q int8, d int16 fp16 bits)."""
+    n = x.shape[-1]
+    nvec = x.numel() // n if n else 0
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if d is None:
+        d = torch.empty(x.shape[:-1] + (n // 32,), dtype=torch.int16, device=x.device)
+    if q.numel() != nvec * n or d.numel() != nvec * (n // 32):
+        raise ValueError("q/d sizes do not match x")
+    _check(load().q8_quantize_act(_dev(x, "x", (torch.float32,)), nvec, n, _dev(q, "q", (torch.int8,)),
+                                  _dev(d, "d", _SCALE_DTYPES), _stream_ptr(stream)), "q8_quantize_act")
+    return q, d
+
+
+def gemv(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tensor,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if q.numel() != n or d.numel() != n // 32:
+        raise ValueError("q must hold n quants and d n/32 scales")
+    if out is None:
+        out = torch.empty(rows, dtype=torch.float32, device=q.device)
+    if out.numel() != rows:
+        raise ValueError("out must hold rows values")
+    _check(load().q1_0_gemv(_dev(packed, "packed", (torch.uint8,)), rows, n, _dev(q, "q", (torch.int8,)),
+                            _dev(d, "d", _SCALE_DTYPES), _dev(out, "out", (torch.float32,)),
+                            _stream_ptr(stream)), "q1_0_gemv")
+    return out
+
+
+def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tensor,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    nvec = q.numel() // n
+    if q.numel() != nvec * n or d.numel() != nvec * (n // 32):
+        raise ValueError("q must be [nvec, n] and d [nvec, n/32]")
+    if out is None:
+        out = torch.empty((nvec, rows), dtype=torch.float32, device=q.device)
+    if out.numel() != nvec * rows:
+        raise ValueError("out must hold nvec*rows values")
+    _check(load().q1_0_gemm_small(_dev(packed, "packed", (torch.uint8,)), rows, n, nvec,
+                                  _dev(q, "q", (torch.int8,)), _dev(d, "d", _SCALE_DTYPES),
+                                  _dev(out, "out", (torch.float32,)), _stream_ptr(stream)), "q1_0_gemm_small")
+    return out
+
+
+def verify(quick: bool = False) -> tuple[int, str]:
+    """Run the on-card self-check; returns (status, report text)."""
+    buf = ctypes.create_string_buffer(16384)
+    rc = load().q1_0_verify(1 if quick else 0, buf, len(buf))
+    return rc, buf.value.decode(errors="replace")
+
+
+class Q1Linear:
+    """A packed Q1_0 weight matrix resident on the GPU (convenience wrapper).
+
+    ``Q1Linear(blocks)`` packs the 18-byte blocks once; ``__call__(q, d)`` runs
+    q1_0_gemv for one activation vector and q1_0_gemm_small for several."""
+
+    def __init__(self, blocks: torch.Tensor, stream=None):
+        if blocks.dim() != 3 or blocks.shape[2] != 18:
+            raise ValueError("blocks must be uint8 [rows, n/128, 18]")
+        self.rows = int(blocks.shape[0])
+        self.n = int(blocks.shape[1]) * 128
+        self.packed = pack(blocks, self.rows, self.n, stream=stream)
+
+    def __call__(self, q: torch.Tensor, d: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+        if q.dim() == 1 or q.shape[0] == 1:
+            return gemv(self.packed, self.rows, self.n, q, d, out, stream)
+        return gemm_small(self.packed, self.rows, self.n, q, d, out, stream)

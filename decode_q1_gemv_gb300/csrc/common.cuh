@@ -1,0 +1,126 @@
+// common.cuh -- shared definitions of the CUDA path: packed weight layout,
+// inline-PTX helpers, error reporting.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/q1gemv.h"
+
+namespace q1 {
+
+// ----------------------------------------------------------------- format --
+constexpr int kBlock = 128;       // weights per Q1_0 block
+constexpr int kBlockBytes = 18;   // fp16 scale + 16 sign bytes
+constexpr int kSub = 32;          // activation values per q8_0 scale
+constexpr int kPanel = 32;        // rows per packed panel
+constexpr int kBlockPad = 8;      // blocks per row are padded to a multiple of 8
+
+// Packed device layout (q1_0_pack writes it, the GEMV kernels read it):
+//
+//   rows_pad = round_up(rows, 32), nbp = round_up(n/128, 8), panels = rows_pad/32
+//
+//   bits   : u32 words, at byte 0.  For panel p, block b, panel row r and lane
+//            pair w (0..3) the word sits at
+//              (((p * nbp/4 + b/4) * 32 + r) * 4 + w) * 4 + b%4
+//            i.e. a 16-byte vector holds one (row, lane pair)'s words for four
+//            consecutive blocks, and a warp's 8 rows x 4 lane pairs read 512
+//            contiguous bytes.
+//   scales : fp16 block scales d0, after the bits (byte offset rows_pad*nbp*16).
+//            Half index ((p * nbp/8 + b/8) * 32 + r) * 8 + b%8: one 16-byte
+//            vector = one row's scales for eight consecutive blocks.
+//
+// Within a word w of (row, block): bit 8*i + pl (i = 0..3, plane pl = 0..7)
+// is the sign bit of block element 32*(pl>>1) + 4*(2*w + (pl&1)) + i, i.e. lane
+// 2w + (pl&1) of sub-block pl>>1.  Masking a word with 0x01010101 << pl leaves
+// that lane-and-sub-block's four sign bits as four bytes of value 0 or 2^pl.
+// Padded rows and blocks hold zero bits and zero scales.
+struct Layout {
+  int64_t rows, n, nb, nbp, panels, rows_pad;
+  int64_t bits_bytes, scales_bytes, total_bytes;
+};
+
+inline Layout layout_of(int64_t rows, int64_t n) {
+  Layout L;
+  L.rows = rows;
+  L.n = n;
+  L.nb = n / kBlock;
+  L.nbp = (L.nb + kBlockPad - 1) / kBlockPad * kBlockPad;
+  L.rows_pad = (rows + kPanel - 1) / kPanel * kPanel;
+  L.panels = L.rows_pad / kPanel;
+  L.bits_bytes = L.rows_pad * L.nbp * 16;
+  L.scales_bytes = L.rows_pad * L.nbp * 2;
+  L.total_bytes = L.bits_bytes + L.scales_bytes;
+  return L;
+}
+
+// Plane (0..7) of lane l in sub-block k inside its lane pair's word.
+__host__ __device__ constexpr int plane_of(int k, int l) { return 2 * k + (l & 1); }
+// Effective plane: plane 0 is used shifted left by one (byte value 2), so every
+// lane group is scaled by 2^pe with pe >= 1 and the activation term can enter
+// the integer accumulator as 2^(pe-1) * A.
+__host__ __device__ constexpr int eff_plane(int k, int l) {
+  return plane_of(k, l) > 0 ? plane_of(k, l) : 1;
+}
+
+// Magic accumulator: the float whose bits are 0x4B400000 is 1.5 * 2^23 = C; for
+// |t| < 2^22 the bits 0x4B400000 + t are the float C + t exactly.
+constexpr uint32_t kMagicBits = 0x4B400000u;
+constexpr float kMagic = 12582912.0f;
+
+// ------------------------------------------------------------ PTX helpers --
+__device__ __forceinline__ uint32_t dp4a_us(uint32_t a, uint32_t b, uint32_t c) {
+  // c + sum_i a.u8[i] * b.s8[i]  (a unsigned bytes, b signed bytes)
+  uint32_t d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// Element-wise single-rounding fma / add on float pairs (sm_100+ f32x2).
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's memory, and
+// allow the next kernel in the stream to begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Streaming 16-byte read-only load that does not allocate in L1.
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------- error record --
+// Sets the thread-local last-error text; returns `code`.
+int fail(int code, const char* fmt, ...);
+// Checks a CUDA runtime status after a launch; records and maps errors.
+int cuda_status(cudaError_t e, const char* what);
+
+}  // namespace q1

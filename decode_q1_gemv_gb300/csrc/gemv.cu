@@ -1,0 +1,295 @@
+// gemv.cu -- the Q1_0 x q8_0 row products: q1_0_gemv (one activation vector)
+// and q1_0_gemm_small (up to 64 vectors sharing one pass over the weights).
+//
+// Definition (bankML "docs/modules/gpu.md", "kernels.rs -- the Q1_0 kernels",
+// first bullet): per 128-weight block, four 32-element sub-blocks; eight lanes
+// of exact integer sums (i8 negation wraps -128 to -128); ab = d1*s on the
+// first sub-block and fma(d1, s, ab) after; acc = fma(d0, ab, acc); then the
+// horizontal sum (a0+a4 + a2+a6) + (a1+a5 + a3+a7).  The lanes' chains over
+// the blocks are independent (second bullet), which is what lets four threads
+// share a row here, two lanes each.
+//
+// How each step is computed without changing a single rounding:
+//   * lane sum.  With q' = q except -128 -> 0 and A = sum(q') + 128 * #(-128)
+//     over the lane's four quants, s = 2*M - A where M = sum(bit_i * q'_i).
+//     The packed layout puts the lane's four sign bits on one bit plane pl of
+//     a word's four bytes, so (word & (0x01010101 << pl)) has bytes 0 or 2^pl
+//     and dp4a with q' gives 2^pl * M.  Plane 0 is shifted to plane 1.  The
+//     dp4a accumulator starts at 0x4B400000 - 2^(pe-1) * A (pe = max(pl, 1)),
+//     so the result's bits are the float F = 1.5*2^23 + 2^(pe-1)*s exactly.
+//   * d1*s.  With d' = d1 * 2^(1-pe) and K = -d' * 1.5*2^23 (both exact),
+//     fma(d', F, K) = d1*s exactly (d1*s has at most 21 significant bits).
+//     Because d1*s is exact, fma(d1, s, ab) is the single rounding of ab + d1*s,
+//     i.e. add.rn(ab, d1*s).
+//   * The outer fma(d0, ab, acc) and the horizontal adds are the same IEEE
+//     single-rounding operations as the definition, two lanes at a time with
+//     fma.rn.f32x2 / add.rn.f32x2.
+// The activation-only constants (q', 0x4B400000 - 2^(pe-1)*A, d', K) are built
+// by every CTA in shared memory from q and d, chunk by chunk along n.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace q1 {
+
+constexpr int kThreads = 128;  // 4 warps; thread (row in panel, lane pair)
+
+struct ProdArgs {
+  const uint4* bits;     // packed sign words, 16-byte vectors
+  const uint4* scales;   // packed fp16 block scales, 16-byte vectors (8 each)
+  const int8_t* q;       // activation quants [nvec][n]
+  const uint16_t* d1;    // activation scales [nvec][n/32]
+  float* out;            // [nvec][rows]
+  int64_t n;
+  int rows, nb, nbp, panels, nvec;
+  int vgroups;           // ceil(nvec / V)
+  int kc;                // blocks per activation chunk held in shared memory
+};
+
+// Shared-memory table for one vector and one chunk of kc blocks:
+//   QC[g][w] (uint4)  = { q' word of lane 2w, q' word of lane 2w+1,
+//                         accumulator init of lane 2w, of lane 2w+1 }
+//   DK[g]    (float4) = { d' even lanes, d' odd lanes, K even, K odd }
+// for each sub-block g of the chunk.  80 bytes per sub-block.
+__host__ __device__ constexpr int table_bytes(int kc) { return kc * 4 * (4 * 16 + 16); }
+
+__device__ __forceinline__ float pow2i(int e) {  // exact 2^e for -126 <= e <= 127
+  return __int_as_float((127 + e) << 23);
+}
+
+__device__ void build_table(const int8_t* __restrict__ q, const uint16_t* __restrict__ d1, int nb,
+                            int blk0, int kcb, uint4* QC, float4* DK) {
+  const int nsub = nb * 4;
+  for (int t = threadIdx.x; t < kcb * 16; t += kThreads) {
+    const int g = t >> 2, w = t & 3;
+    const int G = blk0 * 4 + g;  // sub-block index along n
+    const int k = g & 3;         // sub-block within its block (chunks start on block octets)
+    uint32_t qp[2];
+    int ci[2];
+#pragma unroll
+    for (int par = 0; par < 2; ++par) {
+      const int l = 2 * w + par;
+      uint32_t word = 0u;
+      if (G < nsub) word = *reinterpret_cast<const uint32_t*>(q + int64_t(G) * kSub + 4 * l);
+      const uint32_t m80 = __vcmpeq4(word, 0x80808080u);  // 0xff where q == -128
+      qp[par] = word & ~m80;
+      const int cnt = __popc(m80) >> 3;
+      const int A = __dp4a(int(qp[par]), 0x01010101, 0) + 128 * cnt;
+      const int pe = (k == 0 && par == 0) ? 1 : 2 * k + par;
+      ci[par] = int(kMagicBits) - A * (1 << (pe - 1));
+    }
+    QC[g * 4 + w] = make_uint4(qp[0], qp[1], uint32_t(ci[0]), uint32_t(ci[1]));
+  }
+  for (int g = threadIdx.x; g < kcb * 4; g += kThreads) {
+    const int G = blk0 * 4 + g;
+    const int k = g & 3;
+    const float dv = (G < nsub) ? __half2float(__ushort_as_half(d1[G])) : 0.0f;
+    const int pe_even = (k == 0) ? 1 : 2 * k;
+    const int pe_odd = 2 * k + 1;
+    const float de = __fmul_rn(dv, pow2i(1 - pe_even));
+    const float dodd = __fmul_rn(dv, pow2i(1 - pe_odd));
+    DK[g] = make_float4(de, dodd, -__fmul_rn(de, kMagic), -__fmul_rn(dodd, kMagic));
+  }
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ float half_of(const uint4& v, int i) {
+  const uint32_t w = word_of(v, i >> 1);
+  const uint16_t h = uint16_t((i & 1) ? (w >> 16) : (w & 0xffffu));
+  return __half2float(__ushort_as_half(h));
+}
+
+// R panels per CTA (each thread: R rows, one per panel, one lane pair) and
+// V activation vectors per CTA.  1-D grid: bid = panel_group * vgroups + vgroup.
+template <int R, int V>
+__global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tb = table_bytes(a.kc);
+  const int lane = threadIdx.x & 31;
+  const int w = lane & 3;                               // lane pair: lanes 2w, 2w+1
+  const int prow = (threadIdx.x >> 5) * 8 + (lane >> 2);  // row within the panel
+
+  const int vg = blockIdx.x % a.vgroups;
+  const int pg = blockIdx.x / a.vgroups;
+  const int p0 = pg * R;
+  const int v0 = vg * V;
+
+  pdl_launch_dependents();
+  pdl_wait();
+
+  const int64_t nq4 = a.nbp / 4, nq8 = a.nbp / 8;
+  uint64_t acc[R][V];
+#pragma unroll
+  for (int j = 0; j < R; ++j)
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[j][v] = 0ull;  // both lanes +0
+
+  for (int blk0 = 0; blk0 < a.nbp; blk0 += a.kc) {
+    const int kcb = min(a.kc, a.nbp - blk0);
+    __syncthreads();
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      unsigned char* t = smem + v * tb;
+      const int vv = min(v0 + v, a.nvec - 1);
+      build_table(a.q + int64_t(vv) * a.n, a.d1 + int64_t(vv) * (a.n / kSub), a.nb, blk0, kcb,
+                  reinterpret_cast<uint4*>(t), reinterpret_cast<float4*>(t + a.kc * 4 * 64));
+    }
+    __syncthreads();
+
+    for (int b = blk0; b < blk0 + kcb; b += 8) {
+      uint4 sc[R], wa[R], wb[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int64_t p = p0 + j;
+        if (p < a.panels) {
+          sc[j] = ldg_stream(a.scales + (p * nq8 + b / 8) * kPanel + prow);
+          wa[j] = ldg_stream(a.bits + ((p * nq4 + b / 4) * kPanel + prow) * 4 + w);
+          wb[j] = ldg_stream(a.bits + ((p * nq4 + b / 4 + 1) * kPanel + prow) * 4 + w);
+        } else {
+          sc[j] = wa[j] = wb[j] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) {
+        uint64_t ab[R][V];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int g = (b - blk0 + bb) * 4 + k;
+          uint32_t m0[R], m1[R];
+#pragma unroll
+          for (int j = 0; j < R; ++j) {
+            const uint32_t W = word_of(bb < 4 ? wa[j] : wb[j], bb & 3);
+            m0[j] = W & (0x01010101u << (2 * k));
+            m1[j] = W & (0x01010101u << (2 * k + 1));
+            if (k == 0) m0[j] <<= 1;  // plane 0 -> byte values 0/2
+          }
+#pragma unroll
+          for (int v = 0; v < V; ++v) {
+            const unsigned char* t = smem + v * tb;
+            const uint4 qc = reinterpret_cast<const uint4*>(t)[g * 4 + w];
+            const float4 dk = reinterpret_cast<const float4*>(t + a.kc * 4 * 64)[g];
+            const uint64_t dpair = f2pack(dk.x, dk.y);
+            const uint64_t kpair = f2pack(dk.z, dk.w);
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+              const uint32_t D0 = dp4a_us(m0[j], qc.x, qc.z);
+              const uint32_t D1 = dp4a_us(m1[j], qc.y, qc.w);
+              const uint64_t pr = fma2(dpair, f2pack(__uint_as_float(D0), __uint_as_float(D1)), kpair);
+              ab[j][v] = (k == 0) ? pr : add2(ab[j][v], pr);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const float d0 = half_of(sc[j], bb);
+          const uint64_t d0p = f2pack(d0, d0);
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[j][v] = fma2(d0p, ab[j][v], acc[j][v]);
+        }
+      }
+    }
+  }
+
+  // Horizontal sum: lane pair w holds (a_2w, a_2w+1).  xor 2 pairs w with w+2
+  // (a0+a4, a1+a5 | a2+a6, a3+a7); xor 1 then adds those; the final add joins
+  // the even-lane and odd-lane halves.
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int64_t row = int64_t(p0 + j) * kPanel + prow;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      uint64_t s = acc[j][v];
+      s = add2(s, __shfl_xor_sync(0xffffffffu, s, 2));
+      s = add2(s, __shfl_xor_sync(0xffffffffu, s, 1));
+      float lo, hi;
+      f2unpack(s, lo, hi);
+      const float r = __fadd_rn(lo, hi);
+      if (w == 0 && p0 + j < a.panels && row < a.rows && v0 + v < a.nvec)
+        a.out[int64_t(v0 + v) * a.rows + row] = r;
+    }
+  }
+}
+
+template <int R, int V>
+static int launch(const ProdArgs& a0, int64_t panels, cudaStream_t s, const char* who) {
+  ProdArgs a = a0;
+  a.vgroups = (a.nvec + V - 1) / V;
+  a.kc = std::min<int>(a.nbp, std::max(8, (128 / V) / 8 * 8));
+  const int64_t pgroups = (panels + R - 1) / R;
+  const int64_t grid = pgroups * a.vgroups;
+  if (grid > 0x7fffffff) return fail(Q1_ERR_ARG, "%s: matrix too large for one launch", who);
+  const int smem = table_bytes(a.kc) * V;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_prod<R, V>, a), who);
+}
+
+static int check_prod_args(const char* who, const void* packed, int64_t rows, int64_t n, int64_t nvec,
+                           const int8_t* q, const uint16_t* d, const float* out) {
+  if (rows < 1 || rows > (int64_t(1) << 26) || n < 128 || n > (int64_t(1) << 24) || n % 128)
+    return fail(Q1_ERR_ARG, "%s: bad shape rows=%lld n=%lld", who, (long long)rows, (long long)n);
+  if (nvec < 1 || nvec > 64) return fail(Q1_ERR_ARG, "%s: nvec=%lld outside 1..64", who, (long long)nvec);
+  if (!packed || !q || !d || !out) return fail(Q1_ERR_ARG, "%s: null pointer", who);
+  if (reinterpret_cast<uintptr_t>(packed) % 16 || reinterpret_cast<uintptr_t>(q) % 16 ||
+      reinterpret_cast<uintptr_t>(d) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(Q1_ERR_ARG, "%s: buffers must be 16-byte aligned", who);
+  return Q1_OK;
+}
+
+static ProdArgs make_args(const void* packed, int64_t rows, int64_t n, int64_t nvec, const int8_t* q,
+                          const uint16_t* d, float* out) {
+  Layout L = layout_of(rows, n);
+  ProdArgs a = {};
+  a.bits = static_cast<const uint4*>(packed);
+  a.scales = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(packed) + L.bits_bytes);
+  a.q = q;
+  a.d1 = d;
+  a.out = out;
+  a.n = n;
+  a.rows = int(rows);
+  a.nb = int(L.nb);
+  a.nbp = int(L.nbp);
+  a.panels = int(L.panels);
+  a.nvec = int(nvec);
+  return a;
+}
+
+}  // namespace q1
+
+using namespace q1;
+
+extern "C" int q1_0_gemv(const void* packed, int64_t rows, int64_t n, const int8_t* q, const uint16_t* d,
+                         float* out, void* stream) {
+  if (int e = check_prod_args("q1_0_gemv", packed, rows, n, 1, q, d, out)) return e;
+  ProdArgs a = make_args(packed, rows, n, 1, q, d, out);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Rows per thread: more rows amortise the shared activation constants; fewer
+  // keep enough CTAs in flight for small matrices.
+  const int64_t panels = a.panels;
+  if (panels >= 4 * 304) return launch<4, 1>(a, panels, s, "q1_0_gemv launch");
+  if (panels >= 2 * 304) return launch<2, 1>(a, panels, s, "q1_0_gemv launch");
+  return launch<1, 1>(a, panels, s, "q1_0_gemv launch");
+}
+
+extern "C" int q1_0_gemm_small(const void* packed, int64_t rows, int64_t n, int64_t nvec, const int8_t* q,
+                               const uint16_t* d, float* out, void* stream) {
+  if (int e = check_prod_args("q1_0_gemm_small", packed, rows, n, nvec, q, d, out)) return e;
+  ProdArgs a = make_args(packed, rows, n, nvec, q, d, out);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t panels = a.panels;
+  if (nvec == 1) return launch<1, 1>(a, panels, s, "q1_0_gemm_small launch");
+  if (nvec <= 2) return launch<2, 2>(a, panels, s, "q1_0_gemm_small launch");
+  if (nvec <= 4) return launch<2, 4>(a, panels, s, "q1_0_gemm_small launch");
+  return launch<1, 8>(a, panels, s, "q1_0_gemm_small launch");
+}

@@ -1,0 +1,120 @@
+// pack.cu -- q1_0_pack / q1_0_unpack: 18-byte Q1_0 blocks <-> the packed
+// device layout documented in common.cuh.  Runs once per weight matrix.
+#include "common.cuh"
+
+namespace q1 {
+
+// Element of the 128-element block held by bit (8*i + pl) of lane-pair word w.
+__device__ __forceinline__ int elem_of(int w, int pl, int i) {
+  return 32 * (pl >> 1) + 4 * (2 * w + (pl & 1)) + i;
+}
+
+__device__ __forceinline__ int64_t bits_word_index(int64_t p, int64_t b, int r, int w, int64_t nbp) {
+  return (((p * (nbp / 4) + b / 4) * kPanel + r) * 4 + w) * 4 + (b % 4);
+}
+
+__device__ __forceinline__ int64_t scale_index(int64_t p, int64_t b, int r, int64_t nbp) {
+  return ((p * (nbp / 8) + b / 8) * kPanel + r) * 8 + (b % 8);
+}
+
+// One thread per (padded row, padded block).
+__global__ void k_pack(const uint8_t* __restrict__ blocks, int64_t rows, int64_t nb, int64_t nbp,
+                       int64_t rows_pad, uint32_t* __restrict__ bits, uint16_t* __restrict__ scales) {
+  int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= rows_pad * nbp) return;
+  int64_t r = idx / nbp, b = idx % nbp;
+  int64_t p = r / kPanel;
+  int rr = int(r % kPanel);
+  uint32_t word[4] = {0u, 0u, 0u, 0u};
+  uint16_t sc = 0;
+  if (r < rows && b < nb) {
+    const uint8_t* blk = blocks + (r * nb + b) * kBlockBytes;
+    sc = uint16_t(blk[0] | (blk[1] << 8));
+    uint8_t qs[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) qs[j] = blk[2 + j];
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+#pragma unroll
+      for (int pl = 0; pl < 8; ++pl)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          int e = elem_of(w, pl, i);
+          uint32_t bit = (qs[e >> 3] >> (e & 7)) & 1u;
+          word[w] |= bit << (8 * i + pl);
+        }
+  }
+#pragma unroll
+  for (int w = 0; w < 4; ++w) bits[bits_word_index(p, b, rr, w, nbp)] = word[w];
+  scales[scale_index(p, b, rr, nbp)] = sc;
+}
+
+// One thread per (row, block) of the real matrix.
+__global__ void k_unpack(const uint32_t* __restrict__ bits, const uint16_t* __restrict__ scales,
+                         int64_t rows, int64_t nb, int64_t nbp, uint8_t* __restrict__ blocks) {
+  int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= rows * nb) return;
+  int64_t r = idx / nb, b = idx % nb;
+  int64_t p = r / kPanel;
+  int rr = int(r % kPanel);
+  uint8_t qs[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) qs[j] = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t word = bits[bits_word_index(p, b, rr, w, nbp)];
+#pragma unroll
+    for (int pl = 0; pl < 8; ++pl)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        int e = elem_of(w, pl, i);
+        qs[e >> 3] |= uint8_t(((word >> (8 * i + pl)) & 1u) << (e & 7));
+      }
+  }
+  uint16_t sc = scales[scale_index(p, b, rr, nbp)];
+  uint8_t* blk = blocks + idx * kBlockBytes;
+  blk[0] = uint8_t(sc & 0xff);
+  blk[1] = uint8_t(sc >> 8);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) blk[2 + j] = qs[j];
+}
+
+static int check_pack_args(const char* who, const void* blocks, int64_t rows, int64_t n, const void* packed) {
+  if (rows < 1 || rows > (int64_t(1) << 26) || n < 128 || n > (int64_t(1) << 24) || n % 128)
+    return fail(Q1_ERR_ARG, "%s: bad shape rows=%lld n=%lld", who, (long long)rows, (long long)n);
+  if (!blocks || !packed) return fail(Q1_ERR_ARG, "%s: null pointer", who);
+  if (reinterpret_cast<uintptr_t>(blocks) % 2) return fail(Q1_ERR_ARG, "%s: blocks not 2-byte aligned", who);
+  if (reinterpret_cast<uintptr_t>(packed) % 16) return fail(Q1_ERR_ARG, "%s: packed not 16-byte aligned", who);
+  return Q1_OK;
+}
+
+}  // namespace q1
+
+using namespace q1;
+
+extern "C" int q1_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* packed, void* stream) {
+  if (int e = check_pack_args("q1_0_pack", blocks, rows, n, packed)) return e;
+  Layout L = layout_of(rows, n);
+  uint32_t* bits = static_cast<uint32_t*>(packed);
+  uint16_t* scales = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(packed) + L.bits_bytes);
+  int64_t total = L.rows_pad * L.nbp;
+  int threads = 256;
+  int64_t grid = (total + threads - 1) / threads;
+  k_pack<<<dim3(unsigned(grid)), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales);
+  return cuda_status(cudaGetLastError(), "q1_0_pack launch");
+}
+
+extern "C" int q1_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t* blocks, void* stream) {
+  if (int e = check_pack_args("q1_0_unpack", blocks, rows, n, packed)) return e;
+  Layout L = layout_of(rows, n);
+  const uint32_t* bits = static_cast<const uint32_t*>(packed);
+  const uint16_t* scales =
+      reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(packed) + L.bits_bytes);
+  int64_t total = rows * L.nb;
+  int threads = 256;
+  int64_t grid = (total + threads - 1) / threads;
+  k_unpack<<<dim3(unsigned(grid)), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      bits, scales, rows, L.nb, L.nbp, blocks);
+  return cuda_status(cudaGetLastError(), "q1_0_unpack launch");
+}

@@ -1,0 +1,123 @@
+/*
+ * q1gemv.h -- C ABI of the GB300 Q1_0 (1-bit) GEMV library (libq1gemv.so).
+ *
+ * The library computes the row-parallel product of 1-bit Q1_0 weights with a
+ * q8_0-quantized activation, as bankML's "docs/modules/gpu.md" defines it
+ * ("kernels.rs -- the Q1_0 kernels", first bullet):
+ *
+ *   for every output row, lanes l = 0..7 keep an f32 accumulator a_l = +0;
+ *   for every 128-weight block b (in order), with weight scale d0 (fp16):
+ *     for every 32-element sub-block k = 0..3, with activation scale d1 (fp16):
+ *       s = sum over the lane's 4 elements 32k+4l+i of (bit ? q : -q),
+ *           an exact integer, where negating -128 gives -128;
+ *       ab = d1*s (k = 0), ab = fma(d1, s, ab) (k = 1..3);
+ *     a_l = fma(d0, ab, a_l);
+ *   out = ((a0+a4) + (a2+a6)) + ((a1+a5) + (a3+a7)).
+ *
+ * Every output element equals, bit for bit, the plain CPU definition above on
+ * any GPU, launch shape or batch size.
+ *
+ * Conventions for every call:
+ *   - n (activation length) is a multiple of 128, 128 <= n <= 1<<24; rows >= 1,
+ *     rows <= 1<<26.
+ *   - Pointers are DEVICE pointers owned by the caller unless noted; the
+ *     library keeps no reference to them after the call returns.  Buffers must
+ *     be 16-byte aligned and must not overlap.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work; nothing blocks the host unless noted.
+ *   - Return value: Q1_OK (0) on success, a negative Q1_ERR_* code on a
+ *     rejected argument or a CUDA error (nothing is enqueued after a rejected
+ *     argument); q1_last_error() then names the call and the reason.
+ *   - Activation scales must be finite.  With a non-finite activation scale
+ *     the affected outputs are unspecified (never a fault).  Weight scales may
+ *     be any fp16 value: non-finite ones propagate exactly as in the definition.
+ */
+#ifndef Q1GEMV_H
+#define Q1GEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q1_OK 0
+#define Q1_ERR_ARG (-1)     /* shape, pointer, alignment or size rejected   */
+#define Q1_ERR_CUDA (-2)    /* a CUDA runtime call or launch failed         */
+#define Q1_ERR_NOMEM (-3)   /* q1_0_verify could not allocate device memory */
+#define Q1_MISMATCH 2       /* q1_0_verify: some output differs             */
+
+/* Text of the last error on the calling thread ("" if none).  The pointer is
+ * valid until the next library call on the same thread. */
+const char *q1_last_error(void);
+
+/* Bytes of the packed weight buffer q1_0_pack writes for a rows x n matrix
+ * (18 bytes per 128 weights, rows padded to a multiple of 32 and blocks per
+ * row to a multiple of 8).  Returns a negative Q1_ERR_ARG for a bad shape.
+ * Host-only; touches no device. */
+int64_t q1_0_packed_bytes(int64_t rows, int64_t n);
+
+/* Repack Q1_0 weights once into the library's device layout
+ * ("kernels.rs -- the Q1_0 kernels", pack_q1_0 bullet: repacked once, the
+ * numbers unchanged, only aligned).
+ *   blocks : device, rows*(n/128) consecutive 18-byte blocks, row-major; each
+ *            block = fp16 scale d0 (little-endian) + 16 bytes of sign bits,
+ *            element j in byte 2 + j/8, bit j%8, 1 = +d0, 0 = -d0.
+ *            Only 2-byte alignment is required for this pointer.
+ *   packed : device, q1_0_packed_bytes(rows, n) bytes, written entirely.
+ * Errors: Q1_ERR_ARG for a bad shape or pointer; Q1_ERR_CUDA on launch failure. */
+int q1_0_pack(const uint8_t *blocks, int64_t rows, int64_t n, void *packed, void *stream);
+
+/* Inverse of q1_0_pack: writes rows*(n/128) 18-byte blocks identical to the
+ * ones that were packed.  Same pointer rules as q1_0_pack. */
+int q1_0_unpack(const void *packed, int64_t rows, int64_t n, uint8_t *blocks, void *stream);
+
+/* q8_0 activation quantization (the q8_0 activation of "kernels.rs", pack_act
+ * bullet; scale = max|x| / 127).  For each vector v < nvec and each 32-value
+ * block: amax = max|x|, d = amax/127 (f32), id = d ? 1/d : 0 (f32),
+ * q = roundf(x*id) (half away from zero), scale stored as fp16 (round to
+ * nearest even) of d.
+ *   x : device f32 [nvec][n]; q : device int8 [nvec][n];
+ *   d : device fp16 bits [nvec][n/32].
+ * n is a multiple of 32 here (128 for use with the products), 1 <= nvec <= 65535.
+ * Inputs must be finite and max|x| <= 65504*127 for the scale to stay finite. */
+int q8_quantize_act(const float *x, int64_t nvec, int64_t n, int8_t *q, uint16_t *d, void *stream);
+
+/* Matrix-vector product ("kernels.rs -- the Q1_0 kernels", first and second
+ * bullets: one exact dot product per output row; rows are independent).
+ *   packed : device, from q1_0_pack(rows, n).
+ *   q, d   : device q8_0 activation: int8 [n], fp16 bits [n/32] (any quants,
+ *            including -128).
+ *   out    : device f32 [rows].
+ * Launch uses programmatic dependent launch: the kernel's weight streaming may
+ * start while the previous kernel on `stream` finishes; it reads q and d only
+ * after that kernel's writes are visible. */
+int q1_0_gemv(const void *packed, int64_t rows, int64_t n, const int8_t *q, const uint16_t *d,
+              float *out, void *stream);
+
+/* Small-batch product: the matrix-vector product for each of nvec activation
+ * vectors sharing one pass over the weights (1 <= nvec <= 64).
+ *   q : device int8 [nvec][n]; d : device fp16 bits [nvec][n/32];
+ *   out : device f32 [nvec][rows] (row-major per vector).
+ * out[v][r] is bit-identical to q1_0_gemv on vector v. */
+int q1_0_gemm_small(const void *packed, int64_t rows, int64_t n, int64_t nvec, const int8_t *q,
+                    const uint16_t *d, float *out, void *stream);
+
+/* On-card self-check ("How it is verified": verify_q1_0 compares every kernel
+ * and shape with the CPU bits, including -128 quants and a layer-shaped regime
+ * whose per-block scales make products inexact in f32).  Runs synchronously on
+ * the current device with its own allocations, against a host-side reference
+ * compiled into the library.
+ *   flags  : 0 = default shape set; 1 = quick (two small shapes).
+ *   report : host buffer receiving one line per kernel and shape, or the first
+ *            differing row ("row i differs ..."); may be NULL.
+ * Returns Q1_OK if every output is bit-identical, Q1_MISMATCH (2) if any
+ * differs, or a negative error. */
+int q1_0_verify(int flags, char *report, size_t report_len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q1GEMV_H */

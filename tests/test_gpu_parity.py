@@ -1,0 +1,309 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Every comparison is element by element on the same seeded inputs: int8 quants
+and fp16 scale bits byte for byte, f32 outputs bit for bit (the definition has
+exactly one correct f32 per row; the tolerance is zero).  Small and ragged
+shapes are compared in full; full-size workloads are compared on sampled rows
+that the oracle computes one by one, in the launch configuration the benchmark
+times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_q1_gemv_gb300 import binding, synth
+from tests.golden.cases import load_cases
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+    oracle.build()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def bits_equal(got: np.ndarray, want: np.ndarray):
+    got = np.asarray(got, dtype=np.float32)
+    want = np.asarray(want, dtype=np.float32)
+    assert got.shape == want.shape
+    diff = np.nonzero(got.view(np.uint32) != want.view(np.uint32))[0]
+    assert diff.size == 0, (f"{diff.size} of {got.size} outputs differ; first at {diff[:5]}: "
+                            f"gpu {got.ravel()[diff[:5]]} oracle {want.ravel()[diff[:5]]}")
+
+
+def gpu_gemv(blocks: np.ndarray, q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    rows, nb, _ = blocks.shape
+    n = nb * 128
+    packed = binding.pack(dev(blocks), rows, n)
+    out = binding.gemv(packed, rows, n, dev(q.astype(np.int8)), dev(d.view(np.int16)))
+    return out.cpu().numpy()
+
+
+def gpu_gemm(blocks: np.ndarray, q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    rows, nb, _ = blocks.shape
+    n = nb * 128
+    packed = binding.pack(dev(blocks), rows, n)
+    out = binding.gemm_small(packed, rows, n, dev(q.astype(np.int8)), dev(d.view(np.int16)))
+    return out.cpu().numpy()
+
+
+# ------------------------------------------------------------ self-check --
+def test_library_self_check():
+    rc, report = binding.verify(quick=False)
+    assert rc == binding.Q1_OK, report
+    assert "bit-exact" in report
+
+
+# --------------------------------------------------------------- packing --
+@pytest.mark.parametrize("rows,n", [(1, 128), (31, 384), (33, 1024), (100, 1152), (257, 4096), (64, 14336)])
+def test_pack_unpack_round_trip(rows, n):
+    blocks = synth.weight_blocks(synth.rng_for(101, rows, n), rows, n, "signed")
+    packed = binding.pack(dev(blocks), rows, n)
+    assert packed.numel() == binding.packed_bytes(rows, n)
+    back = binding.unpack(packed, rows, n).cpu().numpy()
+    assert np.array_equal(back, blocks)
+
+
+# ---------------------------------------------------------- quantization --
+@pytest.mark.parametrize("case", ["normal", "outliers", "tiny", "large", "zeros", "ties"])
+def test_quantize_parity(case):
+    rng = synth.rng_for(102, len(case))
+    nvec, n = 3, 4096
+    if case == "normal":
+        x = synth.activations(rng, nvec, n)
+    elif case == "outliers":
+        x = synth.activations(rng, nvec, n, outliers=0.01)
+    elif case == "tiny":
+        x = synth.activations(rng, nvec, n) * np.float32(1e-6)
+    elif case == "large":
+        x = synth.activations(rng, nvec, n) * np.float32(3e4)
+    elif case == "zeros":
+        x = synth.activations(rng, nvec, n)
+        x[:, 64:128] = 0.0
+        x[1, :] = 0.0
+    else:  # values whose scaled magnitude is exactly k + 0.5 when amax = 127
+        x = np.zeros((nvec, n), dtype=np.float32)
+        x[:, ::32] = 127.0
+        x[:, 1::32] = (rng.integers(-126, 126, size=(nvec, n // 32)) + 0.5).astype(np.float32)
+    q, d = binding.quantize(dev(x))
+    want_q, want_d = oracle.q8_quantize(x)
+    assert np.array_equal(q.cpu().numpy(), want_q)
+    assert np.array_equal(d.cpu().numpy().view(np.uint16), want_d)
+
+
+def test_quantize_hand_derived_fixture():
+    import json
+    import os
+    spec = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "q8_hand_derived.json")))
+    for c in spec["cases"]:
+        xb = np.full(32, int(c["x_fill_hex"], 16), dtype=np.uint32)
+        for k, v in c["x_hex"].items():
+            xb[int(k)] = int(v, 16)
+        q, d = binding.quantize(dev(xb.view(np.float32)[None, :]))
+        want = np.full(32, c["expected_q_fill"], dtype=np.int64)
+        for k, v in c["expected_q"].items():
+            want[int(k)] = v
+        assert np.array_equal(q.cpu().numpy()[0].astype(np.int64), want)
+        assert int(d.cpu().numpy().view(np.uint16)[0, 0]) == int(c["expected_d_hex"], 16)
+
+
+# ------------------------------------------------------ golden fixtures ----
+@pytest.mark.parametrize("case", load_cases(), ids=lambda c: c[0])
+def test_gemv_hand_derived(case):
+    name, blocks, q, d1, expected = case
+    got = gpu_gemv(blocks, q, d1)
+    assert got.view(np.uint32)[0] == np.float32(expected).view(np.uint32), (name, got, expected)
+    got_b = gpu_gemm(blocks, np.stack([q, q, q]), np.stack([d1, d1, d1]))
+    assert np.all(got_b.view(np.uint32) == np.float32(expected).view(np.uint32))
+
+
+# ------------------------------------------------------------ gemv: small --
+SHAPES = [(1, 128), (7, 256), (31, 384), (32, 1024), (33, 1152), (100, 2048), (255, 4096),
+          (300, 1024), (1000, 512), (64, 14336), (5, 16384), (3, 17408)]
+
+
+@pytest.mark.parametrize("rows,n", SHAPES)
+@pytest.mark.parametrize("regime", ["quantized", "raw_m128", "halfnormal_subnormal"])
+def test_gemv_parity(rows, n, regime):
+    rng = synth.rng_for(103, rows, n, len(regime))
+    if regime == "quantized":
+        blocks = synth.weight_blocks(rng, rows, n, "halfnormal")
+        q, d = oracle.q8_quantize(synth.activations(rng, 1, n, outliers=0.01))
+    elif regime == "raw_m128":
+        blocks = synth.weight_blocks(rng, rows, n, "lognormal")
+        q, d = synth.raw_quants(rng, 1, n, scale="lognormal", m128_frac=0.05)
+    else:
+        blocks = synth.weight_blocks(rng, rows, n, "halfnormal")
+        q, d = synth.raw_quants(rng, 1, n, scale="halfnormal", m128_frac=0.01)
+        d[0, ::7] = rng.integers(1, 0x400, size=d[0, ::7].shape)  # binary16 subnormal scales
+    got = gpu_gemv(blocks, q[0], d[0])
+    bits_equal(got, oracle.gemv(blocks, q[0], d[0]))
+
+
+@pytest.mark.parametrize("rows,n", [(40000, 256), (20000, 512), (9999, 1152)])
+def test_gemv_parity_many_rows(rows, n):
+    """Row counts that select 4, 2 and 1 rows per thread in the launcher."""
+    rng = synth.rng_for(104, rows, n)
+    blocks = synth.weight_blocks(rng, rows, n, "lognormal")
+    q, d = synth.raw_quants(rng, 1, n, scale="lognormal", m128_frac=0.02)
+    bits_equal(gpu_gemv(blocks, q[0], d[0]), oracle.gemv(blocks, q[0], d[0]))
+
+
+def test_config_single_256x1024():
+    """W 256x1024, Bernoulli(0.5) signs, |N(0,0.02)| block scales, N(0,1) input."""
+    rng = synth.rng_for(1, 0, 0)
+    blocks = synth.weight_blocks(rng, 256, 1024, "halfnormal")
+    x = synth.activations(synth.rng_for(1, 0, 1), 1, 1024)
+    q, d = binding.quantize(dev(x))
+    want_q, want_d = oracle.q8_quantize(x)
+    assert np.array_equal(q.cpu().numpy(), want_q) and np.array_equal(d.cpu().numpy().view(np.uint16), want_d)
+    packed = binding.pack(dev(blocks), 256, 1024)
+    out = binding.gemv(packed, 256, 1024, q[0], d[0]).cpu().numpy()
+    bits_equal(out, oracle.gemv(blocks, want_q[0], want_d[0]))
+
+
+def test_config_4096x4096_outliers_full():
+    """W 4096x4096, input N(0,1) with 1 % outliers at 20: every row compared."""
+    rng = synth.rng_for(2, 0, 0)
+    blocks = synth.weight_blocks(rng, 4096, 4096, "halfnormal")
+    x = synth.activations(synth.rng_for(2, 0, 1), 1, 4096, outliers=0.01)
+    q, d = binding.quantize(dev(x))
+    packed = binding.pack(dev(blocks), 4096, 4096)
+    out = binding.gemv(packed, 4096, 4096, q[0], d[0]).cpu().numpy()
+    want_q, want_d = oracle.q8_quantize(x)
+    bits_equal(out, oracle.gemv(blocks, want_q[0], want_d[0]))
+
+
+# ------------------------------------------------------- batched products --
+@pytest.mark.parametrize("nvec", [1, 2, 3, 4, 5, 8, 9, 16, 33, 64])
+def test_gemm_small_parity(nvec):
+    rows, n = 300, 1152
+    rng = synth.rng_for(105, nvec)
+    blocks = synth.weight_blocks(rng, rows, n, "lognormal")
+    q, d = synth.raw_quants(rng, nvec, n, scale="lognormal", m128_frac=0.03)
+    got = gpu_gemm(blocks, q, d)
+    bits_equal(got, oracle.gemm(blocks, q, d))
+
+
+def test_gemm_small_columns_equal_gemv():
+    rows, n, nvec = 777, 4096, 16
+    rng = synth.rng_for(106)
+    blocks = synth.weight_blocks(rng, rows, n, "halfnormal")
+    x = synth.activations(rng, nvec, n)
+    q, d = binding.quantize(dev(x))
+    packed = binding.pack(dev(blocks), rows, n)
+    outb = binding.gemm_small(packed, rows, n, q, d).cpu().numpy()
+    for v in range(nvec):
+        outv = binding.gemv(packed, rows, n, q[v], d[v]).cpu().numpy()
+        assert np.array_equal(outb[v].view(np.uint32), outv.view(np.uint32))
+
+
+def _sampled(blocks, q, d, count, rng):
+    nvec, rows = q.shape[0], blocks.shape[0]
+    idx = rng.integers(0, rows, size=count)
+    idx[:4] = [0, rows - 1, rows // 2, 31 % rows]
+    vec = rng.integers(0, nvec, size=count)
+    vec[:2] = [0, nvec - 1]
+    return idx, vec, oracle.rows_sampled(blocks, idx, q, d, vec)
+
+
+@pytest.mark.parametrize("rows,n,nvec,scale", [
+    (14336, 4096, 16, "halfnormal"),
+    (4096, 14336, 16, "halfnormal"),
+    (128256, 4096, 64, "lognormal"),
+    (4096, 14336, 64, "lognormal"),
+])
+def test_batched_full_size_sampled(rows, n, nvec, scale):
+    """Multi-sequence (16 vectors) and prefill-chunk (64 vectors, log-normal
+    block scales) products at full size: 3000 sampled outputs vs the oracle."""
+    rng = synth.rng_for(4 if nvec == 16 else 5, rows, n)
+    blocks = synth.weight_blocks(rng, rows, n, scale)
+    x = synth.activations(rng, nvec, n)
+    q, d = binding.quantize(dev(x))
+    packed = binding.pack(dev(blocks), rows, n)
+    out = binding.gemm_small(packed, rows, n, q, d).cpu().numpy()
+    qh, dh = q.cpu().numpy(), d.cpu().numpy().view(np.uint16)
+    want_q, want_d = oracle.q8_quantize(x)
+    assert np.array_equal(qh, want_q) and np.array_equal(dh, want_d)
+    idx, vec, want = _sampled(blocks, want_q, want_d, 3000, rng)
+    bits_equal(out[vec, idx], want)
+
+
+# ------------------------------------------------------- decode set (graph) --
+def test_decode_set_graph_sampled():
+    """The full 225-product Llama-3-8B-shaped decode set, run exactly as the
+    benchmark runs it (one CUDA graph, programmatic dependent launch), with 40
+    sampled rows of every product compared against the oracle."""
+    from decode_q1_gemv_gb300.decode_set import DecodeSet
+    ds = DecodeSet(seed=3)
+    ds.capture()
+    for o in ds.out:
+        o.fill_(float("nan"))
+    ds.replay()
+    ds.replay()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(7)
+    for i, (name, rows, n) in enumerate(ds.shapes):
+        if i % 7 not in (0, 2, 4, 6) and i != len(ds.shapes) - 1:
+            continue  # every q, v, gate, down and lm_head
+        blocks = ds.host_blocks(i)
+        x = ds.host_x(i)
+        want_q, want_d = oracle.q8_quantize(x[None, :])
+        assert np.array_equal(ds.q[i].cpu().numpy(), want_q[0]), name
+        assert np.array_equal(ds.d[i].cpu().numpy().view(np.uint16), want_d[0]), name
+        idx = rng.integers(0, rows, size=40)
+        want = oracle.rows_sampled(blocks, idx, want_q[0], want_d[0])
+        bits_equal(ds.out[i].cpu().numpy()[idx], want)
+
+
+# ---------------------------------------------------- edge and error cases --
+def test_outputs_written_once_and_guard_untouched():
+    rows, n = 77, 512
+    rng = synth.rng_for(107)
+    blocks = synth.weight_blocks(rng, rows, n)
+    q, d = synth.raw_quants(rng, 1, n)
+    packed = binding.pack(dev(blocks), rows, n)
+    buf = torch.full((rows + 64,), float("nan"), device="cuda")
+    binding.gemv(packed, rows, n, dev(q[0]), dev(d[0].view(np.int16)), out=buf[:rows])
+    host = buf.cpu().numpy()
+    assert not np.any(np.isnan(host[:rows]))
+    assert np.all(np.isnan(host[rows:]))
+    bits_equal(host[:rows], oracle.gemv(blocks, q[0], d[0]))
+
+
+def test_deterministic_and_stream_independent():
+    rows, n = 5000, 4096
+    rng = synth.rng_for(108)
+    blocks = synth.weight_blocks(rng, rows, n, "lognormal")
+    q, d = synth.raw_quants(rng, 1, n, scale="lognormal")
+    packed = binding.pack(dev(blocks), rows, n)
+    qd, dd = dev(q[0]), dev(d[0].view(np.int16))
+    a = binding.gemv(packed, rows, n, qd, dd).cpu().numpy()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = binding.gemv(packed, rows, n, qd, dd)
+    s.synchronize()
+    assert np.array_equal(a.view(np.uint32), b.cpu().numpy().view(np.uint32))
+
+
+def test_bad_arguments_raise():
+    packed = torch.empty(binding.packed_bytes(64, 256), dtype=torch.uint8, device="cuda")
+    q = torch.zeros(256, dtype=torch.int8, device="cuda")
+    d = torch.zeros(8, dtype=torch.int16, device="cuda")
+    with pytest.raises(binding.Q1Error):
+        binding.load()  # noqa: B018 - the library loads
+        rc = binding.load().q1_0_gemv(packed.data_ptr(), 64, 200, q.data_ptr(), d.data_ptr(),
+                                      torch.empty(64, device="cuda").data_ptr(), None)
+        binding._check(rc, "q1_0_gemv")
+    with pytest.raises(TypeError):
+        binding.gemv(packed, 64, 256, q.float(), d)
+    with pytest.raises(ValueError):
+        binding.gemv(packed, 64, 256, q.cpu(), d)
