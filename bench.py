@@ -3,17 +3,21 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one pass of the whole hot path over the 225 products of a decode
-token (32 layers x q, k, v, o, gate, up, down + lm_head): q8_0 quantization of
-each product's f32 activation, then the Q1_0 matrix-vector product, captured
-once as a CUDA graph with programmatic dependent launch and replayed.  Weights
-(1.055 GB of Q1_0 blocks) are packed once and stay resident; every step streams
-all of them, more than the 126 MB L2, so no step reuses another's cached bytes.
+token (32 layers x q, k, v, o, gate, up, down + lm_head), each with its own
+activation vector: q8_0 quantization of the f32 activation and the Q1_0
+matrix-vector product.  The timed schedule is one q1_0_gemv_multi launch per
+step (quantization fused), captured as a CUDA graph and replayed; the same work
+is also timed as the launches a decode step's data dependencies allow
+("grouped", 129), one launch per product ("decode", 225) and separate
+quantize + product launches ("separate", 450).  Weights (1.055 GB of Q1_0
+blocks) are packed once and stay resident; every step streams all of them,
+more than the 126 MB L2, so no step reuses another's cached bytes.
 
 Printed (rank 0, one JSON line):
   value       whole-job weight GB/s = n_gpus * weight bytes / max-over-ranks step time
   us_per_set  microseconds per decode matmul set on one GPU
-  roofline    the product kernel alone (its 225 launches captured as one graph,
-              timed with CUDA events): algorithmic bytes / time vs measured HBM peak
+  roofline    the product kernel (one launch per step): algorithmic bytes per
+              launch / launch time vs the measured HBM peak
   e2e         same metric with the activations copied in from pinned host memory
               and the outputs copied back inside every timed step
   cpu_baseline  the CPU oracle timed on a bounded sample (rank 0, N = 1 only)
@@ -208,6 +212,17 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------- ours -----
+def _time_graph(graph, reps, stream):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -225,8 +240,8 @@ def run_ours(args):
 
     binding.load()
     ds = DecodeSet(seed=3, device=str(dev))
-    graph = ds.capture()
-    prod_graph = ds.capture_products()
+    graphs = {sch: ds._capture(lambda sch=sch: ds.step(schedule=sch)) for sch in DecodeSet.SCHEDULES}
+    graph = graphs["set"]
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -244,44 +259,35 @@ def run_ours(args):
         graph.replay()
     torch.cuda.synchronize()
 
-    # ---- main timed region: K decode steps (graph replays), clocks sampled around it
+    # ---- main timed region: K decode steps (one launch each), clocks sampled
+    # over a window of the same load around it
     sampler = ClockSampler(local)
     sampler.start()
     t_pre = time.time()
-    while time.time() - t_pre < 0.6:  # load the GPU so the sampler sees loaded clocks
-        for _ in range(50):
+    while time.time() - t_pre < 0.6:
+        for _ in range(20):
             graph.replay()
         torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    step_ms = _time_graph(graph, args.steps, stream)
     barrier()
-    step_ms = e0.elapsed_time(e1) / args.steps
     t_post = time.time()
     while time.time() - t_post < 0.6:
-        for _ in range(50):
+        for _ in range(20):
             graph.replay()
         torch.cuda.synchronize()
     sampler.stop()
     step_ms = max_over_ranks(step_ms)
 
-    # ---- the product kernel alone: its 225 launches as one graph
-    reps = max(args.steps, 50)
-    for _ in range(3):
-        prod_graph.replay()
-    torch.cuda.synchronize()
-    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    p0.record(stream)
-    for _ in range(reps):
-        prod_graph.replay()
-    p1.record(stream)
-    torch.cuda.synchronize()
-    prod_ms = p0.elapsed_time(p1) / reps
+    # ---- the same work under the other schedules (decode-order dependencies)
+    sched_us = {"set": round(step_ms * 1e3, 2)}
+    for sch in ("grouped", "decode", "separate"):
+        g = graphs[sch]
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        sched_us[sch] = round(max_over_ranks(_time_graph(g, max(args.steps // 4, 10), stream)) * 1e3, 2)
 
     # ---- end to end through the public API with host buffers
     host_x = ds.x_all.cpu().pin_memory()
@@ -307,8 +313,8 @@ def run_ours(args):
     wb = ds.weight_bytes
     peak, peak_kind = measured_peaks()
     value = world * wb / (step_ms * 1e-3) / 1e9
-    prod_bytes = wb + ds.activation_bytes // 4 + ds.activation_bytes // 64 + ds.output_bytes
-    achieved = prod_bytes / (prod_ms * 1e-3) / 1e9
+    launch_bytes = wb + ds.activation_bytes + ds.output_bytes   # one launch per step
+    achieved = launch_bytes / (step_ms * 1e-3) / 1e9
     traffic = recorded_traffic()
     clocks = sampler.summary()
 
@@ -322,21 +328,22 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "products": len(ds.shapes), "batch": 1,
-                       "weight_bytes": wb, "l2": "inputs larger than L2: each step streams 1.055 GB of weights",
+            "config": {"workload": WORKLOAD, "products": len(ds.shapes), "batch": 1, "weight_bytes": wb,
+                       "schedule": "set: one q1_0_gemv_multi launch, q8_0 quantization fused",
+                       "l2": "inputs larger than L2: each step streams 1.055 GB of weights",
                        "parallelism": f"replicas x{world}"},
             "us_per_set": round(step_ms * 1e3, 2),
             "hbm_frac_of_measured": round(value / world / peak, 4),
+            "us_per_set_by_schedule": sched_us,
+            "launches_by_schedule": {sch: ds.launches(sch) for sch in DecodeSet.SCHEDULES},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "kernel": "k_q1_prod (q1_0_gemv)", "launches": len(ds.shapes),
-                         "avg_launch_us": round(prod_ms * 1e3 / len(ds.shapes), 3),
-                         "algorithmic_bytes_per_launch_avg": prod_bytes // len(ds.shapes),
-                         "peak_source": peak_kind},
+                         "kernel": "k_q1_multi (q1_0_gemv_multi, 225 products)", "launches_per_step": 1,
+                         "algorithmic_bytes_per_launch": launch_bytes, "peak_source": peak_kind},
             "e2e": {"value": round(world * wb / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": int(host_x.numel() * 4), "d2h_bytes_per_step": int(host_out.numel() * 4),
                     "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": ds.launches_per_step * args.steps,
+            "gpu_launches": ds.launches("set") * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

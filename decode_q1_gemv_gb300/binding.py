@@ -31,7 +31,16 @@ Q1_MISMATCH = 2
 
 # Every symbol include/q1gemv.h declares (checked by the tests).
 EXPORTS = ("q1_last_error", "q1_0_packed_bytes", "q1_0_pack", "q1_0_unpack", "q8_quantize_act",
-           "q1_0_gemv", "q1_0_gemm_small", "q1_0_verify")
+           "q1_0_gemv", "q1_0_gemv_multi", "q1_0_gemm_small", "q1_0_verify", "q1_device_status")
+
+MAX_PRODUCTS = 256
+
+
+class Product(ctypes.Structure):
+    """Mirror of q1_product (include/q1gemv.h)."""
+    _fields_ = [("packed", ctypes.c_void_p), ("rows", ctypes.c_int64), ("n", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("q", ctypes.c_void_p), ("d", ctypes.c_void_p),
+                ("out", ctypes.c_void_p)]
 
 
 class Q1Error(RuntimeError):
@@ -71,8 +80,12 @@ def load():
         lib.q8_quantize_act.restype = I
         lib.q1_0_gemv.argtypes = [P, I64, I64, P, P, P, P]
         lib.q1_0_gemv.restype = I
+        lib.q1_0_gemv_multi.argtypes = [ctypes.POINTER(Product), I, P]
+        lib.q1_0_gemv_multi.restype = I
         lib.q1_0_gemm_small.argtypes = [P, I64, I64, I64, P, P, P, P]
         lib.q1_0_gemm_small.restype = I
+        lib.q1_device_status.argtypes = [I]
+        lib.q1_device_status.restype = I
         lib.q1_0_verify.argtypes = [I, ctypes.c_char_p, ctypes.c_size_t]
         lib.q1_0_verify.restype = I
         _lib = lib
@@ -169,6 +182,34 @@ def gemv(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tens
     return out
 
 
+def product_array(items):
+    """Build a ctypes q1_product array from tuples
+    (packed, rows, n, x_or_None, q_or_None, d_or_None, out) of CUDA tensors."""
+    arr = (Product * len(items))()
+    for i, (packed, rows, n, x, q, d, out) in enumerate(items):
+        if x is None and (q is None or d is None):
+            raise ValueError("each product needs x, or q and d")
+        if x is not None and x.numel() != n:
+            raise ValueError("x must hold n values")
+        if q is not None and (q.numel() != n or d.numel() != n // 32):
+            raise ValueError("q must hold n quants and d n/32 scales")
+        if out.numel() != rows:
+            raise ValueError("out must hold rows values")
+        arr[i] = Product(_dev(packed, "packed", (torch.uint8,)), int(rows), int(n),
+                         _dev(x, "x", (torch.float32,)) if x is not None else None,
+                         _dev(q, "q", (torch.int8,)) if q is not None else None,
+                         _dev(d, "d", _SCALE_DTYPES) if d is not None else None,
+                         _dev(out, "out", (torch.float32,)))
+    return arr
+
+
+def gemv_multi(items=None, stream=None, array=None):
+    """One launch for several independent products.  `items` as product_array
+    takes them, or a prebuilt `array` (to avoid rebuilding it per call)."""
+    arr = array if array is not None else product_array(items)
+    _check(load().q1_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q1_0_gemv_multi")
+
+
 def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tensor,
                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     nvec = q.numel() // n
@@ -182,6 +223,14 @@ def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torc
                                   _dev(q, "q", (torch.int8,)), _dev(d, "d", _SCALE_DTYPES),
                                   _dev(out, "out", (torch.float32,)), _stream_ptr(stream)), "q1_0_gemm_small")
     return out
+
+
+def device_status(clear: bool = True) -> int:
+    """The library's device status flags (0 = no kernel gave up a wait)."""
+    v = load().q1_device_status(1 if clear else 0)
+    if v < 0:
+        raise Q1Error(v, last_error())
+    return v
 
 
 def verify(quick: bool = False) -> tuple[int, str]:

@@ -7,7 +7,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/q1gemv.h"
+#include "q1gemv.h"
 
 namespace q1 {
 
@@ -122,5 +122,70 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 int fail(int code, const char* fmt, ...);
 // Checks a CUDA runtime status after a launch; records and maps errors.
 int cuda_status(cudaError_t e, const char* what);
+
+}  // namespace q1
+
+namespace q1 {
+
+// ------------------------------------------------ mbarrier / bulk copy ----
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait until the barrier's phase with parity `parity` has completed.  Bounded:
+// gives up after about `limit_ns` nanoseconds and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  uint32_t done = 0;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  if (done) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    if (done) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completing on `bar` (both addresses 16-byte
+// aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Device status flags: a kernel whose bounded wait gives up ORs this into the
+// library's device status word (read with q1_device_status) instead of hanging.
+constexpr unsigned kStatusWaitTimeout = 1u;
 
 }  // namespace q1

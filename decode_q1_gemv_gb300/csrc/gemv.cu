@@ -1,34 +1,14 @@
-// gemv.cu -- the Q1_0 x q8_0 row products: q1_0_gemv (one activation vector)
-// and q1_0_gemm_small (up to 64 vectors sharing one pass over the weights).
+// gemv.cu -- q1_0_gemm_small: the Q1_0 x q8_0 row product for up to 64
+// activation vectors sharing one pass over the weights.
 //
 // Definition (bankML "docs/modules/gpu.md", "kernels.rs -- the Q1_0 kernels",
-// first bullet): per 128-weight block, four 32-element sub-blocks; eight lanes
-// of exact integer sums (i8 negation wraps -128 to -128); ab = d1*s on the
-// first sub-block and fma(d1, s, ab) after; acc = fma(d0, ab, acc); then the
-// horizontal sum (a0+a4 + a2+a6) + (a1+a5 + a3+a7).  The lanes' chains over
-// the blocks are independent (second bullet), which is what lets four threads
-// share a row here, two lanes each.
-//
-// How each step is computed without changing a single rounding:
-//   * lane sum.  With q' = q except -128 -> 0 and A = sum(q') + 128 * #(-128)
-//     over the lane's four quants, s = 2*M - A where M = sum(bit_i * q'_i).
-//     The packed layout puts the lane's four sign bits on one bit plane pl of
-//     a word's four bytes, so (word & (0x01010101 << pl)) has bytes 0 or 2^pl
-//     and dp4a with q' gives 2^pl * M.  Plane 0 is shifted to plane 1.  The
-//     dp4a accumulator starts at 0x4B400000 - 2^(pe-1) * A (pe = max(pl, 1)),
-//     so the result's bits are the float F = 1.5*2^23 + 2^(pe-1)*s exactly.
-//   * d1*s.  With d' = d1 * 2^(1-pe) and K = -d' * 1.5*2^23 (both exact),
-//     fma(d', F, K) = d1*s exactly (d1*s has at most 21 significant bits).
-//     Because d1*s is exact, fma(d1, s, ab) is the single rounding of ab + d1*s,
-//     i.e. add.rn(ab, d1*s).
-//   * The outer fma(d0, ab, acc) and the horizontal adds are the same IEEE
-//     single-rounding operations as the definition, two lanes at a time with
-//     fma.rn.f32x2 / add.rn.f32x2.
-// The activation-only constants (q', 0x4B400000 - 2^(pe-1)*A, d', K) are built
-// by every CTA in shared memory from q and d, chunk by chunk along n.
+// first bullet) and the exactness argument are in table.cuh; out[v][r] is the
+// matrix-vector product of row r and vector v.  A thread owns R rows (one per
+// panel) and one lane pair, and keeps V vectors' chains; the activation
+// constants of the V vectors sit in shared memory, chunk by chunk along n.
 #include <algorithm>
 
-#include "common.cuh"
+#include "table.cuh"
 
 namespace q1 {
 
@@ -45,62 +25,6 @@ struct ProdArgs {
   int vgroups;           // ceil(nvec / V)
   int kc;                // blocks per activation chunk held in shared memory
 };
-
-// Shared-memory table for one vector and one chunk of kc blocks:
-//   QC[g][w] (uint4)  = { q' word of lane 2w, q' word of lane 2w+1,
-//                         accumulator init of lane 2w, of lane 2w+1 }
-//   DK[g]    (float4) = { d' even lanes, d' odd lanes, K even, K odd }
-// for each sub-block g of the chunk.  80 bytes per sub-block.
-__host__ __device__ constexpr int table_bytes(int kc) { return kc * 4 * (4 * 16 + 16); }
-
-__device__ __forceinline__ float pow2i(int e) {  // exact 2^e for -126 <= e <= 127
-  return __int_as_float((127 + e) << 23);
-}
-
-__device__ void build_table(const int8_t* __restrict__ q, const uint16_t* __restrict__ d1, int nb,
-                            int blk0, int kcb, uint4* QC, float4* DK) {
-  const int nsub = nb * 4;
-  for (int t = threadIdx.x; t < kcb * 16; t += kThreads) {
-    const int g = t >> 2, w = t & 3;
-    const int G = blk0 * 4 + g;  // sub-block index along n
-    const int k = g & 3;         // sub-block within its block (chunks start on block octets)
-    uint32_t qp[2];
-    int ci[2];
-#pragma unroll
-    for (int par = 0; par < 2; ++par) {
-      const int l = 2 * w + par;
-      uint32_t word = 0u;
-      if (G < nsub) word = *reinterpret_cast<const uint32_t*>(q + int64_t(G) * kSub + 4 * l);
-      const uint32_t m80 = __vcmpeq4(word, 0x80808080u);  // 0xff where q == -128
-      qp[par] = word & ~m80;
-      const int cnt = __popc(m80) >> 3;
-      const int A = __dp4a(int(qp[par]), 0x01010101, 0) + 128 * cnt;
-      const int pe = (k == 0 && par == 0) ? 1 : 2 * k + par;
-      ci[par] = int(kMagicBits) - A * (1 << (pe - 1));
-    }
-    QC[g * 4 + w] = make_uint4(qp[0], qp[1], uint32_t(ci[0]), uint32_t(ci[1]));
-  }
-  for (int g = threadIdx.x; g < kcb * 4; g += kThreads) {
-    const int G = blk0 * 4 + g;
-    const int k = g & 3;
-    const float dv = (G < nsub) ? __half2float(__ushort_as_half(d1[G])) : 0.0f;
-    const int pe_even = (k == 0) ? 1 : 2 * k;
-    const int pe_odd = 2 * k + 1;
-    const float de = __fmul_rn(dv, pow2i(1 - pe_even));
-    const float dodd = __fmul_rn(dv, pow2i(1 - pe_odd));
-    DK[g] = make_float4(de, dodd, -__fmul_rn(de, kMagic), -__fmul_rn(dodd, kMagic));
-  }
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-__device__ __forceinline__ float half_of(const uint4& v, int i) {
-  const uint32_t w = word_of(v, i >> 1);
-  const uint16_t h = uint16_t((i & 1) ? (w >> 16) : (w & 0xffffu));
-  return __half2float(__ushort_as_half(h));
-}
 
 // R panels per CTA (each thread: R rows, one per panel, one lane pair) and
 // V activation vectors per CTA.  1-D grid: bid = panel_group * vgroups + vgroup.
@@ -134,8 +58,8 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
     for (int v = 0; v < V; ++v) {
       unsigned char* t = smem + v * tb;
       const int vv = min(v0 + v, a.nvec - 1);
-      build_table(a.q + int64_t(vv) * a.n, a.d1 + int64_t(vv) * (a.n / kSub), a.nb, blk0, kcb,
-                  reinterpret_cast<uint4*>(t), reinterpret_cast<float4*>(t + a.kc * 4 * 64));
+      build_table_q(a.q + int64_t(vv) * a.n, a.d1 + int64_t(vv) * (a.n / kSub), a.nb, blk0, kcb, t,
+                    threadIdx.x, kThreads, a.kc);
     }
     __syncthreads();
 
@@ -170,7 +94,7 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
           for (int v = 0; v < V; ++v) {
             const unsigned char* t = smem + v * tb;
             const uint4 qc = reinterpret_cast<const uint4*>(t)[g * 4 + w];
-            const float4 dk = reinterpret_cast<const float4*>(t + a.kc * 4 * 64)[g];
+            const float4 dk = reinterpret_cast<const float4*>(t + table_dk_offset(a.kc))[g];
             const uint64_t dpair = f2pack(dk.x, dk.y);
             const uint64_t kpair = f2pack(dk.z, dk.w);
 #pragma unroll
@@ -268,19 +192,6 @@ static ProdArgs make_args(const void* packed, int64_t rows, int64_t n, int64_t n
 }  // namespace q1
 
 using namespace q1;
-
-extern "C" int q1_0_gemv(const void* packed, int64_t rows, int64_t n, const int8_t* q, const uint16_t* d,
-                         float* out, void* stream) {
-  if (int e = check_prod_args("q1_0_gemv", packed, rows, n, 1, q, d, out)) return e;
-  ProdArgs a = make_args(packed, rows, n, 1, q, d, out);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // Rows per thread: more rows amortise the shared activation constants; fewer
-  // keep enough CTAs in flight for small matrices.
-  const int64_t panels = a.panels;
-  if (panels >= 4 * 304) return launch<4, 1>(a, panels, s, "q1_0_gemv launch");
-  if (panels >= 2 * 304) return launch<2, 1>(a, panels, s, "q1_0_gemv launch");
-  return launch<1, 1>(a, panels, s, "q1_0_gemv launch");
-}
 
 extern "C" int q1_0_gemm_small(const void* packed, int64_t rows, int64_t n, int64_t nvec, const int8_t* q,
                                const uint16_t* d, float* out, void* stream) {

@@ -1,0 +1,381 @@
+// multi.cu -- the streaming matrix-vector kernel: q1_0_gemv (one product) and
+// q1_0_gemv_multi (up to Q1_MAX_PRODUCTS independent products in one launch).
+//
+// Definition (bankML "docs/modules/gpu.md", "kernels.rs -- the Q1_0 kernels",
+// first and second bullets): each output row is one dot product of 128-weight
+// blocks, four sub-blocks each, eight lanes of exact integer sums (i8 negation
+// wraps -128 to -128), ab = d1*s then fma(d1, s, ab), acc = fma(d0, ab, acc),
+// and the horizontal sum (a0+a4 + a2+a6) + (a1+a5 + a3+a7).  Lanes are
+// independent chains, so four threads share a row, two lanes each; table.cuh
+// explains how every step keeps the definition's single roundings.
+//
+// Structure.  A CTA is one producer warp and eight consumer warps.  The
+// producer streams packed weights HBM -> shared memory with 1-D bulk copies
+// into a ring of stages (mbarrier full/empty pairs).  A stage is one octet of
+// blocks (8 x 128 weights per row) for the CTA's current tile of 2R panels
+// (64R rows): 4 KB of sign words and 512 B of scales per panel.  Consumer
+// thread (row, lane pair) handles R rows of a tile.  CTAs are persistent: the
+// products' tiles are split into contiguous ranges of equal weight bytes, one
+// range per CTA, and the producer runs ahead across tile and product
+// boundaries.  The producer reads only weights, so it starts before
+// griddepcontrol.wait; consumers wait for the preceding kernel before reading
+// the activation (f32, quantized here exactly as q8_quantize_act does, or
+// already quantized).  Every wait is bounded and reports through the device
+// status word instead of hanging.
+#include <algorithm>
+
+#include "table.cuh"
+
+namespace q1 {
+
+__device__ unsigned g_device_status = 0u;
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kMultiThreads = kConsumers + 32;
+constexpr int kPanelBits = 4096;   // one panel x one octet: 32 rows x 8 blocks x 16 B
+constexpr int kPanelScales = 512;  // 32 rows x 8 blocks x 2 B
+constexpr int kPanelStage = kPanelBits + kPanelScales;
+constexpr int kConsumerBarrier = 1;
+constexpr int kMaxKc = 128;        // blocks of activation held in the table (n <= 16384 in one chunk)
+
+struct MProd {
+  const uint8_t* packed;
+  const float* x;        // f32 activation, or null
+  const int8_t* q;       // q8_0 quants (when x is null)
+  const uint16_t* d;     // q8_0 scales (when x is null)
+  float* out;
+  int64_t bits_bytes;
+  int64_t cost_begin;    // sum over earlier products of tiles * nbp
+  int rows, nb, nbp, panels, tiles;
+};
+
+template <int PMAX>
+struct MArgs {
+  MProd p[PMAX];
+  int64_t total_cost;
+  int count;
+  int kc;                // table chunk in blocks (multiple of 8)
+};
+
+template <int R> struct Ring;
+template <> struct Ring<1> { static constexpr int stages = 6; };
+template <> struct Ring<2> { static constexpr int stages = 3; };
+template <> struct Ring<4> { static constexpr int stages = 2; };
+
+template <int R>
+__host__ __device__ constexpr int stage_bytes() { return 2 * R * kPanelStage; }
+
+template <int R>
+__host__ __device__ constexpr int multi_smem_bytes(int kc) {
+  return Ring<R>::stages * stage_bytes<R>() + table_bytes(kc) + 2 * Ring<R>::stages * 8;
+}
+
+// Tiles [t_lo, t_hi) of product p that fall in this CTA's cost range.
+__device__ __forceinline__ void tile_range(const MProd& p, int64_t lo, int64_t hi, int& t_lo, int& t_hi) {
+  const int64_t c = p.nbp;
+  auto first_at_or_after = [&](int64_t v) -> int {
+    int64_t t = v <= p.cost_begin ? 0 : (v - p.cost_begin + c - 1) / c;
+    return int(t < p.tiles ? t : p.tiles);
+  };
+  t_lo = first_at_or_after(lo);
+  t_hi = first_at_or_after(hi);
+}
+
+template <int R, int PMAX>
+__global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_constant__ MArgs<PMAX> a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int S = Ring<R>::stages;
+  constexpr int SB = stage_bytes<R>();
+  unsigned char* table = smem + S * SB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(table + table_bytes(a.kc));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t lo = a.total_cost * int64_t(blockIdx.x) / int64_t(gridDim.x);
+  const int64_t hi = a.total_cost * int64_t(blockIdx.x + 1) / int64_t(gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_addr(&bars[s]), 1);
+      mbar_init(smem_addr(&bars[S + s]), kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      bool ok = true;
+      int it = 0;
+      for (int j = 0; j < a.count && ok; ++j) {
+        const MProd& p = a.p[j];
+        int t_lo, t_hi;
+        tile_range(p, lo, hi, t_lo, t_hi);
+        const int octets = p.nbp / 8;
+        for (int t = t_lo; t < t_hi && ok; ++t) {
+          const int p0 = t * 2 * R;
+          const int np = min(2 * R, p.panels - p0);
+          for (int oct = 0; oct < octets; ++oct, ++it) {
+            const int s = it % S;
+            if (it >= S && !mbar_wait(smem_addr(&bars[S + s]), uint32_t(it / S - 1) & 1u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = smem_addr(&bars[s]);
+            mbar_arrive_expect_tx(full, uint32_t(np * kPanelStage));
+            const uint32_t dst = smem_addr(smem + s * SB);
+            for (int u = 0; u < np; ++u) {
+              const int64_t pp = p0 + u;
+              bulk_g2s(dst + u * kPanelBits, p.packed + pp * int64_t(p.nbp) * 512 + int64_t(oct) * kPanelBits,
+                       kPanelBits, full);
+              bulk_g2s(dst + 2 * R * kPanelBits + u * kPanelScales,
+                       p.packed + p.bits_bytes + (pp * (p.nbp / 8) + oct) * kPanelScales, kPanelScales, full);
+            }
+          }
+        }
+      }
+      if (!ok) atomicOr(&g_device_status, kStatusWaitTimeout);
+    }
+    return;
+  }
+
+  // ------------------------------- consumers ------------------------------
+  const int tid = threadIdx.x;
+  const int ps = warp >> 2;                       // panel parity within the tile
+  const int prow = (warp & 3) * 8 + (lane >> 2);  // row within the panel
+  const int w = lane & 3;                         // lane pair 2w, 2w+1
+  const uint4* QC = reinterpret_cast<const uint4*>(table);
+  const float4* DK = reinterpret_cast<const float4*>(table + table_dk_offset(a.kc));
+
+  pdl_wait();  // the activations may be written by the preceding kernel
+
+  // Last tile of this CTA (to signal dependents when it starts).
+  int last_j = -1, last_t = -1;
+  for (int j = 0; j < a.count; ++j) {
+    int t_lo, t_hi;
+    tile_range(a.p[j], lo, hi, t_lo, t_hi);
+    if (t_lo < t_hi) {
+      last_j = j;
+      last_t = t_hi - 1;
+    }
+  }
+  if (last_j < 0) pdl_launch_dependents();
+
+  bool ok = true;
+  int it = 0;
+  for (int j = 0; j < a.count && ok; ++j) {
+    const MProd& p = a.p[j];
+    int t_lo, t_hi;
+    tile_range(p, lo, hi, t_lo, t_hi);
+    if (t_lo >= t_hi) continue;
+    const int octets = p.nbp / 8;
+    const bool one_chunk = p.nbp <= a.kc;
+    if (one_chunk) {
+      named_barrier(kConsumerBarrier, kConsumers);  // previous product's table no longer read
+      if (p.x) build_table_x(p.x, p.nb, 0, p.nbp, table, tid, kConsumers, a.kc);
+      else build_table_q(p.q, p.d, p.nb, 0, p.nbp, table, tid, kConsumers, a.kc);
+      named_barrier(kConsumerBarrier, kConsumers);
+    }
+    for (int t = t_lo; t < t_hi && ok; ++t) {
+      if (j == last_j && t == last_t) pdl_launch_dependents();
+      uint64_t acc[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = 0ull;  // both lanes +0
+
+      for (int oct = 0; oct < octets; ++oct, ++it) {
+        const int b0 = oct * 8;
+        if (!one_chunk && b0 % a.kc == 0) {
+          named_barrier(kConsumerBarrier, kConsumers);
+          const int kcb = min(a.kc, p.nbp - b0);
+          if (p.x) build_table_x(p.x, p.nb, b0, kcb, table, tid, kConsumers, a.kc);
+          else build_table_q(p.q, p.d, p.nb, b0, kcb, table, tid, kConsumers, a.kc);
+          named_barrier(kConsumerBarrier, kConsumers);
+        }
+        const int gb = one_chunk ? b0 : b0 % a.kc;
+        const int s = it % S;
+        if (!mbar_wait(smem_addr(&bars[s]), uint32_t(it / S) & 1u)) {
+          ok = false;
+          break;
+        }
+        const unsigned char* st = smem + s * SB;
+        uint4 sc[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          sc[r] = reinterpret_cast<const uint4*>(st + 2 * R * kPanelBits + (2 * r + ps) * kPanelScales)[prow];
+#pragma unroll
+        for (int quad = 0; quad < 2; ++quad) {
+          uint4 wv[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            wv[r] = reinterpret_cast<const uint4*>(st + (2 * r + ps) * kPanelBits)[quad * 128 + prow * 4 + w];
+          if (quad == 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[S + s]));  // stage fully read
+          }
+#pragma unroll
+          for (int bq = 0; bq < 4; ++bq) {
+            const int bb = quad * 4 + bq;
+            uint64_t ab[R];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int g = (gb + bb) * 4 + k;
+              const uint4 qc = QC[g * 4 + w];
+              const float4 dk = DK[g];
+              const uint64_t dpair = f2pack(dk.x, dk.y);
+              const uint64_t kpair = f2pack(dk.z, dk.w);
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                const uint64_t pr = subblock_products(word_of(wv[r], bq), k, qc, dpair, kpair);
+                ab[r] = (k == 0) ? pr : add2(ab[r], pr);
+              }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const float d0 = half_of(sc[r], bb);
+              acc[r] = fma2(f2pack(d0, d0), ab[r], acc[r]);
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      // Horizontal sum: xor 2 pairs lane pair w with w+2 (a0+a4, a1+a5 |
+      // a2+a6, a3+a7), xor 1 adds those, the last add joins even and odd lanes.
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        uint64_t sum = acc[r];
+        sum = add2(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
+        sum = add2(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
+        float lo2, hi2;
+        f2unpack(sum, lo2, hi2);
+        const int64_t row = (int64_t(t) * 2 * R + 2 * r + ps) * kPanel + prow;
+        if (w == 0 && row < p.rows) p.out[row] = __fadd_rn(lo2, hi2);
+      }
+    }
+  }
+  if (!ok) atomicOr(&g_device_status, kStatusWaitTimeout);
+}
+
+// ---------------------------------------------------------------- host ----
+static int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int v = 0;
+    cached[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 148;
+  }
+  return cached[dev];
+}
+
+template <int R, int PMAX>
+static int set_smem_attr() {
+  static int done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_q1_multi<R, PMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         multi_smem_bytes<R>(kMaxKc));
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
+    done[dev] = 1;
+  }
+  return Q1_OK;
+}
+
+static int check_product(const char* who, int idx, const q1_product& pr) {
+  if (pr.rows < 1 || pr.rows > (int64_t(1) << 26) || pr.n < 128 || pr.n > (int64_t(1) << 24) || pr.n % 128)
+    return fail(Q1_ERR_ARG, "%s: product %d: bad shape rows=%lld n=%lld", who, idx, (long long)pr.rows,
+                (long long)pr.n);
+  if (!pr.packed || !pr.out || (!pr.x && (!pr.q || !pr.d)))
+    return fail(Q1_ERR_ARG, "%s: product %d: null pointer", who, idx);
+  auto mis = [](const void* p) { return p && reinterpret_cast<uintptr_t>(p) % 16 != 0; };
+  if (mis(pr.packed) || mis(pr.x) || mis(pr.q) || mis(pr.d) || mis(pr.out))
+    return fail(Q1_ERR_ARG, "%s: product %d: buffers must be 16-byte aligned", who, idx);
+  return Q1_OK;
+}
+
+template <int R, int PMAX>
+static int launch_multi(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+  if (int e = set_smem_attr<R, PMAX>()) return e;
+  MArgs<PMAX> a;
+  int64_t cost = 0;
+  int64_t total_tiles = 0;
+  int max_nbp = 8;
+  for (int j = 0; j < count; ++j) {
+    const Layout L = layout_of(prods[j].rows, prods[j].n);
+    MProd& p = a.p[j];
+    p.packed = static_cast<const uint8_t*>(prods[j].packed);
+    p.x = prods[j].x;
+    p.q = prods[j].q;
+    p.d = prods[j].d;
+    p.out = prods[j].out;
+    p.bits_bytes = L.bits_bytes;
+    p.rows = int(L.rows);
+    p.nb = int(L.nb);
+    p.nbp = int(L.nbp);
+    p.panels = int(L.panels);
+    p.tiles = int((L.panels + 2 * R - 1) / (2 * R));
+    p.cost_begin = cost;
+    cost += int64_t(p.tiles) * p.nbp;
+    total_tiles += p.tiles;
+    max_nbp = std::max(max_nbp, p.nbp);
+  }
+  a.total_cost = cost;
+  a.count = count;
+  a.kc = std::min(max_nbp, kMaxKc);
+  const int grid = int(std::min<int64_t>(total_tiles, 2 * num_sms()));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kMultiThreads);
+  cfg.dynamicSmemBytes = size_t(multi_smem_bytes<R>(a.kc));
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_multi<R, PMAX>, a), who);
+}
+
+// Rows per thread: the largest R whose tiles still give every CTA some work.
+template <int PMAX>
+static int dispatch(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+  int64_t panels = 0;
+  for (int j = 0; j < count; ++j) panels += (prods[j].rows + kPanel - 1) / kPanel;
+  const int64_t ctas = 2 * int64_t(num_sms());
+  if (panels >= 8 * ctas) return launch_multi<4, PMAX>(prods, count, s, who);
+  if (panels >= 4 * ctas) return launch_multi<2, PMAX>(prods, count, s, who);
+  return launch_multi<1, PMAX>(prods, count, s, who);
+}
+
+}  // namespace q1
+
+using namespace q1;
+
+extern "C" int q1_0_gemv(const void* packed, int64_t rows, int64_t n, const int8_t* q, const uint16_t* d,
+                         float* out, void* stream) {
+  q1_product p = {packed, rows, n, nullptr, q, d, out};
+  if (!q || !d) return fail(Q1_ERR_ARG, "q1_0_gemv: null pointer");
+  if (int e = check_product("q1_0_gemv", 0, p)) return e;
+  return dispatch<1>(&p, 1, static_cast<cudaStream_t>(stream), "q1_0_gemv launch");
+}
+
+extern "C" int q1_0_gemv_multi(const q1_product* products, int count, void* stream) {
+  if (!products || count < 1 || count > Q1_MAX_PRODUCTS)
+    return fail(Q1_ERR_ARG, "q1_0_gemv_multi: count=%d outside 1..%d (or null list)", count, Q1_MAX_PRODUCTS);
+  for (int j = 0; j < count; ++j)
+    if (int e = check_product("q1_0_gemv_multi", j, products[j])) return e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (count == 1) return dispatch<1>(products, count, s, "q1_0_gemv_multi launch");
+  if (count <= 8) return dispatch<8>(products, count, s, "q1_0_gemv_multi launch");
+  return dispatch<Q1_MAX_PRODUCTS>(products, count, s, "q1_0_gemv_multi launch");
+}
+
+extern "C" int q1_device_status(int clear) {
+  unsigned v = 0;
+  if (int e = cuda_status(cudaMemcpyFromSymbol(&v, g_device_status, sizeof v), "q1_device_status")) return e;
+  if (clear && v) {
+    const unsigned zero = 0;
+    if (int e = cuda_status(cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero), "q1_device_status")) return e;
+  }
+  return int(v);
+}

@@ -102,7 +102,10 @@ extern "C" int q1_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* p
   int64_t grid = (total + threads - 1) / threads;
   k_pack<<<dim3(unsigned(grid)), threads, 0, static_cast<cudaStream_t>(stream)>>>(
       blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales);
-  return cuda_status(cudaGetLastError(), "q1_0_pack launch");
+  if (int e = cuda_status(cudaGetLastError(), "q1_0_pack launch")) return e;
+  // The products may read packed weights before the kernel that precedes them
+  // on a stream has finished, so packing completes before this call returns.
+  return cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "q1_0_pack");
 }
 
 extern "C" int q1_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t* blocks, void* stream) {

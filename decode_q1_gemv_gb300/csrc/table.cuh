@@ -1,0 +1,150 @@
+// table.cuh -- activation-side constants of the Q1_0 x q8_0 row product, kept
+// in shared memory by the product kernels.
+//
+// For every 32-element sub-block g of the activation and lane l (elements
+// 4l..4l+3 of the sub-block):
+//   q'  = the four int8 quants with -128 replaced by 0 (one 32-bit word)
+//   A   = sum(q') + 128 * #(-128)      so that the lane sum is s = 2*M - A
+//         with M = sum(bit_i * q'_i) (an i8 negation of -128 stays -128)
+//   ci  = 0x4B400000 - 2^(pe-1) * A    dp4a accumulator init, pe = the lane's
+//                                      effective bit plane (common.cuh)
+// and for every sub-block and lane parity
+//   d'  = d1 * 2^(1-pe),  K = -d' * 1.5*2^23
+// with d1 the sub-block's fp16 scale widened to f32.  Then, for a weight word
+// masked to the lane's plane, dp4a(mask, q', ci) has the bits of the float
+// F = 1.5*2^23 + 2^(pe-1)*s, and fma(d', F, K) = d1*s exactly.
+//
+// Layout for a chunk of kc blocks (kc*4 sub-blocks), 80 bytes per sub-block:
+//   QC[g][w] (uint4)  = { q' lane 2w, q' lane 2w+1, ci lane 2w, ci lane 2w+1 }
+//   DK[g]    (float4) = { d' even lanes, d' odd lanes, K even, K odd }
+#pragma once
+
+#include "common.cuh"
+
+namespace q1 {
+
+__host__ __device__ constexpr int table_bytes(int kc) { return kc * 4 * (4 * 16 + 16); }
+__host__ __device__ constexpr int table_dk_offset(int kc) { return kc * 4 * 64; }
+
+__device__ __forceinline__ float pow2i(int e) {  // exact 2^e for -126 <= e <= 127
+  return __int_as_float((127 + e) << 23);
+}
+
+// Effective plane of lane parity `par` in sub-block k (see eff_plane).
+__device__ __forceinline__ int pe_of(int k, int par) { return (k == 0 && par == 0) ? 1 : 2 * k + par; }
+
+__device__ __forceinline__ void lane_consts(uint32_t word, int k, int par, uint32_t& qp, uint32_t& ci) {
+  const uint32_t m80 = __vcmpeq4(word, 0x80808080u);  // 0xff in bytes equal to -128
+  qp = word & ~m80;
+  const int cnt = __popc(m80) >> 3;
+  const int A = __dp4a(int(qp), 0x01010101, 0) + 128 * cnt;
+  ci = uint32_t(int(kMagicBits) - A * (1 << (pe_of(k, par) - 1)));
+}
+
+__device__ __forceinline__ void scale_consts(float d1, int k, int par, float& dprime, float& K) {
+  dprime = __fmul_rn(d1, pow2i(1 - pe_of(k, par)));
+  K = -__fmul_rn(dprime, kMagic);
+}
+
+// Table for blocks [blk0, blk0 + kcb) from a quantized activation (q int8 [n],
+// d fp16 [n/32]).  Sub-blocks past the activation's end get zero constants.
+static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, const uint16_t* __restrict__ d1,
+                                              int nb, int blk0, int kcb, unsigned char* table, int tid,
+                                              int nthreads, int kc) {
+  uint4* QC = reinterpret_cast<uint4*>(table);
+  float4* DK = reinterpret_cast<float4*>(table + table_dk_offset(kc));
+  const int nsub = nb * 4;
+  for (int t = tid; t < kcb * 16; t += nthreads) {
+    const int g = t >> 2, w = t & 3;
+    const int G = blk0 * 4 + g;
+    const int k = g & 3;
+    uint32_t qp[2], ci[2];
+#pragma unroll
+    for (int par = 0; par < 2; ++par) {
+      uint32_t word = 0u;
+      if (G < nsub) word = *reinterpret_cast<const uint32_t*>(q + int64_t(G) * kSub + 4 * (2 * w + par));
+      lane_consts(word, k, par, qp[par], ci[par]);
+    }
+    QC[g * 4 + w] = make_uint4(qp[0], qp[1], ci[0], ci[1]);
+  }
+  for (int g = tid; g < kcb * 4; g += nthreads) {
+    const int G = blk0 * 4 + g;
+    const int k = g & 3;
+    const float dv = (G < nsub) ? __half2float(__ushort_as_half(d1[G])) : 0.0f;
+    float de, dodd, ke, ko;
+    scale_consts(dv, k, 0, de, ke);
+    scale_consts(dv, k, 1, dodd, ko);
+    DK[g] = make_float4(de, dodd, ke, ko);
+  }
+}
+
+// Table for blocks [blk0, blk0 + kcb) from an f32 activation x [n], quantizing
+// it on the way exactly as q8_quantize_act does (per 32 values: amax, d =
+// amax/127, id = d ? 1/d : 0, q = roundf(x*id), scale fp16(d)).  One thread per
+// (sub-block, lane); the 8 threads of a sub-block are consecutive in a warp.
+// nthreads must be a multiple of 32 and every thread of the group must call.
+static __device__ __noinline__ void build_table_x(const float* __restrict__ x, int nb, int blk0, int kcb,
+                                              unsigned char* table, int tid, int nthreads, int kc) {
+  uint32_t* QCw = reinterpret_cast<uint32_t*>(table);
+  float* DKf = reinterpret_cast<float*>(table + table_dk_offset(kc));
+  const int nsub = nb * 4;
+  const int total = kcb * 4 * 8;
+  for (int base = 0; base < total; base += nthreads) {  // same trip count for every thread
+    const int t = base + tid;
+    const int g = t >> 3, l = t & 7;
+    const int G = blk0 * 4 + g;
+    const bool live = t < total && G < nsub;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) v = *reinterpret_cast<const float4*>(x + int64_t(G) * kSub + 4 * l);
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float dd = __fdiv_rn(amax, 127.0f);
+    const float id = (dd != 0.0f) ? __fdiv_rn(1.0f, dd) : 0.0f;
+    const uint32_t q0 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.x, id)))) & 0xffu;
+    const uint32_t q1 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.y, id)))) & 0xffu;
+    const uint32_t q2 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.z, id)))) & 0xffu;
+    const uint32_t q3 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.w, id)))) & 0xffu;
+    const uint32_t word = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+    const float d1 = __half2float(__float2half_rn(dd));
+    if (t < total) {
+      const int k = g & 3, par = l & 1, w = l >> 1;
+      uint32_t qp, ci;
+      lane_consts(word, k, par, qp, ci);
+      QCw[(g * 4 + w) * 4 + par] = qp;
+      QCw[(g * 4 + w) * 4 + 2 + par] = ci;
+      if (l < 2) {
+        float dprime, K;
+        scale_consts(G < nsub ? d1 : 0.0f, k, par, dprime, K);
+        DKf[g * 4 + par] = dprime;
+        DKf[g * 4 + 2 + par] = K;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ float half_of(const uint4& v, int i) {
+  const uint32_t w = word_of(v, i >> 1);
+  const uint16_t h = uint16_t((i & 1) ? (w >> 16) : (w & 0xffffu));
+  return __half2float(__ushort_as_half(h));
+}
+
+// One sub-block step for one row and one lane pair: masks the row's word W to
+// the two lanes' planes, forms the exact products d1*s for both lanes and
+// returns them as a float pair.
+__device__ __forceinline__ uint64_t subblock_products(uint32_t W, int k, const uint4& qc, uint64_t dpair,
+                                                      uint64_t kpair) {
+  uint32_t m0 = W & (0x01010101u << (2 * k));
+  const uint32_t m1 = W & (0x01010101u << (2 * k + 1));
+  if (k == 0) m0 <<= 1;  // plane 0 is used as plane 1 (byte values 0/2)
+  const uint32_t D0 = dp4a_us(m0, qc.x, qc.z);
+  const uint32_t D1 = dp4a_us(m1, qc.y, qc.w);
+  return fma2(dpair, f2pack(__uint_as_float(D0), __uint_as_float(D1)), kpair);
+}
+
+}  // namespace q1

@@ -1,12 +1,22 @@
 """The Llama-3-8B-shaped 1-bit decode matmul set on one GPU.
 
 One decode step = for each of the 225 products (32 layers x q, k, v, o, gate,
-up, down, then lm_head), in that order: quantize the product's f32 activation
-(q8_quantize_act), then run the Q1_0 matrix-vector product (q1_0_gemv).  All
-weights are packed once and stay resident; inputs are seeded synthetic data
-(``synth``).  The step can be captured once as a CUDA graph and replayed; the
-kernels use programmatic dependent launch, so inside the graph each product's
-weight streaming can begin while the previous kernel drains.
+up, down, then lm_head): q8_0-quantize the product's f32 activation and run
+the Q1_0 matrix-vector product.  All weights are packed once and stay
+resident; inputs are seeded synthetic data (``synth``), one activation vector
+per product.  Schedules of the same work:
+
+  "set"       one q1_0_gemv_multi launch for all 225 products (the products of
+              this workload are independent: each has its own input vector)
+  "grouped"   the launches a real decode step's data dependencies allow: per
+              layer {q, k, v}, {o}, {gate, up}, {down}, then {lm_head}: 129
+              dependent q1_0_gemv_multi launches
+  "decode"    one launch per product in decode order: 225 dependent launches
+  "separate"  q8_quantize_act then q1_0_gemv per product: 450 launches
+
+Every schedule can be captured once as a CUDA graph and replayed; the kernels
+use programmatic dependent launch, so each launch's weight streaming begins
+while the previous kernel drains.
 """
 from __future__ import annotations
 
@@ -84,11 +94,56 @@ class DecodeSet:
         _, rows, n = self.shapes[i]
         return self.packed[self.offsets[i]:self.offsets[i] + binding.packed_bytes(rows, n)]
 
-    def step(self, stream=None):
-        """Enqueue one decode step (quantize + product for every matmul)."""
-        for i, (_, rows, n) in enumerate(self.shapes):
-            binding.quantize(self.x[i], self.q[i], self.d[i], stream=stream)
-            binding.gemv(self.packed_view(i), rows, n, self.q[i], self.d[i], self.out[i], stream=stream)
+    SCHEDULES = ("set", "grouped", "decode", "separate")
+
+    def _item(self, i, fused=True):
+        _, rows, n = self.shapes[i]
+        if fused:
+            return (self.packed_view(i), rows, n, self.x[i], None, None, self.out[i])
+        return (self.packed_view(i), rows, n, None, self.q[i], self.d[i], self.out[i])
+
+    def groups(self, schedule: str):
+        """Lists of product indices, one list per launch, in launch order."""
+        idx = list(range(len(self.shapes)))
+        if schedule == "set":
+            return [idx]
+        if schedule == "decode":
+            return [[i] for i in idx]
+        if schedule == "grouped":
+            out, i = [], 0
+            names = [name.split(".")[-1] for name, _, _ in self.shapes]
+            while i < len(idx):
+                nm = names[i]
+                if nm == "q" and names[i + 1:i + 3] == ["k", "v"]:
+                    out.append([i, i + 1, i + 2])
+                    i += 3
+                elif nm == "gate" and i + 1 < len(idx) and names[i + 1] == "up":
+                    out.append([i, i + 1])
+                    i += 2
+                else:
+                    out.append([i])
+                    i += 1
+            return out
+        raise ValueError(schedule)
+
+    def _arrays(self, schedule):
+        key = "_arr_" + schedule
+        if not hasattr(self, key):
+            setattr(self, key, [binding.product_array([self._item(i) for i in g]) for g in self.groups(schedule)])
+        return getattr(self, key)
+
+    def launches(self, schedule: str) -> int:
+        return 2 * len(self.shapes) if schedule == "separate" else len(self.groups(schedule))
+
+    def step(self, stream=None, schedule: str = "set"):
+        """Enqueue one decode step with the given schedule."""
+        if schedule == "separate":
+            for i, (_, rows, n) in enumerate(self.shapes):
+                binding.quantize(self.x[i], self.q[i], self.d[i], stream=stream)
+                binding.gemv(self.packed_view(i), rows, n, self.q[i], self.d[i], self.out[i], stream=stream)
+            return
+        for arr in self._arrays(schedule):
+            binding.gemv_multi(array=arr, stream=stream)
 
     def products(self, stream=None):
         """Enqueue the products alone (activations already quantized)."""
@@ -108,9 +163,9 @@ class DecodeSet:
         torch.cuda.synchronize(self.device)
         return g
 
-    def capture(self):
+    def capture(self, schedule: str = "set"):
         """Capture one step as a CUDA graph (after a warm-up on a side stream)."""
-        self.graph = self._capture(self.step)
+        self.graph = self._capture(lambda: self.step(schedule=schedule))
         return self.graph
 
     def capture_products(self):
@@ -122,9 +177,6 @@ class DecodeSet:
             self.capture()
         self.graph.replay()
 
-    @property
-    def launches_per_step(self) -> int:
-        return 2 * len(self.shapes)
 
     @property
     def activation_bytes(self) -> int:

@@ -66,6 +66,7 @@ int64_t q1_0_packed_bytes(int64_t rows, int64_t n);
  *            element j in byte 2 + j/8, bit j%8, 1 = +d0, 0 = -d0.
  *            Only 2-byte alignment is required for this pointer.
  *   packed : device, q1_0_packed_bytes(rows, n) bytes, written entirely.
+ * Synchronous: returns after `stream` has finished the packing (see q1_0_gemv).
  * Errors: Q1_ERR_ARG for a bad shape or pointer; Q1_ERR_CUDA on launch failure. */
 int q1_0_pack(const uint8_t *blocks, int64_t rows, int64_t n, void *packed, void *stream);
 
@@ -90,11 +91,39 @@ int q8_quantize_act(const float *x, int64_t nvec, int64_t n, int8_t *q, uint16_t
  *   q, d   : device q8_0 activation: int8 [n], fp16 bits [n/32] (any quants,
  *            including -128).
  *   out    : device f32 [rows].
- * Launch uses programmatic dependent launch: the kernel's weight streaming may
- * start while the previous kernel on `stream` finishes; it reads q and d only
- * after that kernel's writes are visible. */
+ * Launch uses programmatic dependent launch: the kernel starts streaming
+ * `packed` while the preceding kernel on `stream` is still running, and reads
+ * q and d only after that kernel's writes are visible.  So `packed` must not be
+ * written by the kernel immediately preceding this call on the stream
+ * (q1_0_pack and host copies are always complete before it). */
 int q1_0_gemv(const void *packed, int64_t rows, int64_t n, const int8_t *q, const uint16_t *d,
               float *out, void *stream);
+
+/* One product of a multi-product call: out = the matrix-vector product of the
+ * packed rows x n matrix with one activation vector. */
+typedef struct q1_product {
+  const void *packed;     /* device, from q1_0_pack(rows, n)                         */
+  int64_t rows, n;        /* matrix shape                                            */
+  const float *x;         /* device f32 [n]: activation, quantized inside the kernel
+                             exactly as q8_quantize_act would; or NULL              */
+  const int8_t *q;        /* used when x is NULL: device int8 [n] q8_0 quants        */
+  const uint16_t *d;      /* used when x is NULL: device fp16 bits [n/32] scales    */
+  float *out;             /* device f32 [rows]                                       */
+} q1_product;
+
+#define Q1_MAX_PRODUCTS 256
+
+/* Several independent matrix-vector products in ONE launch (the pages' own
+ * next step, "batched submissions ... one wait per group" in "Advantages and
+ * efficiency"; e.g. the q/k/v or gate/up products of a layer, or a whole set of
+ * independent products).  Each out_j is bit-identical to q8_quantize_act(x_j)
+ * (when x_j is given) followed by q1_0_gemv.  Products may differ in shape.
+ *   products : HOST array of `count` descriptors (1 <= count <= Q1_MAX_PRODUCTS),
+ *              read during the call only.
+ * Outputs must not overlap each other or any input.  Same launch behaviour as
+ * q1_0_gemv (programmatic dependent launch; `packed` may be read before the
+ * preceding kernel on `stream` has finished). */
+int q1_0_gemv_multi(const q1_product *products, int count, void *stream);
 
 /* Small-batch product: the matrix-vector product for each of nvec activation
  * vectors sharing one pass over the weights (1 <= nvec <= 64).
@@ -103,6 +132,14 @@ int q1_0_gemv(const void *packed, int64_t rows, int64_t n, const int8_t *q, cons
  * out[v][r] is bit-identical to q1_0_gemv on vector v. */
 int q1_0_gemm_small(const void *packed, int64_t rows, int64_t n, int64_t nvec, const int8_t *q,
                     const uint16_t *d, float *out, void *stream);
+
+/* Device status word of the library's kernels on the current device.  A
+ * kernel whose bounded internal wait gives up (it never should: every wait is
+ * for work the same kernel issued) sets bit 0 instead of hanging, and skips
+ * its remaining output.  Synchronous: copies the word to the host.
+ *   clear : nonzero resets the word to 0 after reading it.
+ * Returns the status flags (0 = no event) or a negative Q1_ERR_CUDA. */
+int q1_device_status(int clear);
 
 /* On-card self-check ("How it is verified": verify_q1_0 compares every kernel
  * and shape with the CPU bits, including -128 quants and a layer-shaped regime

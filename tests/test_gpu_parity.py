@@ -237,31 +237,90 @@ def test_batched_full_size_sampled(rows, n, nvec, scale):
     bits_equal(out[vec, idx], want)
 
 
-# ------------------------------------------------------- decode set (graph) --
-def test_decode_set_graph_sampled():
-    """The full 225-product Llama-3-8B-shaped decode set, run exactly as the
-    benchmark runs it (one CUDA graph, programmatic dependent launch), with 40
-    sampled rows of every product compared against the oracle."""
-    from decode_q1_gemv_gb300.decode_set import DecodeSet
-    ds = DecodeSet(seed=3)
-    ds.capture()
-    for o in ds.out:
-        o.fill_(float("nan"))
-    ds.replay()
-    ds.replay()
+# ----------------------------------------------------- multi-product call --
+def test_gemv_multi_mixed_products():
+    """One q1_0_gemv_multi launch over products of different shapes, some with
+    f32 activations (quantized in the kernel) and some already quantized."""
+    shapes = [(1, 128), (33, 384), (300, 1024), (4096, 4096), (1024, 4096), (64, 14336), (7, 17408), (2000, 1152)]
+    items, want = [], []
+    for i, (rows, n) in enumerate(shapes):
+        rng = synth.rng_for(110, i)
+        blocks = synth.weight_blocks(rng, rows, n, "lognormal" if i % 2 else "halfnormal")
+        packed = binding.pack(dev(blocks), rows, n)
+        out = torch.full((rows,), float("nan"), device="cuda")
+        if i % 3 == 2:
+            q, d = synth.raw_quants(rng, 1, n, scale="lognormal", m128_frac=0.03)
+            items.append((packed, rows, n, None, dev(q[0]), dev(d[0].view(np.int16)), out))
+        else:
+            x = synth.activations(rng, 1, n, outliers=0.01)
+            q, d = oracle.q8_quantize(x)
+            items.append((packed, rows, n, dev(x[0]), None, None, out))
+        want.append(oracle.gemv(blocks, q[0], d[0]))
+    binding.gemv_multi(items)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(7)
-    for i, (name, rows, n) in enumerate(ds.shapes):
-        if i % 7 not in (0, 2, 4, 6) and i != len(ds.shapes) - 1:
-            continue  # every q, v, gate, down and lm_head
+    for (packed, rows, n, x, q, d, out), w in zip(items, want):
+        bits_equal(out.cpu().numpy(), w)
+
+
+def test_gemv_multi_fused_equals_quantize_then_gemv():
+    rows, n = 4096, 14336
+    rng = synth.rng_for(111)
+    blocks = synth.weight_blocks(rng, rows, n)
+    x = dev(synth.activations(rng, 1, n, outliers=0.01)[0])
+    packed = binding.pack(dev(blocks), rows, n)
+    q, d = binding.quantize(x)
+    a = binding.gemv(packed, rows, n, q, d)
+    b = torch.empty(rows, device="cuda")
+    binding.gemv_multi([(packed, rows, n, x, None, None, b)])
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_gemv_multi_rejects_bad_lists():
+    rows, n = 32, 128
+    packed = torch.empty(binding.packed_bytes(rows, n), dtype=torch.uint8, device="cuda")
+    out = torch.empty(rows, device="cuda")
+    with pytest.raises(ValueError):
+        binding.product_array([(packed, rows, n, None, None, None, out)])
+    arr = (binding.Product * 0)()
+    with pytest.raises(binding.Q1Error):
+        binding.gemv_multi(array=arr)
+
+
+# ------------------------------------------------------- decode set (graph) --
+@pytest.fixture(scope="module")
+def decode_set():
+    from decode_q1_gemv_gb300.decode_set import DecodeSet
+    return DecodeSet(seed=3)
+
+
+@pytest.mark.parametrize("schedule", ["set", "grouped", "decode", "separate"])
+def test_decode_set_graph_sampled(decode_set, schedule):
+    """The full 225-product Llama-3-8B-shaped decode set, run exactly as the
+    benchmark runs it (one CUDA graph per schedule, programmatic dependent
+    launch), with 24 sampled rows of products of every shape compared against
+    the oracle."""
+    ds = decode_set
+    g = ds.capture(schedule)
+    ds.out_all.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(len(schedule))
+    picks = [0, 1, 2, 3, 4, 5, 6, 7 * 17 + 1, 7 * 31 + 4, 7 * 31 + 6, len(ds.shapes) - 1]
+    for i in picks:
+        name, rows, n = ds.shapes[i]
         blocks = ds.host_blocks(i)
         x = ds.host_x(i)
         want_q, want_d = oracle.q8_quantize(x[None, :])
-        assert np.array_equal(ds.q[i].cpu().numpy(), want_q[0]), name
-        assert np.array_equal(ds.d[i].cpu().numpy().view(np.uint16), want_d[0]), name
-        idx = rng.integers(0, rows, size=40)
+        idx = rng.integers(0, rows, size=24)
+        idx[:2] = [0, rows - 1]
         want = oracle.rows_sampled(blocks, idx, want_q[0], want_d[0])
-        bits_equal(ds.out[i].cpu().numpy()[idx], want)
+        got = ds.out[i].cpu().numpy()
+        assert not np.any(np.isnan(got)), name
+        bits_equal(got[idx], want)
+        if schedule == "separate":
+            assert np.array_equal(ds.q[i].cpu().numpy(), want_q[0]), name
+            assert np.array_equal(ds.d[i].cpu().numpy().view(np.uint16), want_d[0]), name
 
 
 # ---------------------------------------------------- edge and error cases --
@@ -307,3 +366,8 @@ def test_bad_arguments_raise():
         binding.gemv(packed, 64, 256, q.float(), d)
     with pytest.raises(ValueError):
         binding.gemv(packed, 64, 256, q.cpu(), d)
+
+
+def test_device_status_clean_after_suite():
+    """No kernel gave up a bounded wait during the parity runs."""
+    assert binding.device_status(clear=True) == 0
