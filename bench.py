@@ -59,7 +59,8 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for rel in ("decode_q1_gemv_gb300/csrc/gemv.cu", "decode_q1_gemv_gb300/csrc/common.cuh"):
+    for rel in ("decode_q1_gemv_gb300/csrc/multi.cu", "decode_q1_gemv_gb300/csrc/table.cuh",
+                "decode_q1_gemv_gb300/csrc/common.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -139,30 +140,29 @@ class ClockSampler:
 # ---------------------------------------------------------- CPU baseline --
 def cpu_oracle_sample(layers: int, budget_s: float, threads: int, seed: int = 3):
     """Time the threaded CPU oracle (q8_0 quantization + product) on the first
-    products of the decode set until about `budget_s` of work, returns
-    (weight GB/s, description, threads)."""
-    import numpy as np
-
+    `layers` layers of the decode set, repeated until about `budget_s` seconds
+    of work; returns (weight GB/s, description, threads)."""
     import oracle
     from decode_q1_gemv_gb300 import synth
 
     oracle.build()
-    shapes = synth.decode_set_shapes()
-    done_bytes, elapsed, count = 0, 0.0, 0
-    for i, (name, rows, n) in enumerate(shapes[:7 * layers]):
-        blocks = synth.weight_blocks(synth.rng_for(seed, i, 0), rows, n)
-        x = synth.activations(synth.rng_for(seed, i, 1), 1, n)
-        t0 = time.perf_counter()
-        q, d = oracle.q8_quantize(x)
-        out, _ = oracle.gemv_threaded(blocks, q[0], d[0], threads)
-        elapsed += time.perf_counter() - t0
-        done_bytes += rows * n * 18 // 128
-        count += 1
-        if elapsed >= budget_s:
-            break
+    shapes = synth.decode_set_shapes()[:7 * layers]
+    inputs = [(synth.weight_blocks(synth.rng_for(seed, i, 0), rows, n), synth.activations(synth.rng_for(seed, i, 1), 1, n))
+              for i, (_, rows, n) in enumerate(shapes)]
+    pass_bytes = sum(rows * n * 18 // 128 for _, rows, n in shapes)
+    done_bytes, elapsed, passes = 0, 0.0, 0
+    while elapsed < budget_s:
+        for blocks, x in inputs:
+            t0 = time.perf_counter()
+            q, d = oracle.q8_quantize(x)
+            oracle.gemv_threaded(blocks, q[0], d[0], threads)
+            elapsed += time.perf_counter() - t0
+        done_bytes += pass_bytes
+        passes += 1
     gbs = done_bytes / elapsed / 1e9
-    desc = (f"first {count} products of the decode set ({done_bytes / 1e6:.1f} MB of weights), "
-            f"q8_0 quantization + threaded oracle product, {threads} threads, {elapsed:.1f} s")
+    desc = (f"first {layers} layers of the decode set ({len(shapes)} products, {pass_bytes / 1e6:.1f} MB of "
+            f"weights) x {passes} passes: q8_0 quantization + threaded oracle product, {threads} threads, "
+            f"{elapsed:.1f} s")
     return gbs, desc, threads
 
 
@@ -212,6 +212,16 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------- ours -----
+def max_over_ranks(v: float, world: int, dist=None, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (the rank's own value at N=1)."""
+    if world == 1:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _time_graph(graph, reps, stream):
     import torch
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -239,8 +249,13 @@ def run_ours(args):
     from decode_q1_gemv_gb300.decode_set import DecodeSet
 
     binding.load()
-    ds = DecodeSet(seed=3, device=str(dev))
-    graphs = {sch: ds._capture(lambda sch=sch: ds.step(schedule=sch)) for sch in DecodeSet.SCHEDULES}
+    from decode_q1_gemv_gb300 import synth
+    shapes = synth.decode_set_shapes()
+    if args.layers < synth.LLAMA3_8B_LAYERS:
+        shapes = shapes[:7 * args.layers]  # a smaller set (profiling runs); the lm_head is dropped too
+    ds = DecodeSet(seed=3, device=str(dev), shapes=shapes)
+    schedules = ["set"] + [s for s in args.schedules.split(",") if s and s != "set"]
+    graphs = {sch: ds._capture(lambda sch=sch: ds.step(schedule=sch)) for sch in schedules}
     graph = graphs["set"]
     stream = torch.cuda.current_stream(dev)
 
@@ -248,12 +263,8 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def reduce_max(v: float) -> float:
+        return max_over_ranks(v, world, dist, dev)
 
     for _ in range(max(args.warmup, 3)):
         graph.replay()
@@ -278,16 +289,16 @@ def run_ours(args):
             graph.replay()
         torch.cuda.synchronize()
     sampler.stop()
-    step_ms = max_over_ranks(step_ms)
+    step_ms = reduce_max(step_ms)
 
     # ---- the same work under the other schedules (decode-order dependencies)
     sched_us = {"set": round(step_ms * 1e3, 2)}
-    for sch in ("grouped", "decode", "separate"):
+    for sch in schedules[1:]:
         g = graphs[sch]
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        sched_us[sch] = round(max_over_ranks(_time_graph(g, max(args.steps // 4, 10), stream)) * 1e3, 2)
+        sched_us[sch] = round(reduce_max(_time_graph(g, max(args.steps // 4, 10), stream)) * 1e3, 2)
 
     # ---- end to end through the public API with host buffers
     host_x = ds.x_all.cpu().pin_memory()
@@ -308,7 +319,7 @@ def run_ours(args):
     x1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps)
+    e2e_ms = reduce_max(x0.elapsed_time(x1) / args.steps)
 
     wb = ds.weight_bytes
     peak, peak_kind = measured_peaks()
@@ -320,7 +331,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, desc, cores = cpu_oracle_sample(layers=32, budget_s=args.cpu_budget, threads=os.cpu_count() or 1)
+        gbs, desc, cores = cpu_oracle_sample(layers=4, budget_s=args.cpu_budget, threads=os.cpu_count() or 1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:
@@ -328,14 +339,15 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "products": len(ds.shapes), "batch": 1, "weight_bytes": wb,
+            "config": {"workload": WORKLOAD if args.layers >= 32 else f"first {args.layers} layers of the set",
+                       "products": len(ds.shapes), "batch": 1, "weight_bytes": wb,
                        "schedule": "set: one q1_0_gemv_multi launch, q8_0 quantization fused",
                        "l2": "inputs larger than L2: each step streams 1.055 GB of weights",
                        "parallelism": f"replicas x{world}"},
             "us_per_set": round(step_ms * 1e3, 2),
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "us_per_set_by_schedule": sched_us,
-            "launches_by_schedule": {sch: ds.launches(sch) for sch in DecodeSet.SCHEDULES},
+            "launches_by_schedule": {sch: ds.launches(sch) for sch in schedules},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "kernel": "k_q1_multi (q1_0_gemv_multi, 225 products)", "launches_per_step": 1,
@@ -361,6 +373,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU-oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=32, help="layers of the decode set (32 = full set with lm_head)")
+    ap.add_argument("--schedules", default="grouped,decode,separate",
+                    help="schedules timed besides 'set' (comma list; empty for none)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

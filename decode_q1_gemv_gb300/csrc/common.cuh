@@ -15,22 +15,25 @@ namespace q1 {
 constexpr int kBlock = 128;       // weights per Q1_0 block
 constexpr int kBlockBytes = 18;   // fp16 scale + 16 sign bytes
 constexpr int kSub = 32;          // activation values per q8_0 scale
-constexpr int kPanel = 32;        // rows per packed panel
-constexpr int kBlockPad = 8;      // blocks per row are padded to a multiple of 8
+constexpr int kPanel = 32;        // rows per panel
+constexpr int kGroup = 8;         // panels per panel group (256 rows)
+constexpr int kBlockPad = 4;      // blocks per row are padded to a multiple of 4 (a quad)
 
-// Packed device layout (q1_0_pack writes it, the GEMV kernels read it):
+// Packed device layout (q1_0_pack writes it, the product kernels read it):
 //
-//   rows_pad = round_up(rows, 32), nbp = round_up(n/128, 8), panels = rows_pad/32
+//   rows_pad = round_up(rows, 256), nbp = round_up(n/128, 4), nq = nbp/4,
+//   panels = rows_pad/32, groups = rows_pad/256.
 //
-//   bits   : u32 words, at byte 0.  For panel p, block b, panel row r and lane
-//            pair w (0..3) the word sits at
-//              (((p * nbp/4 + b/4) * 32 + r) * 4 + w) * 4 + b%4
-//            i.e. a 16-byte vector holds one (row, lane pair)'s words for four
-//            consecutive blocks, and a warp's 8 rows x 4 lane pairs read 512
-//            contiguous bytes.
-//   scales : fp16 block scales d0, after the bits (byte offset rows_pad*nbp*16).
-//            Half index ((p * nbp/8 + b/8) * 32 + r) * 8 + b%8: one 16-byte
-//            vector = one row's scales for eight consecutive blocks.
+//   bits   : u32 words at byte 0.  For panel group gi, block quad qd (blocks
+//            4qd..4qd+3), panel pi within the group (0..7), panel row r (0..31),
+//            lane pair w (0..3) and block bq within the quad, the word sits at
+//              ((((gi*nq + qd)*8 + pi)*32 + r)*4 + w)*4 + bq
+//            so one quad of one panel is 2 KB, a warp's 8 rows x 4 lane pairs
+//            read 512 contiguous bytes, and the quad of 2, 4 or 8 aligned
+//            consecutive panels is one contiguous 4, 8 or 16 KB chunk.
+//   scales : fp16 block scales d0 after the bits (byte offset rows_pad*nbp*16),
+//            half index (((gi*nq + qd)*8 + pi)*32 + r)*4 + bq: 256 B per panel
+//            and quad, contiguous across the panels of a group in the same way.
 //
 // Within a word w of (row, block): bit 8*i + pl (i = 0..3, plane pl = 0..7)
 // is the sign bit of block element 32*(pl>>1) + 4*(2*w + (pl&1)) + i, i.e. lane
@@ -48,12 +51,28 @@ inline Layout layout_of(int64_t rows, int64_t n) {
   L.n = n;
   L.nb = n / kBlock;
   L.nbp = (L.nb + kBlockPad - 1) / kBlockPad * kBlockPad;
-  L.rows_pad = (rows + kPanel - 1) / kPanel * kPanel;
+  L.rows_pad = (rows + kPanel * kGroup - 1) / (kPanel * kGroup) * (kPanel * kGroup);
   L.panels = L.rows_pad / kPanel;
   L.bits_bytes = L.rows_pad * L.nbp * 16;
   L.scales_bytes = L.rows_pad * L.nbp * 2;
   L.total_bytes = L.bits_bytes + L.scales_bytes;
   return L;
+}
+
+// Word index of (panel p, block b, panel row r, lane pair w) and half index of
+// the scale of (panel p, block b, row r); p counts panels from the start.
+__host__ __device__ __forceinline__ int64_t bits_word_index(int64_t p, int64_t b, int r, int w, int64_t nbp) {
+  return ((((p / kGroup) * (nbp / 4) + b / 4) * kGroup + p % kGroup) * kPanel + r) * 16 + w * 4 + (b % 4);
+}
+__host__ __device__ __forceinline__ int64_t scale_index(int64_t p, int64_t b, int r, int64_t nbp) {
+  return ((((p / kGroup) * (nbp / 4) + b / 4) * kGroup + p % kGroup) * kPanel + r) * 4 + (b % 4);
+}
+// Byte offsets of the quad qd of panel p within the bits and scales regions.
+__host__ __device__ __forceinline__ int64_t quad_bits_offset(int64_t p, int64_t qd, int64_t nbp) {
+  return (((p / kGroup) * (nbp / 4) + qd) * kGroup + p % kGroup) * 2048;
+}
+__host__ __device__ __forceinline__ int64_t quad_scales_offset(int64_t p, int64_t qd, int64_t nbp) {
+  return (((p / kGroup) * (nbp / 4) + qd) * kGroup + p % kGroup) * 256;
 }
 
 // Plane (0..7) of lane l in sub-block k inside its lane pair's word.
@@ -155,21 +174,27 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 
 // Wait until the barrier's phase with parity `parity` has completed.  Bounded:
-// gives up after about `limit_ns` nanoseconds and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
-  uint32_t done = 0;
+// gives up after about `limit_ns` nanoseconds and returns false (the clock is
+// read only every 64 polls).
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
   asm volatile(
       "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
       : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-  if (done) return true;
+  return done != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer();
-  for (;;) {
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-    if (done) return true;
-    if (globaltimer() - t0 > limit_ns) return false;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 63) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, limit_ns);
 }
 
 // 1-D bulk copy global -> shared, completing on `bar` (both addresses 16-byte

@@ -16,7 +16,7 @@ constexpr int kThreads = 128;  // 4 warps; thread (row in panel, lane pair)
 
 struct ProdArgs {
   const uint4* bits;     // packed sign words, 16-byte vectors
-  const uint4* scales;   // packed fp16 block scales, 16-byte vectors (8 each)
+  const uint16_t* scales;  // packed fp16 block scales
   const int8_t* q;       // activation quants [nvec][n]
   const uint16_t* d1;    // activation scales [nvec][n/32]
   float* out;            // [nvec][rows]
@@ -41,15 +41,13 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
   const int p0 = pg * R;
   const int v0 = vg * V;
 
-  pdl_launch_dependents();
   pdl_wait();
 
-  const int64_t nq4 = a.nbp / 4, nq8 = a.nbp / 8;
-  uint64_t acc[R][V];
+  uint64_t acc[V][R];
 #pragma unroll
-  for (int j = 0; j < R; ++j)
+  for (int v = 0; v < V; ++v)
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[j][v] = 0ull;  // both lanes +0
+    for (int j = 0; j < R; ++j) acc[v][j] = 0ull;  // both lanes +0
 
   for (int blk0 = 0; blk0 < a.nbp; blk0 += a.kc) {
     const int kcb = min(a.kc, a.nbp - blk0);
@@ -63,60 +61,30 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
     }
     __syncthreads();
 
-    for (int b = blk0; b < blk0 + kcb; b += 8) {
-      uint4 sc[R], wa[R], wb[R];
+    for (int b = blk0; b < blk0 + kcb; b += 4) {
+      uint4 wv[R];
+      uint2 sc[R];
 #pragma unroll
       for (int j = 0; j < R; ++j) {
         const int64_t p = p0 + j;
         if (p < a.panels) {
-          sc[j] = ldg_stream(a.scales + (p * nq8 + b / 8) * kPanel + prow);
-          wa[j] = ldg_stream(a.bits + ((p * nq4 + b / 4) * kPanel + prow) * 4 + w);
-          wb[j] = ldg_stream(a.bits + ((p * nq4 + b / 4 + 1) * kPanel + prow) * 4 + w);
+          wv[j] = ldg_stream(a.bits + bits_word_index(p, b, prow, w, a.nbp) / 4);
+          sc[j] = *reinterpret_cast<const uint2*>(a.scales + scale_index(p, b, prow, a.nbp));
         } else {
-          sc[j] = wa[j] = wb[j] = make_uint4(0u, 0u, 0u, 0u);
+          wv[j] = make_uint4(0u, 0u, 0u, 0u);
+          sc[j] = make_uint2(0u, 0u);
         }
       }
 #pragma unroll
-      for (int bb = 0; bb < 8; ++bb) {
-        uint64_t ab[R][V];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int g = (b - blk0 + bb) * 4 + k;
-          uint32_t m0[R], m1[R];
-#pragma unroll
-          for (int j = 0; j < R; ++j) {
-            const uint32_t W = word_of(bb < 4 ? wa[j] : wb[j], bb & 3);
-            m0[j] = W & (0x01010101u << (2 * k));
-            m1[j] = W & (0x01010101u << (2 * k + 1));
-            if (k == 0) m0[j] <<= 1;  // plane 0 -> byte values 0/2
-          }
-#pragma unroll
-          for (int v = 0; v < V; ++v) {
-            const unsigned char* t = smem + v * tb;
-            const uint4 qc = reinterpret_cast<const uint4*>(t)[g * 4 + w];
-            const float4 dk = reinterpret_cast<const float4*>(t + table_dk_offset(a.kc))[g];
-            const uint64_t dpair = f2pack(dk.x, dk.y);
-            const uint64_t kpair = f2pack(dk.z, dk.w);
-#pragma unroll
-            for (int j = 0; j < R; ++j) {
-              const uint32_t D0 = dp4a_us(m0[j], qc.x, qc.z);
-              const uint32_t D1 = dp4a_us(m1[j], qc.y, qc.w);
-              const uint64_t pr = fma2(dpair, f2pack(__uint_as_float(D0), __uint_as_float(D1)), kpair);
-              ab[j][v] = (k == 0) ? pr : add2(ab[j][v], pr);
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-          const float d0 = half_of(sc[j], bb);
-          const uint64_t d0p = f2pack(d0, d0);
-#pragma unroll
-          for (int v = 0; v < V; ++v) acc[j][v] = fma2(d0p, ab[j][v], acc[j][v]);
-        }
+      for (int v = 0; v < V; ++v) {
+        const unsigned char* t = smem + v * tb;
+        quad_all<R>(wv, sc, reinterpret_cast<const uint4*>(t) + (b - blk0) * 16,
+                    reinterpret_cast<const float4*>(t + table_dk_offset(a.kc)) + (b - blk0) * 4, w, acc[v]);
       }
     }
   }
 
+  pdl_launch_dependents();
   // Horizontal sum: lane pair w holds (a_2w, a_2w+1).  xor 2 pairs w with w+2
   // (a0+a4, a1+a5 | a2+a6, a3+a7); xor 1 then adds those; the final add joins
   // the even-lane and odd-lane halves.
@@ -125,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
     const int64_t row = int64_t(p0 + j) * kPanel + prow;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      uint64_t s = acc[j][v];
+      uint64_t s = acc[v][j];
       s = add2(s, __shfl_xor_sync(0xffffffffu, s, 2));
       s = add2(s, __shfl_xor_sync(0xffffffffu, s, 1));
       float lo, hi;
@@ -176,7 +144,7 @@ static ProdArgs make_args(const void* packed, int64_t rows, int64_t n, int64_t n
   Layout L = layout_of(rows, n);
   ProdArgs a = {};
   a.bits = static_cast<const uint4*>(packed);
-  a.scales = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(packed) + L.bits_bytes);
+  a.scales = reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(packed) + L.bits_bytes);
   a.q = q;
   a.d1 = d;
   a.out = out;

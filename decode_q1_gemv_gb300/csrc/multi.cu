@@ -11,9 +11,10 @@
 //
 // Structure.  A CTA is one producer warp and eight consumer warps.  The
 // producer streams packed weights HBM -> shared memory with 1-D bulk copies
-// into a ring of stages (mbarrier full/empty pairs).  A stage is one octet of
-// blocks (8 x 128 weights per row) for the CTA's current tile of 2R panels
-// (64R rows): 4 KB of sign words and 512 B of scales per panel.  Consumer
+// into a ring of stages (mbarrier full/empty pairs).  A stage is one quad of
+// blocks (4 x 128 weights per row) for the CTA's current tile of 2R panels
+// (64R rows, two panels side by side): 2 KB of sign words and 256 B of scales
+// per panel, two contiguous copies thanks to the packed layout.  Consumer
 // thread (row, lane pair) handles R rows of a tile.  CTAs are persistent: the
 // products' tiles are split into contiguous ranges of equal weight bytes, one
 // range per CTA, and the producer runs ahead across tile and product
@@ -33,9 +34,9 @@ __device__ unsigned g_device_status = 0u;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kMultiThreads = kConsumers + 32;
-constexpr int kPanelBits = 4096;   // one panel x one octet: 32 rows x 8 blocks x 16 B
-constexpr int kPanelScales = 512;  // 32 rows x 8 blocks x 2 B
-constexpr int kPanelStage = kPanelBits + kPanelScales;
+constexpr int kSlots = kConsumerWarps / 4;  // panels computed side by side (4 warps = 32 rows each)
+constexpr int kQuadBits = 2048;    // one panel x one quad of blocks: 32 rows x 4 blocks x 16 B
+constexpr int kQuadScales = 256;   // 32 rows x 4 blocks x 2 B
 constexpr int kConsumerBarrier = 1;
 constexpr int kMaxKc = 128;        // blocks of activation held in the table (n <= 16384 in one chunk)
 
@@ -55,20 +56,19 @@ struct MArgs {
   MProd p[PMAX];
   int64_t total_cost;
   int count;
-  int kc;                // table chunk in blocks (multiple of 8)
+  int kc;                // table chunk in blocks (multiple of 4)
 };
 
-template <int R> struct Ring;
-template <> struct Ring<1> { static constexpr int stages = 6; };
-template <> struct Ring<2> { static constexpr int stages = 3; };
-template <> struct Ring<4> { static constexpr int stages = 2; };
-
+// Ring of stages: a stage is one quad of blocks for the tile's 2R panels; about
+// 74 KB of weights in flight per CTA whatever R is.
 template <int R>
-__host__ __device__ constexpr int stage_bytes() { return 2 * R * kPanelStage; }
+__host__ __device__ constexpr int ring_stages() { return 16 / R; }
+template <int R>
+__host__ __device__ constexpr int stage_bytes() { return kSlots * R * (kQuadBits + kQuadScales); }
 
 template <int R>
 __host__ __device__ constexpr int multi_smem_bytes(int kc) {
-  return Ring<R>::stages * stage_bytes<R>() + table_bytes(kc) + 2 * Ring<R>::stages * 8;
+  return ring_stages<R>() * stage_bytes<R>() + table_bytes(kc) + 2 * ring_stages<R>() * 8;
 }
 
 // Tiles [t_lo, t_hi) of product p that fall in this CTA's cost range.
@@ -85,8 +85,9 @@ __device__ __forceinline__ void tile_range(const MProd& p, int64_t lo, int64_t h
 template <int R, int PMAX>
 __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_constant__ MArgs<PMAX> a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int S = Ring<R>::stages;
+  constexpr int S = ring_stages<R>();
   constexpr int SB = stage_bytes<R>();
+  constexpr int TB = kSlots * R * kQuadBits;  // bits part of a stage
   unsigned char* table = smem + S * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(table + table_bytes(a.kc));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,29 +109,25 @@ __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_cons
       bool ok = true;
       int it = 0;
       for (int j = 0; j < a.count && ok; ++j) {
-        const MProd& p = a.p[j];
         int t_lo, t_hi;
-        tile_range(p, lo, hi, t_lo, t_hi);
-        const int octets = p.nbp / 8;
+        tile_range(a.p[j], lo, hi, t_lo, t_hi);
+        const uint8_t* bits = a.p[j].packed;
+        const uint8_t* scales = bits + a.p[j].bits_bytes;
+        const int nbp = a.p[j].nbp;
+        const int quads = nbp / 4;
         for (int t = t_lo; t < t_hi && ok; ++t) {
-          const int p0 = t * 2 * R;
-          const int np = min(2 * R, p.panels - p0);
-          for (int oct = 0; oct < octets; ++oct, ++it) {
+          const int64_t p0 = int64_t(t) * kSlots * R;  // aligned panels inside one panel group
+          for (int qd = 0; qd < quads; ++qd, ++it) {
             const int s = it % S;
             if (it >= S && !mbar_wait(smem_addr(&bars[S + s]), uint32_t(it / S - 1) & 1u)) {
               ok = false;
               break;
             }
             const uint32_t full = smem_addr(&bars[s]);
-            mbar_arrive_expect_tx(full, uint32_t(np * kPanelStage));
+            mbar_arrive_expect_tx(full, uint32_t(SB));
             const uint32_t dst = smem_addr(smem + s * SB);
-            for (int u = 0; u < np; ++u) {
-              const int64_t pp = p0 + u;
-              bulk_g2s(dst + u * kPanelBits, p.packed + pp * int64_t(p.nbp) * 512 + int64_t(oct) * kPanelBits,
-                       kPanelBits, full);
-              bulk_g2s(dst + 2 * R * kPanelBits + u * kPanelScales,
-                       p.packed + p.bits_bytes + (pp * (p.nbp / 8) + oct) * kPanelScales, kPanelScales, full);
-            }
+            bulk_g2s(dst, bits + quad_bits_offset(p0, qd, nbp), TB, full);
+            bulk_g2s(dst + TB, scales + quad_scales_offset(p0, qd, nbp), kSlots * R * kQuadScales, full);
           }
         }
       }
@@ -141,15 +138,16 @@ __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_cons
 
   // ------------------------------- consumers ------------------------------
   const int tid = threadIdx.x;
-  const int ps = warp >> 2;                       // panel parity within the tile
+  const int ps = warp >> 2;                       // panel slot within the tile
   const int prow = (warp & 3) * 8 + (lane >> 2);  // row within the panel
   const int w = lane & 3;                         // lane pair 2w, 2w+1
   const uint4* QC = reinterpret_cast<const uint4*>(table);
   const float4* DK = reinterpret_cast<const float4*>(table + table_dk_offset(a.kc));
+  const int kc = a.kc;
 
   pdl_wait();  // the activations may be written by the preceding kernel
 
-  // Last tile of this CTA (to signal dependents when it starts).
+  // Last tile of this CTA (dependents are signalled when it starts).
   int last_j = -1, last_t = -1;
   for (int j = 0; j < a.count; ++j) {
     int t_lo, t_hi;
@@ -164,16 +162,20 @@ __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_cons
   bool ok = true;
   int it = 0;
   for (int j = 0; j < a.count && ok; ++j) {
-    const MProd& p = a.p[j];
     int t_lo, t_hi;
-    tile_range(p, lo, hi, t_lo, t_hi);
+    tile_range(a.p[j], lo, hi, t_lo, t_hi);
     if (t_lo >= t_hi) continue;
-    const int octets = p.nbp / 8;
-    const bool one_chunk = p.nbp <= a.kc;
+    const float* px = a.p[j].x;
+    const int8_t* pq = a.p[j].q;
+    const uint16_t* pd = a.p[j].d;
+    float* pout = a.p[j].out;
+    const int prows = a.p[j].rows, pnb = a.p[j].nb, pnbp = a.p[j].nbp;
+    const int quads = pnbp / 4;
+    const bool one_chunk = pnbp <= kc;
     if (one_chunk) {
       named_barrier(kConsumerBarrier, kConsumers);  // previous product's table no longer read
-      if (p.x) build_table_x(p.x, p.nb, 0, p.nbp, table, tid, kConsumers, a.kc);
-      else build_table_q(p.q, p.d, p.nb, 0, p.nbp, table, tid, kConsumers, a.kc);
+      if (px) build_table_x(px, pnb, 0, pnbp, table, tid, kConsumers, kc);
+      else build_table_q(pq, pd, pnb, 0, pnbp, table, tid, kConsumers, kc);
       named_barrier(kConsumerBarrier, kConsumers);
     }
     for (int t = t_lo; t < t_hi && ok; ++t) {
@@ -182,60 +184,34 @@ __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_cons
 #pragma unroll
       for (int r = 0; r < R; ++r) acc[r] = 0ull;  // both lanes +0
 
-      for (int oct = 0; oct < octets; ++oct, ++it) {
-        const int b0 = oct * 8;
-        if (!one_chunk && b0 % a.kc == 0) {
+      for (int qd = 0; qd < quads; ++qd, ++it) {
+        const int b0 = qd * 4;
+        if (!one_chunk && b0 % kc == 0) {
           named_barrier(kConsumerBarrier, kConsumers);
-          const int kcb = min(a.kc, p.nbp - b0);
-          if (p.x) build_table_x(p.x, p.nb, b0, kcb, table, tid, kConsumers, a.kc);
-          else build_table_q(p.q, p.d, p.nb, b0, kcb, table, tid, kConsumers, a.kc);
+          const int kcb = min(kc, pnbp - b0);
+          if (px) build_table_x(px, pnb, b0, kcb, table, tid, kConsumers, kc);
+          else build_table_q(pq, pd, pnb, b0, kcb, table, tid, kConsumers, kc);
           named_barrier(kConsumerBarrier, kConsumers);
         }
-        const int gb = one_chunk ? b0 : b0 % a.kc;
+        const int gb = one_chunk ? b0 : b0 % kc;  // block index within the table
         const int s = it % S;
         if (!mbar_wait(smem_addr(&bars[s]), uint32_t(it / S) & 1u)) {
           ok = false;
           break;
         }
         const unsigned char* st = smem + s * SB;
-        uint4 sc[R];
+        uint4 wv[R];
+        uint2 sc[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-          sc[r] = reinterpret_cast<const uint4*>(st + 2 * R * kPanelBits + (2 * r + ps) * kPanelScales)[prow];
-#pragma unroll
-        for (int quad = 0; quad < 2; ++quad) {
-          uint4 wv[R];
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-            wv[r] = reinterpret_cast<const uint4*>(st + (2 * r + ps) * kPanelBits)[quad * 128 + prow * 4 + w];
-          if (quad == 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bars[S + s]));  // stage fully read
-          }
-#pragma unroll
-          for (int bq = 0; bq < 4; ++bq) {
-            const int bb = quad * 4 + bq;
-            uint64_t ab[R];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int g = (gb + bb) * 4 + k;
-              const uint4 qc = QC[g * 4 + w];
-              const float4 dk = DK[g];
-              const uint64_t dpair = f2pack(dk.x, dk.y);
-              const uint64_t kpair = f2pack(dk.z, dk.w);
-#pragma unroll
-              for (int r = 0; r < R; ++r) {
-                const uint64_t pr = subblock_products(word_of(wv[r], bq), k, qc, dpair, kpair);
-                ab[r] = (k == 0) ? pr : add2(ab[r], pr);
-              }
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-              const float d0 = half_of(sc[r], bb);
-              acc[r] = fma2(f2pack(d0, d0), ab[r], acc[r]);
-            }
-          }
+        for (int r = 0; r < R; ++r) {
+          const int tp = kSlots * r + ps;
+          wv[r] = reinterpret_cast<const uint4*>(st + tp * kQuadBits)[prow * 4 + w];
+          sc[r] = reinterpret_cast<const uint2*>(st + TB + tp * kQuadScales)[prow];
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&bars[S + s]));  // stage consumed
+
+        quad_all<R>(wv, sc, QC + gb * 16, DK + gb * 4, w, acc);
       }
       if (!ok) break;
       // Horizontal sum: xor 2 pairs lane pair w with w+2 (a0+a4, a1+a5 |
@@ -247,8 +223,8 @@ __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_cons
         sum = add2(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
         float lo2, hi2;
         f2unpack(sum, lo2, hi2);
-        const int64_t row = (int64_t(t) * 2 * R + 2 * r + ps) * kPanel + prow;
-        if (w == 0 && row < p.rows) p.out[row] = __fadd_rn(lo2, hi2);
+        const int64_t row = (int64_t(t) * kSlots * R + kSlots * r + ps) * kPanel + prow;
+        if (w == 0 && row < prows) pout[row] = __fadd_rn(lo2, hi2);
       }
     }
   }
@@ -313,7 +289,7 @@ static int launch_multi(const q1_product* prods, int count, cudaStream_t s, cons
     p.nb = int(L.nb);
     p.nbp = int(L.nbp);
     p.panels = int(L.panels);
-    p.tiles = int((L.panels + 2 * R - 1) / (2 * R));
+    p.tiles = int(L.panels / (kSlots * R));  // panels come in groups of 8, so tiles are whole
     p.cost_begin = cost;
     cost += int64_t(p.tiles) * p.nbp;
     total_tiles += p.tiles;

@@ -9,14 +9,6 @@ __device__ __forceinline__ int elem_of(int w, int pl, int i) {
   return 32 * (pl >> 1) + 4 * (2 * w + (pl & 1)) + i;
 }
 
-__device__ __forceinline__ int64_t bits_word_index(int64_t p, int64_t b, int r, int w, int64_t nbp) {
-  return (((p * (nbp / 4) + b / 4) * kPanel + r) * 4 + w) * 4 + (b % 4);
-}
-
-__device__ __forceinline__ int64_t scale_index(int64_t p, int64_t b, int r, int64_t nbp) {
-  return ((p * (nbp / 8) + b / 8) * kPanel + r) * 8 + (b % 8);
-}
-
 // One thread per (padded row, padded block).
 __global__ void k_pack(const uint8_t* __restrict__ blocks, int64_t rows, int64_t nb, int64_t nbp,
                        int64_t rows_pad, uint32_t* __restrict__ bits, uint16_t* __restrict__ scales) {
@@ -25,7 +17,7 @@ __global__ void k_pack(const uint8_t* __restrict__ blocks, int64_t rows, int64_t
   int64_t r = idx / nbp, b = idx % nbp;
   int64_t p = r / kPanel;
   int rr = int(r % kPanel);
-  uint32_t word[4] = {0u, 0u, 0u, 0u};
+  uint32_t word[4] = {0u, 0u, 0u, 0u};  // one per lane pair
   uint16_t sc = 0;
   if (r < rows && b < nb) {
     const uint8_t* blk = blocks + (r * nb + b) * kBlockBytes;

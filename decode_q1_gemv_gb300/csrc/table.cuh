@@ -137,14 +137,73 @@ __device__ __forceinline__ float half_of(const uint4& v, int i) {
 // One sub-block step for one row and one lane pair: masks the row's word W to
 // the two lanes' planes, forms the exact products d1*s for both lanes and
 // returns them as a float pair.
-__device__ __forceinline__ uint64_t subblock_products(uint32_t W, int k, const uint4& qc, uint64_t dpair,
-                                                      uint64_t kpair) {
-  uint32_t m0 = W & (0x01010101u << (2 * k));
-  const uint32_t m1 = W & (0x01010101u << (2 * k + 1));
-  if (k == 0) m0 <<= 1;  // plane 0 is used as plane 1 (byte values 0/2)
+template <int K>
+__device__ __forceinline__ uint64_t subblock_products(uint32_t W, const uint4& qc, uint64_t dpair, uint64_t kpair) {
+  uint32_t m0 = W & (0x01010101u << (2 * K));
+  const uint32_t m1 = W & (0x01010101u << (2 * K + 1));
+  if constexpr (K == 0) m0 <<= 1;  // plane 0 is used as plane 1 (byte values 0/2)
   const uint32_t D0 = dp4a_us(m0, qc.x, qc.z);
   const uint32_t D1 = dp4a_us(m1, qc.y, qc.w);
   return fma2(dpair, f2pack(__uint_as_float(D0), __uint_as_float(D1)), kpair);
+}
+
+template <int I>
+__device__ __forceinline__ uint32_t word_at(const uint4& v) {
+  if constexpr (I == 0) return v.x;
+  else if constexpr (I == 1) return v.y;
+  else if constexpr (I == 2) return v.z;
+  else return v.w;
+}
+
+// fp16 scale I (0..3) of a quad held as 4 halves in a uint2.
+template <int I>
+__device__ __forceinline__ float quad_scale(const uint2& v) {
+  const uint32_t w = (I < 2) ? v.x : v.y;
+  return __half2float(__ushort_as_half(uint16_t((I & 1) ? (w >> 16) : (w & 0xffffu))));
+}
+
+// Sub-block K of block BQ of a quad for R rows: ab[r] = d1*s (K = 0) or
+// add.rn(ab[r], d1*s) (K > 0).  QCq/DKq point at the quad's first sub-block.
+template <int R, int BQ, int K>
+__device__ __forceinline__ void quad_subblock(const uint4 (&wv)[R], const uint4* QCq, const float4* DKq, int w,
+                                              uint64_t (&ab)[R]) {
+  const uint4 qc = QCq[(BQ * 4 + K) * 4 + w];
+  const float4 dk = DKq[BQ * 4 + K];
+  const uint64_t dpair = f2pack(dk.x, dk.y);
+  const uint64_t kpair = f2pack(dk.z, dk.w);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const uint64_t pr = subblock_products<K>(word_at<BQ>(wv[r]), qc, dpair, kpair);
+    if constexpr (K == 0) ab[r] = pr;
+    else ab[r] = add2(ab[r], pr);
+  }
+}
+
+// Block BQ of a quad for R rows: the four sub-blocks, then the outer
+// acc = fma(d0, ab, acc) with d0 the row's block scale.
+template <int R, int BQ>
+__device__ __forceinline__ void quad_block(const uint4 (&wv)[R], const uint2 (&sc)[R], const uint4* QCq,
+                                           const float4* DKq, int w, uint64_t (&acc)[R]) {
+  uint64_t ab[R];
+  quad_subblock<R, BQ, 0>(wv, QCq, DKq, w, ab);
+  quad_subblock<R, BQ, 1>(wv, QCq, DKq, w, ab);
+  quad_subblock<R, BQ, 2>(wv, QCq, DKq, w, ab);
+  quad_subblock<R, BQ, 3>(wv, QCq, DKq, w, ab);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const float d0 = quad_scale<BQ>(sc[r]);
+    acc[r] = fma2(f2pack(d0, d0), ab[r], acc[r]);
+  }
+}
+
+// A whole quad (4 blocks) for R rows.
+template <int R>
+__device__ __forceinline__ void quad_all(const uint4 (&wv)[R], const uint2 (&sc)[R], const uint4* QCq,
+                                         const float4* DKq, int w, uint64_t (&acc)[R]) {
+  quad_block<R, 0>(wv, sc, QCq, DKq, w, acc);
+  quad_block<R, 1>(wv, sc, QCq, DKq, w, acc);
+  quad_block<R, 2>(wv, sc, QCq, DKq, w, acc);
+  quad_block<R, 3>(wv, sc, QCq, DKq, w, acc);
 }
 
 }  // namespace q1

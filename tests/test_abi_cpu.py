@@ -46,13 +46,13 @@ def test_library_exports_are_c_symbols():
 
 
 @pytest.mark.parametrize("rows,n,expect", [
-    (1, 128, 32 * 8 * 18),            # one row pads to a 32-row panel, 1 block to 8
-    (32, 1024, 32 * 8 * 18),
-    (33, 1024, 64 * 8 * 18),
+    (1, 128, 256 * 4 * 18),           # rows pad to a 256-row panel group, blocks to 4
+    (32, 1024, 256 * 8 * 18),
+    (257, 1024, 512 * 8 * 18),
     (4096, 4096, 4096 * 32 * 18),     # exactly 18 bytes per 128 weights
     (4096, 14336, 4096 * 112 * 18),
     (128256, 4096, 128256 * 32 * 18),
-    (100, 384, 128 * 8 * 18),         # 3 blocks pad to 8
+    (100, 640, 256 * 8 * 18),         # 5 blocks pad to 8
 ])
 def test_packed_bytes(lib, rows, n, expect):
     assert binding.packed_bytes(rows, n) == expect

@@ -1,0 +1,64 @@
+"""Host logic of bench.py's multi-process path, on CPU with gloo (world size 2):
+the max over ranks every rank agrees on, and the reference arm's rank > 0 exit."""
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    got = bench.max_over_ranks(1.5 * (rank + 1), world, dist, torch.device("cpu"))
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((rank, got))
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res == {0: 3.0, 1: 3.0}
+
+
+def test_max_over_ranks_single_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(2.5, 1) == 2.5
+
+
+def test_reference_arm_rank_above_zero_does_no_work(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "1")
+
+    class A:
+        steps, warmup, gpus = 3, 3, 2
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.run_reference(A()) == 0
+    assert buf.getvalue() == ""

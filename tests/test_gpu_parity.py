@@ -371,3 +371,25 @@ def test_bad_arguments_raise():
 def test_device_status_clean_after_suite():
     """No kernel gave up a bounded wait during the parity runs."""
     assert binding.device_status(clear=True) == 0
+
+
+def test_bench_json_line_contract():
+    """bench.py prints one JSON line with the keys the benchmark contract needs."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--layers", "1", "--steps", "3", "--warmup", "3",
+                        "--no-cpu-baseline", "--schedules", "grouped"], cwd=root, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in d, key
+    assert d["roofline"]["bound"] == "hbm" and d["roofline"]["peak"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] == 3 and d["value"] > 0
