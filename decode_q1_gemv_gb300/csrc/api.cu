@@ -36,3 +36,9 @@ extern "C" int64_t q1_0_packed_bytes(int64_t rows, int64_t n) {
   q1::g_last_error.clear();
   return q1::layout_of(rows, n).total_bytes;
 }
+
+extern "C" int q1_device_status(int clear) {
+  unsigned v = 0;
+  if (int e = q1::status_word_dp4a(&v, clear)) return e;
+  return int(v);
+}

@@ -26,20 +26,21 @@ constexpr int kBlockPad = 4;      // blocks per row are padded to a multiple of 
 //
 //   bits   : u32 words at byte 0.  For panel group gi, block quad qd (blocks
 //            4qd..4qd+3), panel pi within the group (0..7), panel row r (0..31),
-//            lane pair w (0..3) and block bq within the quad, the word sits at
+//            word w (0..3) and block bq within the quad, the word sits at
 //              ((((gi*nq + qd)*8 + pi)*32 + r)*4 + w)*4 + bq
-//            so one quad of one panel is 2 KB, a warp's 8 rows x 4 lane pairs
+//            so one quad of one panel is 2 KB, a warp's 8 rows x 4 words
 //            read 512 contiguous bytes, and the quad of 2, 4 or 8 aligned
 //            consecutive panels is one contiguous 4, 8 or 16 KB chunk.
 //   scales : fp16 block scales d0 after the bits (byte offset rows_pad*nbp*16),
 //            half index (((gi*nq + qd)*8 + pi)*32 + r)*4 + bq: 256 B per panel
 //            and quad, contiguous across the panels of a group in the same way.
 //
-// Within a word w of (row, block): bit 8*i + pl (i = 0..3, plane pl = 0..7)
-// is the sign bit of block element 32*(pl>>1) + 4*(2*w + (pl&1)) + i, i.e. lane
-// 2w + (pl&1) of sub-block pl>>1.  Masking a word with 0x01010101 << pl leaves
-// that lane-and-sub-block's four sign bits as four bytes of value 0 or 2^pl.
-// Padded rows and blocks hold zero bits and zero scales.
+// Within word w of (row, block): bit 8*i + pl (i = 0..3, plane pl = 0..7) is
+// the sign bit of block element 32*(pl>>1) + 4*(w + 4*(pl&1)) + i, i.e. element
+// i of lane w (even planes) or lane w + 4 (odd planes) of sub-block pl>>1.
+// Masking a word with 0x01010101 << pl leaves that lane-and-sub-block's four
+// sign bits as four bytes of value 0 or 2^pl.  Padded rows and blocks hold
+// zero bits and zero scales.
 struct Layout {
   int64_t rows, n, nb, nbp, panels, rows_pad;
   int64_t bits_bytes, scales_bytes, total_bytes;
@@ -59,7 +60,7 @@ inline Layout layout_of(int64_t rows, int64_t n) {
   return L;
 }
 
-// Word index of (panel p, block b, panel row r, lane pair w) and half index of
+// Word index of (panel p, block b, panel row r, word w) and half index of
 // the scale of (panel p, block b, row r); p counts panels from the start.
 __host__ __device__ __forceinline__ int64_t bits_word_index(int64_t p, int64_t b, int r, int w, int64_t nbp) {
   return ((((p / kGroup) * (nbp / 4) + b / 4) * kGroup + p % kGroup) * kPanel + r) * 16 + w * 4 + (b % 4);
@@ -73,15 +74,6 @@ __host__ __device__ __forceinline__ int64_t quad_bits_offset(int64_t p, int64_t 
 }
 __host__ __device__ __forceinline__ int64_t quad_scales_offset(int64_t p, int64_t qd, int64_t nbp) {
   return (((p / kGroup) * (nbp / 4) + qd) * kGroup + p % kGroup) * 256;
-}
-
-// Plane (0..7) of lane l in sub-block k inside its lane pair's word.
-__host__ __device__ constexpr int plane_of(int k, int l) { return 2 * k + (l & 1); }
-// Effective plane: plane 0 is used shifted left by one (byte value 2), so every
-// lane group is scaled by 2^pe with pe >= 1 and the activation term can enter
-// the integer accumulator as 2^(pe-1) * A.
-__host__ __device__ constexpr int eff_plane(int k, int l) {
-  return plane_of(k, l) > 0 ? plane_of(k, l) : 1;
 }
 
 // Magic accumulator: the float whose bits are 0x4B400000 is 1.5 * 2^23 = C; for
@@ -141,6 +133,14 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 int fail(int code, const char* fmt, ...);
 // Checks a CUDA runtime status after a launch; records and maps errors.
 int cuda_status(cudaError_t e, const char* what);
+// SM count of the current device (cached per device).
+int num_sms();
+// Argument checks of one q1_product (shape, pointers, 16-byte alignment).
+int check_product(const char* who, int idx, const q1_product& pr);
+// The streaming matrix-vector kernel behind q1_0_gemv / q1_0_gemv_multi.
+int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, const char* who);
+// Device status word of the product kernels (read and optionally cleared).
+int status_word_dp4a(unsigned* v, int clear);
 
 }  // namespace q1
 

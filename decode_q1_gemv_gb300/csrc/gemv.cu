@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tb = table_bytes(a.kc);
   const int lane = threadIdx.x & 31;
-  const int w = lane & 3;                               // lane pair: lanes 2w, 2w+1
+  const int w = lane & 3;                               // word w: lanes w and w+4
   const int prow = (threadIdx.x >> 5) * 8 + (lane >> 2);  // row within the panel
 
   const int vg = blockIdx.x % a.vgroups;
@@ -85,20 +85,18 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
   }
 
   pdl_launch_dependents();
-  // Horizontal sum: lane pair w holds (a_2w, a_2w+1).  xor 2 pairs w with w+2
-  // (a0+a4, a1+a5 | a2+a6, a3+a7); xor 1 then adds those; the final add joins
-  // the even-lane and odd-lane halves.
+  // Horizontal sum: thread w holds (a_w, a_w+4) and adds them; xor 2 then
+  // gives (a0+a4)+(a2+a6) and (a1+a5)+(a3+a7), xor 1 joins the two.
 #pragma unroll
   for (int j = 0; j < R; ++j) {
     const int64_t row = int64_t(p0 + j) * kPanel + prow;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      uint64_t s = acc[v][j];
-      s = add2(s, __shfl_xor_sync(0xffffffffu, s, 2));
-      s = add2(s, __shfl_xor_sync(0xffffffffu, s, 1));
       float lo, hi;
-      f2unpack(s, lo, hi);
-      const float r = __fadd_rn(lo, hi);
+      f2unpack(acc[v][j], lo, hi);
+      float r = __fadd_rn(lo, hi);
+      r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, 2));
+      r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, 1));
       if (w == 0 && p0 + j < a.panels && row < a.rows && v0 + v < a.nvec)
         a.out[int64_t(v0 + v) * a.rows + row] = r;
     }

@@ -29,7 +29,7 @@
 
 namespace q1 {
 
-__device__ unsigned g_device_status = 0u;
+static __device__ unsigned g_status_dp4a = 0u;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_cons
           }
         }
       }
-      if (!ok) atomicOr(&g_device_status, kStatusWaitTimeout);
+      if (!ok) atomicOr(&g_status_dp4a, kStatusWaitTimeout);
     }
     return;
   }
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_cons
   const int tid = threadIdx.x;
   const int ps = warp >> 2;                       // panel slot within the tile
   const int prow = (warp & 3) * 8 + (lane >> 2);  // row within the panel
-  const int w = lane & 3;                         // lane pair 2w, 2w+1
+  const int w = lane & 3;                         // word w: lanes w and w+4
   const uint4* QC = reinterpret_cast<const uint4*>(table);
   const float4* DK = reinterpret_cast<const float4*>(table + table_dk_offset(a.kc));
   const int kc = a.kc;
@@ -214,35 +214,24 @@ __global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_cons
         quad_all<R>(wv, sc, QC + gb * 16, DK + gb * 4, w, acc);
       }
       if (!ok) break;
-      // Horizontal sum: xor 2 pairs lane pair w with w+2 (a0+a4, a1+a5 |
-      // a2+a6, a3+a7), xor 1 adds those, the last add joins even and odd lanes.
+      // Horizontal sum: thread w holds (a_w, a_w+4) and adds them; xor 2 then
+      // gives (a0+a4)+(a2+a6) and (a1+a5)+(a3+a7), xor 1 joins the two.
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        uint64_t sum = acc[r];
-        sum = add2(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
-        sum = add2(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
         float lo2, hi2;
-        f2unpack(sum, lo2, hi2);
+        f2unpack(acc[r], lo2, hi2);
+        float sum = __fadd_rn(lo2, hi2);
+        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
+        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
         const int64_t row = (int64_t(t) * kSlots * R + kSlots * r + ps) * kPanel + prow;
-        if (w == 0 && row < prows) pout[row] = __fadd_rn(lo2, hi2);
+        if (w == 0 && row < prows) pout[row] = sum;
       }
     }
   }
-  if (!ok) atomicOr(&g_device_status, kStatusWaitTimeout);
+  if (!ok) atomicOr(&g_status_dp4a, kStatusWaitTimeout);
 }
 
 // ---------------------------------------------------------------- host ----
-static int num_sms() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int v = 0;
-    cached[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 148;
-  }
-  return cached[dev];
-}
-
 template <int R, int PMAX>
 static int set_smem_attr() {
   static int done[64] = {0};
@@ -254,18 +243,6 @@ static int set_smem_attr() {
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
     done[dev] = 1;
   }
-  return Q1_OK;
-}
-
-static int check_product(const char* who, int idx, const q1_product& pr) {
-  if (pr.rows < 1 || pr.rows > (int64_t(1) << 26) || pr.n < 128 || pr.n > (int64_t(1) << 24) || pr.n % 128)
-    return fail(Q1_ERR_ARG, "%s: product %d: bad shape rows=%lld n=%lld", who, idx, (long long)pr.rows,
-                (long long)pr.n);
-  if (!pr.packed || !pr.out || (!pr.x && (!pr.q || !pr.d)))
-    return fail(Q1_ERR_ARG, "%s: product %d: null pointer", who, idx);
-  auto mis = [](const void* p) { return p && reinterpret_cast<uintptr_t>(p) % 16 != 0; };
-  if (mis(pr.packed) || mis(pr.x) || mis(pr.q) || mis(pr.d) || mis(pr.out))
-    return fail(Q1_ERR_ARG, "%s: product %d: buffers must be 16-byte aligned", who, idx);
   return Q1_OK;
 }
 
@@ -323,6 +300,44 @@ static int dispatch(const q1_product* prods, int count, cudaStream_t s, const ch
   return launch_multi<1, PMAX>(prods, count, s, who);
 }
 
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int v = 0;
+    cached[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 148;
+  }
+  return cached[dev];
+}
+
+int check_product(const char* who, int idx, const q1_product& pr) {
+  if (pr.rows < 1 || pr.rows > (int64_t(1) << 26) || pr.n < 128 || pr.n > (int64_t(1) << 24) || pr.n % 128)
+    return fail(Q1_ERR_ARG, "%s: product %d: bad shape rows=%lld n=%lld", who, idx, (long long)pr.rows,
+                (long long)pr.n);
+  if (!pr.packed || !pr.out || (!pr.x && (!pr.q || !pr.d)))
+    return fail(Q1_ERR_ARG, "%s: product %d: null pointer", who, idx);
+  auto mis = [](const void* p) { return p && reinterpret_cast<uintptr_t>(p) % 16 != 0; };
+  if (mis(pr.packed) || mis(pr.x) || mis(pr.q) || mis(pr.d) || mis(pr.out))
+    return fail(Q1_ERR_ARG, "%s: product %d: buffers must be 16-byte aligned", who, idx);
+  return Q1_OK;
+}
+
+int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+  if (count == 1) return dispatch<1>(prods, count, s, who);
+  if (count <= 8) return dispatch<8>(prods, count, s, who);
+  return dispatch<Q1_MAX_PRODUCTS>(prods, count, s, who);
+}
+
+int status_word_dp4a(unsigned* v, int clear) {
+  if (int e = cuda_status(cudaMemcpyFromSymbol(v, g_status_dp4a, sizeof *v), "q1_device_status")) return e;
+  if (clear && *v) {
+    const unsigned zero = 0;
+    return cuda_status(cudaMemcpyToSymbol(g_status_dp4a, &zero, sizeof zero), "q1_device_status");
+  }
+  return Q1_OK;
+}
+
 }  // namespace q1
 
 using namespace q1;
@@ -332,7 +347,7 @@ extern "C" int q1_0_gemv(const void* packed, int64_t rows, int64_t n, const int8
   q1_product p = {packed, rows, n, nullptr, q, d, out};
   if (!q || !d) return fail(Q1_ERR_ARG, "q1_0_gemv: null pointer");
   if (int e = check_product("q1_0_gemv", 0, p)) return e;
-  return dispatch<1>(&p, 1, static_cast<cudaStream_t>(stream), "q1_0_gemv launch");
+  return launch_products_dp4a(&p, 1, static_cast<cudaStream_t>(stream), "q1_0_gemv launch");
 }
 
 extern "C" int q1_0_gemv_multi(const q1_product* products, int count, void* stream) {
@@ -340,18 +355,5 @@ extern "C" int q1_0_gemv_multi(const q1_product* products, int count, void* stre
     return fail(Q1_ERR_ARG, "q1_0_gemv_multi: count=%d outside 1..%d (or null list)", count, Q1_MAX_PRODUCTS);
   for (int j = 0; j < count; ++j)
     if (int e = check_product("q1_0_gemv_multi", j, products[j])) return e;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (count == 1) return dispatch<1>(products, count, s, "q1_0_gemv_multi launch");
-  if (count <= 8) return dispatch<8>(products, count, s, "q1_0_gemv_multi launch");
-  return dispatch<Q1_MAX_PRODUCTS>(products, count, s, "q1_0_gemv_multi launch");
-}
-
-extern "C" int q1_device_status(int clear) {
-  unsigned v = 0;
-  if (int e = cuda_status(cudaMemcpyFromSymbol(&v, g_device_status, sizeof v), "q1_device_status")) return e;
-  if (clear && v) {
-    const unsigned zero = 0;
-    if (int e = cuda_status(cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero), "q1_device_status")) return e;
-  }
-  return int(v);
+  return launch_products_dp4a(products, count, static_cast<cudaStream_t>(stream), "q1_0_gemv_multi launch");
 }

@@ -4,9 +4,10 @@
 
 namespace q1 {
 
-// Element of the 128-element block held by bit (8*i + pl) of lane-pair word w.
+// Element of the 128-element block held by bit (8*i + pl) of word w: lane
+// w + 4*(pl & 1) of sub-block pl >> 1, element i of the lane.
 __device__ __forceinline__ int elem_of(int w, int pl, int i) {
-  return 32 * (pl >> 1) + 4 * (2 * w + (pl & 1)) + i;
+  return 32 * (pl >> 1) + 4 * (w + 4 * (pl & 1)) + i;
 }
 
 // One thread per (padded row, padded block).
@@ -17,7 +18,7 @@ __global__ void k_pack(const uint8_t* __restrict__ blocks, int64_t rows, int64_t
   int64_t r = idx / nbp, b = idx % nbp;
   int64_t p = r / kPanel;
   int rr = int(r % kPanel);
-  uint32_t word[4] = {0u, 0u, 0u, 0u};  // one per lane pair
+  uint32_t word[4] = {0u, 0u, 0u, 0u};  // word w holds lanes w and w + 4
   uint16_t sc = 0;
   if (r < rows && b < nb) {
     const uint8_t* blk = blocks + (r * nb + b) * kBlockBytes;

@@ -7,7 +7,7 @@
 //   A   = sum(q') + 128 * #(-128)      so that the lane sum is s = 2*M - A
 //         with M = sum(bit_i * q'_i) (an i8 negation of -128 stays -128)
 //   ci  = 0x4B400000 - 2^(pe-1) * A    dp4a accumulator init, pe = the lane's
-//                                      effective bit plane (common.cuh)
+//                                      effective bit plane (below)
 // and for every sub-block and lane parity
 //   d'  = d1 * 2^(1-pe),  K = -d' * 1.5*2^23
 // with d1 the sub-block's fp16 scale widened to f32.  Then, for a weight word
@@ -15,8 +15,8 @@
 // F = 1.5*2^23 + 2^(pe-1)*s, and fma(d', F, K) = d1*s exactly.
 //
 // Layout for a chunk of kc blocks (kc*4 sub-blocks), 80 bytes per sub-block:
-//   QC[g][w] (uint4)  = { q' lane 2w, q' lane 2w+1, ci lane 2w, ci lane 2w+1 }
-//   DK[g]    (float4) = { d' even lanes, d' odd lanes, K even, K odd }
+//   QC[g][w] (uint4)  = { q' lane w, q' lane w+4, ci lane w, ci lane w+4 }
+//   DK[g]    (float4) = { d' lanes 0-3, d' lanes 4-7, K lanes 0-3, K lanes 4-7 }
 #pragma once
 
 #include "common.cuh"
@@ -30,7 +30,10 @@ __device__ __forceinline__ float pow2i(int e) {  // exact 2^e for -126 <= e <= 1
   return __int_as_float((127 + e) << 23);
 }
 
-// Effective plane of lane parity `par` in sub-block k (see eff_plane).
+// Effective bit plane of sub-block k for the low (par 0: lanes 0-3, plane 2k)
+// or high (par 1: lanes 4-7, plane 2k+1) half of a word.  Plane 0 is used
+// shifted left by one (byte values 0/2), so every lane's dp4a result is
+// 2^pe * M with pe >= 1 and the activation term enters as 2^(pe-1) * A.
 __device__ __forceinline__ int pe_of(int k, int par) { return (k == 0 && par == 0) ? 1 : 2 * k + par; }
 
 __device__ __forceinline__ void lane_consts(uint32_t word, int k, int par, uint32_t& qp, uint32_t& ci) {
@@ -62,7 +65,7 @@ static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, 
 #pragma unroll
     for (int par = 0; par < 2; ++par) {
       uint32_t word = 0u;
-      if (G < nsub) word = *reinterpret_cast<const uint32_t*>(q + int64_t(G) * kSub + 4 * (2 * w + par));
+      if (G < nsub) word = *reinterpret_cast<const uint32_t*>(q + int64_t(G) * kSub + 4 * (w + 4 * par));
       lane_consts(word, k, par, qp[par], ci[par]);
     }
     QC[g * 4 + w] = make_uint4(qp[0], qp[1], ci[0], ci[1]);
@@ -109,12 +112,12 @@ static __device__ __noinline__ void build_table_x(const float* __restrict__ x, i
     const uint32_t word = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
     const float d1 = __half2float(__float2half_rn(dd));
     if (t < total) {
-      const int k = g & 3, par = l & 1, w = l >> 1;
+      const int k = g & 3, par = l >> 2, w = l & 3;
       uint32_t qp, ci;
       lane_consts(word, k, par, qp, ci);
       QCw[(g * 4 + w) * 4 + par] = qp;
       QCw[(g * 4 + w) * 4 + 2 + par] = ci;
-      if (l < 2) {
+      if ((l & 3) == 0) {
         float dprime, K;
         scale_consts(G < nsub ? d1 : 0.0f, k, par, dprime, K);
         DKf[g * 4 + par] = dprime;
@@ -134,9 +137,9 @@ __device__ __forceinline__ float half_of(const uint4& v, int i) {
   return __half2float(__ushort_as_half(h));
 }
 
-// One sub-block step for one row and one lane pair: masks the row's word W to
-// the two lanes' planes, forms the exact products d1*s for both lanes and
-// returns them as a float pair.
+// One sub-block step for one row and one word (lanes w and w+4): masks the
+// row's word W to the two lanes' planes, forms the exact products d1*s for
+// both lanes and returns them as a float pair (lane w, lane w+4).
 template <int K>
 __device__ __forceinline__ uint64_t subblock_products(uint32_t W, const uint4& qc, uint64_t dpair, uint64_t kpair) {
   uint32_t m0 = W & (0x01010101u << (2 * K));
