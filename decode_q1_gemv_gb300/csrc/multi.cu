@@ -9,13 +9,15 @@
 // independent chains, so four threads share a row, two lanes each; table.cuh
 // explains how every step keeps the definition's single roundings.
 //
-// Structure.  A CTA is one producer warp and eight consumer warps.  The
-// producer streams packed weights HBM -> shared memory with 1-D bulk copies
-// into a ring of stages (mbarrier full/empty pairs).  A stage is one quad of
-// blocks (4 x 128 weights per row) for the CTA's current tile of 2R panels
-// (64R rows, two panels side by side): 2 KB of sign words and 256 B of scales
-// per panel, two contiguous copies thanks to the packed layout.  Consumer
-// thread (row, lane pair) handles R rows of a tile.  CTAs are persistent: the
+// Structure.  A CTA is one producer warp and four consumer warps per panel
+// slot (two slots for R <= 4 rows per thread, one for R = 8).  The producer
+// streams packed weights HBM -> shared memory with 1-D bulk copies into a
+// ring of stages (mbarrier full/empty pairs).  A stage is one quad of blocks
+// (4 x 128 weights per row) for the CTA's current tile of slots*R panels (8
+// panels = 256 rows for the large launches): 2 KB of sign words and 256 B of
+// scales per panel, two contiguous copies thanks to the packed layout.
+// Consumer thread (row, lane pair) handles R rows of a tile.  CTAs are
+// persistent: the
 // products' tiles are split into contiguous ranges of equal weight bytes, one
 // range per CTA, and the producer runs ahead across tile and product
 // boundaries.  The producer reads only weights, so it starts before
@@ -31,10 +33,17 @@ namespace q1 {
 
 static __device__ unsigned g_status_dp4a = 0u;
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kMultiThreads = kConsumers + 32;
-constexpr int kSlots = kConsumerWarps / 4;  // panels computed side by side (4 warps = 32 rows each)
+// Panels computed side by side (4 consumer warps = 32 rows each): two for
+// R <= 4 rows per thread, one for R = 8 (same 8-panel tile, twice the rows
+// per thread, half the warps).
+template <int R>
+__host__ __device__ constexpr int slots_of() { return R >= 8 ? 1 : 2; }
+template <int R>
+__host__ __device__ constexpr int consumer_warps() { return 4 * slots_of<R>(); }
+template <int R>
+__host__ __device__ constexpr int consumers() { return 32 * consumer_warps<R>(); }
+template <int R>
+__host__ __device__ constexpr int multi_threads() { return consumers<R>() + 32; }
 constexpr int kQuadBits = 2048;    // one panel x one quad of blocks: 32 rows x 4 blocks x 16 B
 constexpr int kQuadScales = 256;   // 32 rows x 4 blocks x 2 B
 constexpr int kConsumerBarrier = 1;
@@ -59,12 +68,12 @@ struct MArgs {
   int kc;                // table chunk in blocks (multiple of 4)
 };
 
-// Ring of stages: a stage is one quad of blocks for the tile's 2R panels; about
-// 74 KB of weights in flight per CTA whatever R is.
+// Ring of stages: a stage is one quad of blocks for the tile's slots*R panels;
+// about 74 KB of weights in flight per CTA whatever R is.
 template <int R>
-__host__ __device__ constexpr int ring_stages() { return 16 / R; }
+__host__ __device__ constexpr int ring_stages() { return 32 / (slots_of<R>() * R); }
 template <int R>
-__host__ __device__ constexpr int stage_bytes() { return kSlots * R * (kQuadBits + kQuadScales); }
+__host__ __device__ constexpr int stage_bytes() { return slots_of<R>() * R * (kQuadBits + kQuadScales); }
 
 template <int R>
 __host__ __device__ constexpr int multi_smem_bytes(int kc) {
@@ -83,10 +92,13 @@ __device__ __forceinline__ void tile_range(const MProd& p, int64_t lo, int64_t h
 }
 
 template <int R, int PMAX>
-__global__ void __launch_bounds__(kMultiThreads, 2) k_q1_multi(const __grid_constant__ MArgs<PMAX> a) {
+__global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid_constant__ MArgs<PMAX> a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int S = ring_stages<R>();
   constexpr int SB = stage_bytes<R>();
+  constexpr int kSlots = slots_of<R>();
+  constexpr int kConsumerWarps = consumer_warps<R>();
+  constexpr int kConsumers = consumers<R>();
   constexpr int TB = kSlots * R * kQuadBits;  // bits part of a stage
   unsigned char* table = smem + S * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(table + table_bytes(a.kc));
@@ -266,7 +278,7 @@ static int launch_multi(const q1_product* prods, int count, cudaStream_t s, cons
     p.nb = int(L.nb);
     p.nbp = int(L.nbp);
     p.panels = int(L.panels);
-    p.tiles = int(L.panels / (kSlots * R));  // panels come in groups of 8, so tiles are whole
+    p.tiles = int(L.panels / (slots_of<R>() * R));  // panels come in groups of 8, so tiles are whole
     p.cost_begin = cost;
     cost += int64_t(p.tiles) * p.nbp;
     total_tiles += p.tiles;
@@ -278,7 +290,7 @@ static int launch_multi(const q1_product* prods, int count, cudaStream_t s, cons
   const int grid = int(std::min<int64_t>(total_tiles, 2 * num_sms()));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
-  cfg.blockDim = dim3(kMultiThreads);
+  cfg.blockDim = dim3(multi_threads<R>());
   cfg.dynamicSmemBytes = size_t(multi_smem_bytes<R>(a.kc));
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -295,7 +307,7 @@ static int dispatch(const q1_product* prods, int count, cudaStream_t s, const ch
   int64_t panels = 0;
   for (int j = 0; j < count; ++j) panels += (prods[j].rows + kPanel - 1) / kPanel;
   const int64_t ctas = 2 * int64_t(num_sms());
-  if (panels >= 8 * ctas) return launch_multi<4, PMAX>(prods, count, s, who);
+  if (panels >= 8 * ctas) return launch_multi<8, PMAX>(prods, count, s, who);
   if (panels >= 4 * ctas) return launch_multi<2, PMAX>(prods, count, s, who);
   return launch_multi<1, PMAX>(prods, count, s, who);
 }
