@@ -233,6 +233,65 @@ def _time_graph(graph, reps, stream):
     return e0.elapsed_time(e1) / reps
 
 
+# The other configurations (single products and the batched product), timed
+# one launch at a time with L2 flushed before each: cold-L2 median of `reps`.
+OTHER_CONFIGS = (
+    # name, rows, n, vectors, scale distribution, outlier fraction
+    ("gemv_256x1024", 256, 1024, 1, "halfnormal", 0.0),
+    ("gemv_4096x4096", 4096, 4096, 1, "halfnormal", 0.01),
+    ("b16_14336x4096", 14336, 4096, 16, "halfnormal", 0.0),
+    ("b16_4096x14336", 4096, 14336, 16, "halfnormal", 0.0),
+    ("b64_128256x4096", 128256, 4096, 64, "lognormal", 0.0),
+    ("b64_4096x14336", 4096, 14336, 64, "lognormal", 0.0),
+)
+
+
+def time_other_configs(dev, reps: int = 15):
+    import torch
+    from decode_q1_gemv_gb300 import binding, synth
+
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for ci, (name, rows, n, nvec, scale, outl) in enumerate(OTHER_CONFIGS):
+        blocks = synth.weight_blocks(synth.rng_for(11, ci, 0), rows, n, scale)
+        x = synth.activations(synth.rng_for(11, ci, 1), nvec, n, outliers=outl)
+        packed = binding.pack(torch.from_numpy(blocks).to(dev), rows, n)
+        q, d = binding.quantize(torch.from_numpy(x).to(dev))
+        out = torch.empty((nvec, rows), dtype=torch.float32, device=dev)
+
+        def launch():
+            if nvec == 1:
+                binding.gemv(packed, rows, n, q[0], d[0], out[0])
+            else:
+                binding.gemm_small(packed, rows, n, q, d, out)
+
+        for _ in range(3):
+            launch()
+        ts = []
+        for _ in range(reps):
+            flush.add_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        ts.sort()
+        us = ts[len(ts) // 2]
+        wbytes = rows * n * 18 // 128
+        entry = {"rows": rows, "n": n, "vectors": nvec, "us": round(us, 2), "us_min": round(ts[0], 2),
+                 "weight_gbs": round(wbytes / (us * 1e-6) / 1e9, 1)}
+        if nvec > 1:
+            # lane-chain work of the exact contract: 0.5 fp32 ops per weight per vector
+            entry["weight_vector_products_per_s"] = round(rows * n * nvec / (us * 1e-6), 0)
+        res[name] = entry
+        del packed, q, d, out
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -321,6 +380,10 @@ def run_ours(args):
     barrier()
     e2e_ms = reduce_max(x0.elapsed_time(x1) / args.steps)
 
+    other = None
+    if rank == 0 and args.configs:
+        other = time_other_configs(dev)
+
     wb = ds.weight_bytes
     peak, peak_kind = measured_peaks()
     value = world * wb / (step_ms * 1e-3) / 1e9
@@ -345,6 +408,7 @@ def run_ours(args):
                        "l2": "inputs larger than L2: each step streams 1.055 GB of weights",
                        "parallelism": f"replicas x{world}"},
             "us_per_set": round(step_ms * 1e3, 2),
+            "other_configs_cold_l2": other,
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "us_per_set_by_schedule": sched_us,
             "launches_by_schedule": {sch: ds.launches(sch) for sch in schedules},
@@ -373,6 +437,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU-oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip timing the single-product and batched configurations")
     ap.add_argument("--layers", type=int, default=32, help="layers of the decode set (32 = full set with lm_head)")
     ap.add_argument("--schedules", default="grouped,decode,separate",
                     help="schedules timed besides 'set' (comma list; empty for none)")

@@ -165,8 +165,12 @@ extern "C" int q1_0_gemm_small(const void* packed, int64_t rows, int64_t n, int6
   ProdArgs a = make_args(packed, rows, n, nvec, q, d, out);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t panels = a.panels;
+  // Four rows per thread amortize each activation-table load over four rows
+  // (one row per thread leaves the loop bound by shared-memory loads).  Four
+  // vectors per CTA, or two when that leaves fewer than two CTAs per SM.
   if (nvec == 1) return launch<1, 1>(a, panels, s, "q1_0_gemm_small launch");
-  if (nvec <= 2) return launch<2, 2>(a, panels, s, "q1_0_gemm_small launch");
-  if (nvec <= 4) return launch<2, 4>(a, panels, s, "q1_0_gemm_small launch");
-  return launch<1, 8>(a, panels, s, "q1_0_gemm_small launch");
+  const int64_t pgroups = (panels + 3) / 4;
+  if (nvec <= 2 || pgroups * ((nvec + 3) / 4) < 2 * int64_t(num_sms()))
+    return launch<4, 2>(a, panels, s, "q1_0_gemm_small launch");
+  return launch<4, 4>(a, panels, s, "q1_0_gemm_small launch");
 }
