@@ -292,6 +292,18 @@ def time_other_configs(dev, reps: int = 15):
     return res
 
 
+def run_configs_only(args):
+    import torch
+
+    torch.cuda.set_device(0)
+    from decode_q1_gemv_gb300 import binding
+
+    binding.load()
+    res = time_other_configs(torch.device("cuda", 0), reps=max(args.steps, 1))
+    print(json.dumps({"other_configs_cold_l2": res}), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -439,6 +451,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip timing the single-product and batched configurations")
+    ap.add_argument("--configs-only", action="store_true",
+                    help="time only the single-product and batched configurations (for profiling)")
     ap.add_argument("--layers", type=int, default=32, help="layers of the decode set (32 = full set with lm_head)")
     ap.add_argument("--schedules", default="grouped,decode,separate",
                     help="schedules timed besides 'set' (comma list; empty for none)")
@@ -447,6 +461,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.configs_only:
+        return run_configs_only(args)
     return run_ours(args)
 
 
