@@ -43,11 +43,11 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
 
   pdl_wait();
 
-  uint64_t acc[V][R];
+  float accE[V][R], accO[V][R];  // lane w and lane w+4 chains
 #pragma unroll
   for (int v = 0; v < V; ++v)
 #pragma unroll
-    for (int j = 0; j < R; ++j) acc[v][j] = 0ull;  // both lanes +0
+    for (int j = 0; j < R; ++j) accE[v][j] = accO[v][j] = 0.0f;
 
   for (int blk0 = 0; blk0 < a.nbp; blk0 += a.kc) {
     const int kcb = min(a.kc, a.nbp - blk0);
@@ -79,24 +79,19 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
       for (int v = 0; v < V; ++v) {
         const unsigned char* t = smem + v * tb;
         quad_all<R>(wv, sc, reinterpret_cast<const uint4*>(t) + (b - blk0) * 16,
-                    reinterpret_cast<const float4*>(t + table_dk_offset(a.kc)) + (b - blk0) * 4, w, acc[v]);
+                    reinterpret_cast<const float4*>(t + table_dk_offset(a.kc)) + (b - blk0) * 4, w, accE[v],
+                    accO[v]);
       }
     }
   }
 
   pdl_launch_dependents();
-  // Horizontal sum: thread w holds (a_w, a_w+4) and adds them; xor 2 then
-  // gives (a0+a4)+(a2+a6) and (a1+a5)+(a3+a7), xor 1 joins the two.
 #pragma unroll
   for (int j = 0; j < R; ++j) {
     const int64_t row = int64_t(p0 + j) * kPanel + prow;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      float lo, hi;
-      f2unpack(acc[v][j], lo, hi);
-      float r = __fadd_rn(lo, hi);
-      r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, 2));
-      r = __fadd_rn(r, __shfl_xor_sync(0xffffffffu, r, 1));
+      const float r = row_sum(accE[v][j], accO[v][j]);
       if (w == 0 && p0 + j < a.panels && row < a.rows && v0 + v < a.nvec)
         a.out[int64_t(v0 + v) * a.rows + row] = r;
     }

@@ -208,9 +208,9 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
     }
     for (int t = t_lo; t < t_hi && ok; ++t) {
       if (j == last_j && t == last_t) pdl_launch_dependents();
-      uint64_t acc[R];
+      float accE[R], accO[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) acc[r] = 0ull;  // both lanes +0
+      for (int r = 0; r < R; ++r) accE[r] = accO[r] = 0.0f;
 
       for (int qd = 0; qd < quads; ++qd, ++it) {
         const int b0 = qd * 4;
@@ -239,18 +239,12 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&bars[S + s]));  // stage consumed
 
-        quad_all<R>(wv, sc, QC + gb * 16, DK + gb * 4, w, acc);
+        quad_all<R>(wv, sc, QC + gb * 16, DK + gb * 4, w, accE, accO);
       }
       if (!ok) break;
-      // Horizontal sum: thread w holds (a_w, a_w+4) and adds them; xor 2 then
-      // gives (a0+a4)+(a2+a6) and (a1+a5)+(a3+a7), xor 1 joins the two.
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        float lo2, hi2;
-        f2unpack(acc[r], lo2, hi2);
-        float sum = __fadd_rn(lo2, hi2);
-        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
-        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
+        const float sum = row_sum(accE[r], accO[r]);
         const int64_t row = (int64_t(t) * kSlots * R + kSlots * r + ps) * kPanel + prow;
         if (w == 0 && row < prows) pout[row] = sum;
       }

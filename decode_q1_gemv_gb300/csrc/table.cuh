@@ -127,29 +127,6 @@ static __device__ __noinline__ void build_table_x(const float* __restrict__ x, i
   }
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-__device__ __forceinline__ float half_of(const uint4& v, int i) {
-  const uint32_t w = word_of(v, i >> 1);
-  const uint16_t h = uint16_t((i & 1) ? (w >> 16) : (w & 0xffffu));
-  return __half2float(__ushort_as_half(h));
-}
-
-// One sub-block step for one row and one word (lanes w and w+4): masks the
-// row's word W to the two lanes' planes, forms the exact products d1*s for
-// both lanes and returns them as a float pair (lane w, lane w+4).
-template <int K>
-__device__ __forceinline__ uint64_t subblock_products(uint32_t W, const uint4& qc, uint64_t dpair, uint64_t kpair) {
-  uint32_t m0 = W & (0x01010101u << (2 * K));
-  const uint32_t m1 = W & (0x01010101u << (2 * K + 1));
-  if constexpr (K == 0) m0 <<= 1;  // plane 0 is used as plane 1 (byte values 0/2)
-  const uint32_t D0 = dp4a_us(m0, qc.x, qc.z);
-  const uint32_t D1 = dp4a_us(m1, qc.y, qc.w);
-  return fma2(dpair, f2pack(__uint_as_float(D0), __uint_as_float(D1)), kpair);
-}
-
 template <int I>
 __device__ __forceinline__ uint32_t word_at(const uint4& v) {
   if constexpr (I == 0) return v.x;
@@ -165,48 +142,73 @@ __device__ __forceinline__ float quad_scale(const uint2& v) {
   return __half2float(__ushort_as_half(uint16_t((I & 1) ? (w >> 16) : (w & 0xffffu))));
 }
 
-// Sub-block K of block BQ of a quad for R rows: ab[r] = d1*s (K = 0) or
-// add.rn(ab[r], d1*s) (K > 0).  QCq/DKq point at the quad's first sub-block.
+// Sub-block K of block BQ of a quad for R rows and one word (lanes w and
+// w+4): masks each row's word to the two lanes' planes and forms the exact
+// products d1*s, then ab = d1*s (K = 0) or add.rn(ab, d1*s) (K > 0) for lane
+// w (abE) and lane w+4 (abO).  QCq/DKq point at the quad's first sub-block.
+// The chains are scalar f32 operations: the dp4a already occupies the
+// FMA-heavy pipe, and scalar fma/add can issue to either FMA pipe, where the
+// paired f32x2 forms load the heavy pipe as well.
 template <int R, int BQ, int K>
 __device__ __forceinline__ void quad_subblock(const uint4 (&wv)[R], const uint4* QCq, const float4* DKq, int w,
-                                              uint64_t (&ab)[R]) {
+                                              float (&abE)[R], float (&abO)[R]) {
   const uint4 qc = QCq[(BQ * 4 + K) * 4 + w];
   const float4 dk = DKq[BQ * 4 + K];
-  const uint64_t dpair = f2pack(dk.x, dk.y);
-  const uint64_t kpair = f2pack(dk.z, dk.w);
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const uint64_t pr = subblock_products<K>(word_at<BQ>(wv[r]), qc, dpair, kpair);
-    if constexpr (K == 0) ab[r] = pr;
-    else ab[r] = add2(ab[r], pr);
+    const uint32_t W = word_at<BQ>(wv[r]);
+    uint32_t m0 = W & (0x01010101u << (2 * K));
+    const uint32_t m1 = W & (0x01010101u << (2 * K + 1));
+    if constexpr (K == 0) m0 <<= 1;  // plane 0 is used as plane 1 (byte values 0/2)
+    const float pE = __fmaf_rn(dk.x, __uint_as_float(dp4a_us(m0, qc.x, qc.z)), dk.z);
+    const float pO = __fmaf_rn(dk.y, __uint_as_float(dp4a_us(m1, qc.y, qc.w)), dk.w);
+    if constexpr (K == 0) {
+      abE[r] = pE;
+      abO[r] = pO;
+    } else {
+      abE[r] = __fadd_rn(abE[r], pE);
+      abO[r] = __fadd_rn(abO[r], pO);
+    }
   }
 }
 
 // Block BQ of a quad for R rows: the four sub-blocks, then the outer
-// acc = fma(d0, ab, acc) with d0 the row's block scale.
+// acc = fma(d0, ab, acc) with d0 the row's block scale, per lane.
 template <int R, int BQ>
 __device__ __forceinline__ void quad_block(const uint4 (&wv)[R], const uint2 (&sc)[R], const uint4* QCq,
-                                           const float4* DKq, int w, uint64_t (&acc)[R]) {
-  uint64_t ab[R];
-  quad_subblock<R, BQ, 0>(wv, QCq, DKq, w, ab);
-  quad_subblock<R, BQ, 1>(wv, QCq, DKq, w, ab);
-  quad_subblock<R, BQ, 2>(wv, QCq, DKq, w, ab);
-  quad_subblock<R, BQ, 3>(wv, QCq, DKq, w, ab);
+                                           const float4* DKq, int w, float (&accE)[R], float (&accO)[R]) {
+  float abE[R], abO[R];
+  quad_subblock<R, BQ, 0>(wv, QCq, DKq, w, abE, abO);
+  quad_subblock<R, BQ, 1>(wv, QCq, DKq, w, abE, abO);
+  quad_subblock<R, BQ, 2>(wv, QCq, DKq, w, abE, abO);
+  quad_subblock<R, BQ, 3>(wv, QCq, DKq, w, abE, abO);
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const float d0 = quad_scale<BQ>(sc[r]);
-    acc[r] = fma2(f2pack(d0, d0), ab[r], acc[r]);
+    accE[r] = __fmaf_rn(d0, abE[r], accE[r]);
+    accO[r] = __fmaf_rn(d0, abO[r], accO[r]);
   }
 }
 
-// A whole quad (4 blocks) for R rows.
+// A whole quad (4 blocks) for R rows: accE[r] is lane w's chain of row r,
+// accO[r] lane w+4's.
 template <int R>
 __device__ __forceinline__ void quad_all(const uint4 (&wv)[R], const uint2 (&sc)[R], const uint4* QCq,
-                                         const float4* DKq, int w, uint64_t (&acc)[R]) {
-  quad_block<R, 0>(wv, sc, QCq, DKq, w, acc);
-  quad_block<R, 1>(wv, sc, QCq, DKq, w, acc);
-  quad_block<R, 2>(wv, sc, QCq, DKq, w, acc);
-  quad_block<R, 3>(wv, sc, QCq, DKq, w, acc);
+                                         const float4* DKq, int w, float (&accE)[R], float (&accO)[R]) {
+  quad_block<R, 0>(wv, sc, QCq, DKq, w, accE, accO);
+  quad_block<R, 1>(wv, sc, QCq, DKq, w, accE, accO);
+  quad_block<R, 2>(wv, sc, QCq, DKq, w, accE, accO);
+  quad_block<R, 3>(wv, sc, QCq, DKq, w, accE, accO);
+}
+
+// Horizontal sum of a row: thread w holds (a_w, a_w+4) and adds them; xor 2
+// then gives (a0+a4)+(a2+a6) and (a1+a5)+(a3+a7), xor 1 joins the two.  All
+// 32 lanes of the warp take part; the row's sum ends up in every thread of
+// its group of four.
+__device__ __forceinline__ float row_sum(float accE, float accO) {
+  float sum = __fadd_rn(accE, accO);
+  sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
+  return __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
 }
 
 }  // namespace q1
