@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
     for (int v = 0; v < V; ++v) {
       unsigned char* t = smem + v * tb;
       const int vv = min(v0 + v, a.nvec - 1);
-      build_table_q(a.q + int64_t(vv) * a.n, a.d1 + int64_t(vv) * (a.n / kSub), a.nb, blk0, kcb, t,
+      build_table_q<4>(a.q + int64_t(vv) * a.n, a.d1 + int64_t(vv) * (a.n / kSub), a.nb, blk0, kcb, t,
                     threadIdx.x, kThreads, a.kc);
     }
     __syncthreads();

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
   constexpr int kConsumerWarps = consumer_warps<R>();
   constexpr int kConsumers = consumers<R>();
   constexpr int TB = kSlots * R * kQuadBits;  // bits part of a stage
+  constexpr int kTableBatch = R >= 8 ? 8 : 4;  // load rounds in flight while a table is built
   unsigned char* table = smem + S * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(table + table_bytes(a.kc));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -202,8 +203,8 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
     const bool one_chunk = pnbp <= kc;
     if (one_chunk) {
       named_barrier(kConsumerBarrier, kConsumers);  // previous product's table no longer read
-      if (px) build_table_x(px, pnb, 0, pnbp, table, tid, kConsumers, kc);
-      else build_table_q(pq, pd, pnb, 0, pnbp, table, tid, kConsumers, kc);
+      if (px) build_table_x<kTableBatch>(px, pnb, 0, pnbp, table, tid, kConsumers, kc);
+      else build_table_q<kTableBatch>(pq, pd, pnb, 0, pnbp, table, tid, kConsumers, kc);
       named_barrier(kConsumerBarrier, kConsumers);
     }
     for (int t = t_lo; t < t_hi && ok; ++t) {
@@ -217,8 +218,8 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
         if (!one_chunk && b0 % kc == 0) {
           named_barrier(kConsumerBarrier, kConsumers);
           const int kcb = min(kc, pnbp - b0);
-          if (px) build_table_x(px, pnb, b0, kcb, table, tid, kConsumers, kc);
-          else build_table_q(pq, pd, pnb, b0, kcb, table, tid, kConsumers, kc);
+          if (px) build_table_x<kTableBatch>(px, pnb, b0, kcb, table, tid, kConsumers, kc);
+          else build_table_q<kTableBatch>(pq, pd, pnb, b0, kcb, table, tid, kConsumers, kc);
           named_barrier(kConsumerBarrier, kConsumers);
         }
         const int gb = one_chunk ? b0 : b0 % kc;  // block index within the table

@@ -51,33 +51,59 @@ __device__ __forceinline__ void scale_consts(float d1, int k, int par, float& dp
 
 // Table for blocks [blk0, blk0 + kcb) from a quantized activation (q int8 [n],
 // d fp16 [n/32]).  Sub-blocks past the activation's end get zero constants.
+// Both builders issue the global loads of kTableBatch rounds (a round: one
+// entry per thread) before using any of them, so their latencies overlap; a
+// larger batch holds more registers across the call, and the caller picks the
+// largest that its kernel affords without spilling.
+template <int kTableBatch>
 static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, const uint16_t* __restrict__ d1,
                                               int nb, int blk0, int kcb, unsigned char* table, int tid,
                                               int nthreads, int kc) {
   uint4* QC = reinterpret_cast<uint4*>(table);
   float4* DK = reinterpret_cast<float4*>(table + table_dk_offset(kc));
   const int nsub = nb * 4;
-  for (int t = tid; t < kcb * 16; t += nthreads) {
-    const int g = t >> 2, w = t & 3;
-    const int G = blk0 * 4 + g;
-    const int k = g & 3;
-    uint32_t qp[2], ci[2];
+  for (int base = 0; base < kcb * 16; base += kTableBatch * nthreads) {
+    uint32_t wb[kTableBatch][2];
 #pragma unroll
-    for (int par = 0; par < 2; ++par) {
-      uint32_t word = 0u;
-      if (G < nsub) word = *reinterpret_cast<const uint32_t*>(q + int64_t(G) * kSub + 4 * (w + 4 * par));
-      lane_consts(word, k, par, qp[par], ci[par]);
+    for (int u = 0; u < kTableBatch; ++u) {
+      const int t = base + u * nthreads + tid;
+      const int G = blk0 * 4 + (t >> 2), w = t & 3;
+#pragma unroll
+      for (int par = 0; par < 2; ++par) {
+        wb[u][par] = 0u;
+        if (t < kcb * 16 && G < nsub)
+          wb[u][par] = *reinterpret_cast<const uint32_t*>(q + int64_t(G) * kSub + 4 * (w + 4 * par));
+      }
     }
-    QC[g * 4 + w] = make_uint4(qp[0], qp[1], ci[0], ci[1]);
+#pragma unroll
+    for (int u = 0; u < kTableBatch; ++u) {
+      const int t = base + u * nthreads + tid;
+      if (t >= kcb * 16) break;
+      const int g = t >> 2, w = t & 3;
+      uint32_t qp[2], ci[2];
+#pragma unroll
+      for (int par = 0; par < 2; ++par) lane_consts(wb[u][par], g & 3, par, qp[par], ci[par]);
+      QC[g * 4 + w] = make_uint4(qp[0], qp[1], ci[0], ci[1]);
+    }
   }
-  for (int g = tid; g < kcb * 4; g += nthreads) {
-    const int G = blk0 * 4 + g;
-    const int k = g & 3;
-    const float dv = (G < nsub) ? __half2float(__ushort_as_half(d1[G])) : 0.0f;
-    float de, dodd, ke, ko;
-    scale_consts(dv, k, 0, de, ke);
-    scale_consts(dv, k, 1, dodd, ko);
-    DK[g] = make_float4(de, dodd, ke, ko);
+  for (int base = 0; base < kcb * 4; base += kTableBatch * nthreads) {
+    uint16_t hb[kTableBatch];
+#pragma unroll
+    for (int u = 0; u < kTableBatch; ++u) {
+      const int g = base + u * nthreads + tid;
+      const int G = blk0 * 4 + g;
+      hb[u] = (g < kcb * 4 && G < nsub) ? d1[G] : uint16_t(0);
+    }
+#pragma unroll
+    for (int u = 0; u < kTableBatch; ++u) {
+      const int g = base + u * nthreads + tid;
+      if (g >= kcb * 4) break;
+      const float dv = __half2float(__ushort_as_half(hb[u]));
+      float de, dodd, ke, ko;
+      scale_consts(dv, g & 3, 0, de, ke);
+      scale_consts(dv, g & 3, 1, dodd, ko);
+      DK[g] = make_float4(de, dodd, ke, ko);
+    }
   }
 }
 
@@ -86,42 +112,52 @@ static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, 
 // amax/127, id = d ? 1/d : 0, q = roundf(x*id), scale fp16(d)).  One thread per
 // (sub-block, lane); the 8 threads of a sub-block are consecutive in a warp.
 // nthreads must be a multiple of 32 and every thread of the group must call.
+template <int kTableBatch>
 static __device__ __noinline__ void build_table_x(const float* __restrict__ x, int nb, int blk0, int kcb,
                                               unsigned char* table, int tid, int nthreads, int kc) {
   uint32_t* QCw = reinterpret_cast<uint32_t*>(table);
   float* DKf = reinterpret_cast<float*>(table + table_dk_offset(kc));
   const int nsub = nb * 4;
   const int total = kcb * 4 * 8;
-  for (int base = 0; base < total; base += nthreads) {  // same trip count for every thread
-    const int t = base + tid;
-    const int g = t >> 3, l = t & 7;
-    const int G = blk0 * 4 + g;
-    const bool live = t < total && G < nsub;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live) v = *reinterpret_cast<const float4*>(x + int64_t(G) * kSub + 4 * l);
-    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    const float dd = __fdiv_rn(amax, 127.0f);
-    const float id = (dd != 0.0f) ? __fdiv_rn(1.0f, dd) : 0.0f;
-    const uint32_t q0 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.x, id)))) & 0xffu;
-    const uint32_t q1 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.y, id)))) & 0xffu;
-    const uint32_t q2 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.z, id)))) & 0xffu;
-    const uint32_t q3 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.w, id)))) & 0xffu;
-    const uint32_t word = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
-    const float d1 = __half2float(__float2half_rn(dd));
-    if (t < total) {
-      const int k = g & 3, par = l >> 2, w = l & 3;
-      uint32_t qp, ci;
-      lane_consts(word, k, par, qp, ci);
-      QCw[(g * 4 + w) * 4 + par] = qp;
-      QCw[(g * 4 + w) * 4 + 2 + par] = ci;
-      if ((l & 3) == 0) {
-        float dprime, K;
-        scale_consts(G < nsub ? d1 : 0.0f, k, par, dprime, K);
-        DKf[g * 4 + par] = dprime;
-        DKf[g * 4 + 2 + par] = K;
+  for (int base = 0; base < total; base += kTableBatch * nthreads) {  // same trip count for every thread
+    float4 vb[kTableBatch];
+#pragma unroll
+    for (int u = 0; u < kTableBatch; ++u) {
+      const int t = base + u * nthreads + tid;
+      const int G = blk0 * 4 + (t >> 3);
+      vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < total && G < nsub) vb[u] = *reinterpret_cast<const float4*>(x + int64_t(G) * kSub + 4 * (t & 7));
+    }
+#pragma unroll
+    for (int u = 0; u < kTableBatch; ++u) {
+      const int t = base + u * nthreads + tid;
+      const int g = t >> 3, l = t & 7;
+      const int G = blk0 * 4 + g;
+      const float4 v = vb[u];
+      float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+      const float dd = __fdiv_rn(amax, 127.0f);
+      const float id = (dd != 0.0f) ? __fdiv_rn(1.0f, dd) : 0.0f;
+      const uint32_t q0 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.x, id)))) & 0xffu;
+      const uint32_t q1 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.y, id)))) & 0xffu;
+      const uint32_t q2 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.z, id)))) & 0xffu;
+      const uint32_t q3 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.w, id)))) & 0xffu;
+      const uint32_t word = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+      const float d1 = __half2float(__float2half_rn(dd));
+      if (t < total) {
+        const int k = g & 3, par = l >> 2, w = l & 3;
+        uint32_t qp, ci;
+        lane_consts(word, k, par, qp, ci);
+        QCw[(g * 4 + w) * 4 + par] = qp;
+        QCw[(g * 4 + w) * 4 + 2 + par] = ci;
+        if ((l & 3) == 0) {
+          float dprime, K;
+          scale_consts(G < nsub ? d1 : 0.0f, k, par, dprime, K);
+          DKf[g * 4 + par] = dprime;
+          DKf[g * 4 + 2 + par] = K;
+        }
       }
     }
   }
