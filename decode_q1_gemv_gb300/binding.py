@@ -31,7 +31,8 @@ Q1_MISMATCH = 2
 
 # Every symbol include/q1gemv.h declares (checked by the tests).
 EXPORTS = ("q1_last_error", "q1_0_packed_bytes", "q1_0_pack", "q1_0_unpack", "q8_quantize_act",
-           "q1_0_gemv", "q1_0_gemv_multi", "q1_0_gemm_small", "q1_0_verify", "q1_device_status")
+           "q1_0_gemv", "q1_0_gemv_multi", "q1_0_gemv_multi_plan", "q1_0_gemm_small", "q1_0_verify",
+           "q1_device_status")
 
 MAX_PRODUCTS = 256
 
@@ -41,6 +42,12 @@ class Product(ctypes.Structure):
     _fields_ = [("packed", ctypes.c_void_p), ("rows", ctypes.c_int64), ("n", ctypes.c_int64),
                 ("x", ctypes.c_void_p), ("q", ctypes.c_void_p), ("d", ctypes.c_void_p),
                 ("out", ctypes.c_void_p)]
+
+
+class MultiPlan(ctypes.Structure):
+    """Mirror of q1_multi_plan (include/q1gemv.h)."""
+    _fields_ = [("rows_per_thread", ctypes.c_int), ("grid", ctypes.c_int), ("total_cost", ctypes.c_int64),
+                ("max_range_cost", ctypes.c_int64)]
 
 
 class Q1Error(RuntimeError):
@@ -82,6 +89,9 @@ def load():
         lib.q1_0_gemv.restype = I
         lib.q1_0_gemv_multi.argtypes = [ctypes.POINTER(Product), I, P]
         lib.q1_0_gemv_multi.restype = I
+        lib.q1_0_gemv_multi_plan.argtypes = [ctypes.POINTER(Product), I, I, ctypes.POINTER(MultiPlan),
+                                             ctypes.POINTER(I64), I]
+        lib.q1_0_gemv_multi_plan.restype = I
         lib.q1_0_gemm_small.argtypes = [P, I64, I64, I64, P, P, P, P]
         lib.q1_0_gemm_small.restype = I
         lib.q1_device_status.argtypes = [I]
@@ -208,6 +218,21 @@ def gemv_multi(items=None, stream=None, array=None):
     takes them, or a prebuilt `array` (to avoid rebuilding it per call)."""
     arr = array if array is not None else product_array(items)
     _check(load().q1_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q1_0_gemv_multi")
+
+
+def multi_plan(shapes, sms: int = 0) -> dict:
+    """The work split q1_0_gemv_multi would make for products of the given
+    (rows, n) shapes, in list order, on `sms` SMs (0 = the current device).
+    Nothing is launched; needs no GPU when sms > 0."""
+    arr = (Product * len(shapes))()
+    for i, (rows, n) in enumerate(shapes):
+        arr[i] = Product(None, int(rows), int(n), None, None, None, None)
+    plan = MultiPlan()
+    cuts = (ctypes.c_int64 * (2 * max(int(sms), 4096) + 1))()
+    _check(load().q1_0_gemv_multi_plan(arr, len(arr), int(sms), ctypes.byref(plan), cuts, len(cuts)),
+           "q1_0_gemv_multi_plan")
+    return {"rows_per_thread": plan.rows_per_thread, "grid": plan.grid, "total_cost": plan.total_cost,
+            "max_range_cost": plan.max_range_cost, "cuts": list(cuts[:plan.grid + 1])}
 
 
 def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tensor,

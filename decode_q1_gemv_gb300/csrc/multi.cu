@@ -60,12 +60,16 @@ struct MProd {
   int rows, nb, nbp, panels, tiles;
 };
 
+constexpr int kMaxCuts = 512;  // CTAs of a many-product launch that get host-computed ranges
+
 template <int PMAX>
 struct MArgs {
   MProd p[PMAX];
   int64_t total_cost;
   int count;
   int kc;                // table chunk in blocks (multiple of 4)
+  int ncut;              // 0: equal split of the cost axis; else CTA b owns [cut[b], cut[b+1])
+  int64_t cut[PMAX > 8 ? kMaxCuts + 1 : 1];
 };
 
 // Ring of stages: a stage is one quad of blocks for the tile's slots*R panels;
@@ -81,7 +85,7 @@ __host__ __device__ constexpr int multi_smem_bytes(int kc) {
 }
 
 // Tiles [t_lo, t_hi) of product p that fall in this CTA's cost range.
-__device__ __forceinline__ void tile_range(const MProd& p, int64_t lo, int64_t hi, int& t_lo, int& t_hi) {
+__host__ __device__ __forceinline__ void tile_range(const MProd& p, int64_t lo, int64_t hi, int& t_lo, int& t_hi) {
   const int64_t c = p.nbp;
   auto first_at_or_after = [&](int64_t v) -> int {
     int64_t t = v <= p.cost_begin ? 0 : (v - p.cost_begin + c - 1) / c;
@@ -119,8 +123,14 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
   unsigned char* table = smem + S * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(table + table_bytes(a.kc));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t lo = a.total_cost * int64_t(blockIdx.x) / int64_t(gridDim.x);
-  const int64_t hi = a.total_cost * int64_t(blockIdx.x + 1) / int64_t(gridDim.x);
+  int64_t lo = a.total_cost * int64_t(blockIdx.x) / int64_t(gridDim.x);
+  int64_t hi = a.total_cost * int64_t(blockIdx.x + 1) / int64_t(gridDim.x);
+  if constexpr (PMAX > 8) {
+    if (a.ncut) {
+      lo = a.cut[blockIdx.x];
+      hi = a.cut[blockIdx.x + 1];
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -269,10 +279,57 @@ static int set_smem_attr() {
   return Q1_OK;
 }
 
+// Cuts of the cost axis at tile boundaries for at most G contiguous ranges
+// whose largest cost is at most V, filled greedily in product order; false if
+// V does not suffice.  cut[0..nseg] receives the boundaries when non-null.
+template <int PMAX>
+static bool fill_ranges(const MArgs<PMAX>& a, int64_t V, int G, int64_t* cut, int& nseg) {
+  int seg = 0;
+  int64_t cur = 0, pos = 0;
+  if (cut) cut[0] = 0;
+  for (int j = 0; j < a.count; ++j) {
+    const int64_t c = a.p[j].nbp;
+    if (c > V) return false;
+    int64_t left = a.p[j].tiles;
+    while (left > 0) {
+      const int64_t k = std::min(left, (V - cur) / c);
+      if (k == 0) {
+        if (++seg >= G) return false;
+        if (cut) cut[seg] = pos;
+        cur = 0;
+        continue;
+      }
+      cur += k * c;
+      pos += k * c;
+      left -= k;
+    }
+  }
+  nseg = seg + 1;
+  if (cut) cut[nseg] = pos;
+  return true;
+}
+
+// The smallest largest-range cost V for G contiguous ranges: the equal share
+// rounded up always fits once a whole tile is added, so V is searched in
+// [share, share + largest tile cost].
+template <int PMAX>
+static int balanced_ranges(MArgs<PMAX>& a, int G, int64_t max_tile) {
+  int64_t lo = (a.total_cost + G - 1) / G, hi = lo + max_tile;
+  int nseg = 0;
+  while (lo < hi) {
+    const int64_t m = (lo + hi) / 2;
+    if (fill_ranges(a, m, G, nullptr, nseg)) hi = m;
+    else lo = m + 1;
+  }
+  fill_ranges(a, lo, G, a.cut, nseg);
+  a.ncut = nseg;
+  return nseg;
+}
+
+// The launch plan of k_q1_multi<R, PMAX> for `count` products on `sms` SMs:
+// the kernel arguments and the grid.
 template <int R, int PMAX>
-static int launch_multi(const q1_product* prods, int count, cudaStream_t s, const char* who) {
-  if (int e = set_smem_attr<R, PMAX>()) return e;
-  MArgs<PMAX> a;
+static void plan_multi(const q1_product* prods, int count, int sms, MArgs<PMAX>& a, int& grid) {
   int64_t cost = 0;
   int64_t total_tiles = 0;
   int max_nbp = 8;
@@ -298,7 +355,23 @@ static int launch_multi(const q1_product* prods, int count, cudaStream_t s, cons
   a.total_cost = cost;
   a.count = count;
   a.kc = std::min(max_nbp, kMaxKc);
-  const int grid = int(std::min<int64_t>(total_tiles, 2 * num_sms()));
+  a.ncut = 0;
+  grid = int(std::min<int64_t>(total_tiles, 2 * int64_t(sms)));
+  // Many products of unequal tile costs: an equal split of the cost axis,
+  // rounded to whole tiles, leaves up to a tile's cost of imbalance per CTA;
+  // the host places the boundaries so that the largest range is as small as
+  // contiguous ranges allow.
+  if constexpr (PMAX > 8) {
+    if (grid <= kMaxCuts) grid = balanced_ranges(a, grid, max_nbp);
+  }
+}
+
+template <int R, int PMAX>
+static int launch_multi(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+  if (int e = set_smem_attr<R, PMAX>()) return e;
+  MArgs<PMAX> a;
+  int grid = 0;
+  plan_multi<R, PMAX>(prods, count, num_sms(), a, grid);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(multi_threads<R>());
@@ -312,15 +385,63 @@ static int launch_multi(const q1_product* prods, int count, cudaStream_t s, cons
   return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_multi<R, PMAX>, a), who);
 }
 
+// The plan reported by q1_0_gemv_multi_plan: the CTA ranges exactly as the
+// kernel derives them from the arguments, and their tile costs.
+template <int R, int PMAX>
+static int report_plan(const q1_product* prods, int count, int sms, q1_multi_plan* out, int64_t* cuts,
+                       int max_cuts) {
+  MArgs<PMAX>* a = new MArgs<PMAX>;
+  int grid = 0;
+  plan_multi<R, PMAX>(prods, count, sms, *a, grid);
+  out->rows_per_thread = R;
+  out->grid = grid;
+  out->total_cost = a->total_cost;
+  out->max_range_cost = 0;
+  for (int b = 0; b < grid; ++b) {
+    int64_t lo = a->total_cost * b / grid, hi = a->total_cost * (b + 1) / grid;
+    if (a->ncut) {
+      lo = a->cut[b];
+      hi = a->cut[b + 1];
+    }
+    int64_t c = 0;
+    for (int j = 0; j < count; ++j) {
+      int t_lo, t_hi;
+      tile_range(a->p[j], lo, hi, t_lo, t_hi);
+      c += int64_t(t_hi - t_lo) * a->p[j].nbp;
+    }
+    out->max_range_cost = std::max(out->max_range_cost, c);
+    if (cuts && b < max_cuts) cuts[b] = lo;
+    if (cuts && b + 1 < max_cuts && b == grid - 1) cuts[b + 1] = hi;
+  }
+  delete a;
+  return Q1_OK;
+}
+
 // Rows per thread: the largest R whose tiles still give every CTA some work.
-template <int PMAX>
-static int dispatch(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+static int rows_per_thread(const q1_product* prods, int count, int sms) {
   int64_t panels = 0;
   for (int j = 0; j < count; ++j) panels += (prods[j].rows + kPanel - 1) / kPanel;
-  const int64_t ctas = 2 * int64_t(num_sms());
-  if (panels >= 8 * ctas) return launch_multi<8, PMAX>(prods, count, s, who);
-  if (panels >= 4 * ctas) return launch_multi<2, PMAX>(prods, count, s, who);
-  return launch_multi<1, PMAX>(prods, count, s, who);
+  const int64_t ctas = 2 * int64_t(sms);
+  return panels >= 8 * ctas ? 8 : panels >= 4 * ctas ? 2 : 1;
+}
+
+template <int PMAX>
+static int dispatch(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+  switch (rows_per_thread(prods, count, num_sms())) {
+    case 8: return launch_multi<8, PMAX>(prods, count, s, who);
+    case 2: return launch_multi<2, PMAX>(prods, count, s, who);
+    default: return launch_multi<1, PMAX>(prods, count, s, who);
+  }
+}
+
+template <int PMAX>
+static int dispatch_plan(const q1_product* prods, int count, int sms, q1_multi_plan* out, int64_t* cuts,
+                         int max_cuts) {
+  switch (rows_per_thread(prods, count, sms)) {
+    case 8: return report_plan<8, PMAX>(prods, count, sms, out, cuts, max_cuts);
+    case 2: return report_plan<2, PMAX>(prods, count, sms, out, cuts, max_cuts);
+    default: return report_plan<1, PMAX>(prods, count, sms, out, cuts, max_cuts);
+  }
 }
 
 int num_sms() {
@@ -371,6 +492,25 @@ extern "C" int q1_0_gemv(const void* packed, int64_t rows, int64_t n, const int8
   if (!q || !d) return fail(Q1_ERR_ARG, "q1_0_gemv: null pointer");
   if (int e = check_product("q1_0_gemv", 0, p)) return e;
   return launch_products_dp4a(&p, 1, static_cast<cudaStream_t>(stream), "q1_0_gemv launch");
+}
+
+extern "C" int q1_0_gemv_multi_plan(const q1_product* products, int count, int sms, q1_multi_plan* plan,
+                                    int64_t* cuts, int max_cuts) {
+  if (!products || !plan || count < 1 || count > Q1_MAX_PRODUCTS)
+    return fail(Q1_ERR_ARG, "q1_0_gemv_multi_plan: count=%d outside 1..%d (or null list/plan)", count,
+                Q1_MAX_PRODUCTS);
+  if (sms < 0 || sms > 4096) return fail(Q1_ERR_ARG, "q1_0_gemv_multi_plan: sms=%d outside 0..4096", sms);
+  for (int j = 0; j < count; ++j) {
+    const q1_product& pr = products[j];
+    if (pr.rows < 1 || pr.rows > (int64_t(1) << 26) || pr.n < 128 || pr.n > (int64_t(1) << 24) || pr.n % 128)
+      return fail(Q1_ERR_ARG, "q1_0_gemv_multi_plan: product %d: bad shape rows=%lld n=%lld", j,
+                  (long long)pr.rows, (long long)pr.n);
+  }
+  if (cuts && max_cuts < 0) return fail(Q1_ERR_ARG, "q1_0_gemv_multi_plan: max_cuts=%d < 0", max_cuts);
+  const int n_sms = sms > 0 ? sms : num_sms();
+  if (count == 1) return dispatch_plan<1>(products, count, n_sms, plan, cuts, max_cuts);
+  if (count <= 8) return dispatch_plan<8>(products, count, n_sms, plan, cuts, max_cuts);
+  return dispatch_plan<Q1_MAX_PRODUCTS>(products, count, n_sms, plan, cuts, max_cuts);
 }
 
 extern "C" int q1_0_gemv_multi(const q1_product* products, int count, void* stream) {

@@ -125,6 +125,34 @@ typedef struct q1_product {
  * preceding kernel on `stream` has finished). */
 int q1_0_gemv_multi(const q1_product *products, int count, void *stream);
 
+/* The work split of a q1_0_gemv_multi launch, as the call would make it.
+ * Planning only: nothing is launched and no pointer in `products` is read
+ * (only rows and n; the shapes are checked as q1_0_gemv_multi checks them).
+ * A tile is rows_per_thread x 32 rows (x 2 panel slots when rows_per_thread
+ * is 1 or 2) across all of n; its cost is the product's quad-padded blocks
+ * per row.  The products' tiles are laid on one axis in list order; CTA b gets the
+ * tiles whose first block falls in its contiguous range of that axis.  With
+ * more than 8 products the host places the range boundaries so that the
+ * largest range is as small as contiguous ranges allow (a binary search over
+ * the bound, each step one greedy fill in list order); otherwise the axis is
+ * split evenly.  No counterpart in the pages: it exposes the launcher's own
+ * decision for inspection and testing.
+ *   sms      : SMs to plan for (0 = the current device's count).
+ *   plan     : HOST, receives rows per thread, grid, the total cost and the
+ *              largest cost any CTA gets.
+ *   cuts     : optional HOST int64 [max_cuts], receives the grid+1 range
+ *              boundaries (as many as fit); may be NULL.
+ * Returns Q1_OK or Q1_ERR_ARG. */
+typedef struct q1_multi_plan {
+  int rows_per_thread;    /* rows of a tile each consumer thread handles (1, 2 or 8) */
+  int grid;               /* CTAs launched                                          */
+  int64_t total_cost;     /* sum over products of tiles x padded blocks per row     */
+  int64_t max_range_cost; /* largest tile cost owned by one CTA                     */
+} q1_multi_plan;
+
+int q1_0_gemv_multi_plan(const q1_product *products, int count, int sms, q1_multi_plan *plan, int64_t *cuts,
+                         int max_cuts);
+
 /* Small-batch product: the matrix-vector product for each of nvec activation
  * vectors sharing one pass over the weights (1 <= nvec <= 64).
  *   q : device int8 [nvec][n]; d : device fp16 bits [nvec][n/32];

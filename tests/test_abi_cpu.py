@@ -110,3 +110,110 @@ def test_oracle_and_library_share_no_code():
     assert "#include \"" not in otext
     otext_py = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
     assert "import decode_q1_gemv_gb300" not in otext_py and "from decode_q1_gemv_gb300" not in otext_py
+
+
+# ------------------------------------------------- multi-product work split --
+# q1_0_gemv_multi_plan reports the launcher's split without launching; these
+# checks hold it to what the header promises, using only the shapes.
+def _tiles(shapes, rows_per_thread):
+    """(tiles, cost per tile) per product: a tile is rows_per_thread x 32 rows
+    (two panel slots below 8 rows per thread), its cost the quad-padded
+    blocks per row."""
+    panels_per_tile = 8 if rows_per_thread == 8 else 2 * rows_per_thread
+    out = []
+    for rows, n in shapes:
+        panels = -(-rows // 256) * 8
+        nbp = -(-(n // 128) // 4) * 4
+        out.append((panels // panels_per_tile, nbp))
+    return out
+
+
+def _tile_starts(tiles):
+    starts, pos = [], 0
+    for t, c in tiles:
+        for _ in range(t):
+            starts.append(pos)
+            pos += c
+    return starts, pos
+
+
+def _check_partition(plan, tiles):
+    starts, total = _tile_starts(tiles)
+    cuts = plan["cuts"]
+    assert plan["total_cost"] == total
+    assert len(cuts) == plan["grid"] + 1 and cuts[0] == 0 and cuts[-1] == total
+    assert all(a <= b for a, b in zip(cuts, cuts[1:]))
+    boundaries = set(starts) | {total}
+    # every CTA range starts on a tile boundary (or is empty at the end), so each
+    # tile belongs to exactly one CTA and the range cost is the cut difference
+    assert all(c in boundaries for c in cuts)
+    assert max(b - a for a, b in zip(cuts, cuts[1:])) == plan["max_range_cost"]
+
+
+def _best_max_range(tiles, ctas):
+    """Smallest possible largest range over contiguous splits into at most
+    `ctas` ranges at tile boundaries, by exhaustive search over the cut points
+    (tiny inputs only)."""
+    import itertools
+    costs = [c for t, c in tiles for _ in range(t)]
+    n = len(costs)
+    best = sum(costs)
+    for k in range(0, min(ctas - 1, n - 1) + 1):
+        for cut in itertools.combinations(range(1, n), k):
+            edges = (0,) + cut + (n,)
+            best = min(best, max(sum(costs[a:b]) for a, b in zip(edges, edges[1:])))
+    return best
+
+
+def test_multi_plan_decode_set_is_balanced(lib):
+    from decode_q1_gemv_gb300 import synth
+    shapes = [(rows, n) for _, rows, n in synth.decode_set_shapes()]
+    plan = binding.multi_plan(shapes, sms=152)
+    assert plan["rows_per_thread"] == 8 and 0 < plan["grid"] <= 304
+    tiles = _tiles(shapes, 8)
+    _check_partition(plan, tiles)
+    # an even split rounded to whole tiles: the largest range it leaves
+    starts, total = _tile_starts(tiles)
+    even = [0] * 304
+    for s0, (t, c) in zip(starts, [(1, c) for t, c in tiles for _ in range(t)]):
+        even[min(b for b in range(304) if total * (b + 1) // 304 > s0)] += c
+    share = -(-total // 304)
+    assert share <= plan["max_range_cost"] <= share + 112
+    assert plan["max_range_cost"] < max(even)
+
+
+def test_multi_plan_small_lists_split_evenly(lib):
+    shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
+    plan = binding.multi_plan(shapes, sms=152)
+    tiles = _tiles(shapes, plan["rows_per_thread"])
+    starts, total = _tile_starts(tiles)
+    g = plan["grid"]
+    assert plan["cuts"] == [total * b // g for b in range(g + 1)]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_multi_plan_matches_exhaustive_optimum(lib, seed):
+    """More than 8 products, few tiles: the split's largest range equals the
+    exhaustive optimum over all contiguous splits."""
+    import random
+    rnd = random.Random(seed)
+    shapes = [(rnd.choice([32, 64, 96, 256]), 128 * rnd.choice([1, 4, 8, 28, 40])) for _ in range(rnd.randint(9, 11))]
+    plan = binding.multi_plan(shapes, sms=1)
+    tiles = _tiles(shapes, plan["rows_per_thread"])
+    _check_partition(plan, tiles)
+    assert plan["max_range_cost"] == _best_max_range(tiles, min(sum(t for t, _ in tiles), 2))
+    plan3 = binding.multi_plan(shapes, sms=2)
+    tiles3 = _tiles(shapes, plan3["rows_per_thread"])
+    _check_partition(plan3, tiles3)
+    ctas = min(sum(t for t, _ in tiles3), 4)  # at most two CTAs per SM
+    assert plan3["grid"] <= ctas
+    assert plan3["max_range_cost"] == _best_max_range(tiles3, ctas)
+
+
+def test_multi_plan_rejects_bad_arguments(lib):
+    with pytest.raises(binding.Q1Error):
+        binding.multi_plan([(0, 128)], sms=4)
+    with pytest.raises(binding.Q1Error):
+        binding.multi_plan([(32, 100)], sms=4)
+    with pytest.raises(binding.Q1Error):
+        binding.multi_plan([(32, 128)], sms=-1)

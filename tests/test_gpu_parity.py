@@ -262,6 +262,36 @@ def test_gemv_multi_mixed_products():
         bits_equal(out.cpu().numpy(), w)
 
 
+@pytest.mark.parametrize("size", ["small", "large"])
+def test_gemv_multi_many_products_balanced(size):
+    """More than 8 products of unequal tile costs, so the launcher places the
+    CTA range boundaries itself: every output of every product is compared.
+    'large' has enough rows for eight rows per thread."""
+    rng0 = np.random.default_rng(131 if size == "small" else 132)
+    if size == "small":
+        shapes = [(int(rng0.integers(1, 3000)), 128 * int(rng0.choice([1, 3, 8, 32, 112]))) for _ in range(20)]
+    else:
+        shapes = [(int(rng0.choice([4096, 6144, 8192, 16384])), 128 * int(rng0.choice([1, 2, 4, 9, 16])))
+                  for _ in range(14)]
+    plan = binding.multi_plan(shapes)
+    if size == "large":
+        assert plan["rows_per_thread"] == 8
+    assert plan["max_range_cost"] < plan["total_cost"]
+    items, want = [], []
+    for i, (rows, n) in enumerate(shapes):
+        rng = synth.rng_for(130, i)
+        blocks = synth.weight_blocks(rng, rows, n, "lognormal" if i % 2 else "halfnormal")
+        x = synth.activations(rng, 1, n, outliers=0.01)
+        q, d = oracle.q8_quantize(x)
+        out = torch.full((rows,), float("nan"), device="cuda")
+        items.append((binding.pack(dev(blocks), rows, n), rows, n, dev(x[0]), None, None, out))
+        want.append(oracle.gemv(blocks, q[0], d[0]))
+    binding.gemv_multi(items)
+    torch.cuda.synchronize()
+    for item, w in zip(items, want):
+        bits_equal(item[-1].cpu().numpy(), w)
+
+
 def test_gemv_multi_fused_equals_quantize_then_gemv():
     rows, n = 4096, 14336
     rng = synth.rng_for(111)
@@ -305,6 +335,8 @@ def test_decode_set_graph_sampled(decode_set, schedule):
     g.replay()
     g.replay()
     torch.cuda.synchronize()
+    for i in range(len(ds.shapes)):  # every row of every product written
+        assert not torch.isnan(ds.out[i]).any().item(), ds.shapes[i][0]
     rng = np.random.default_rng(len(schedule))
     picks = [0, 1, 2, 3, 4, 5, 6, 7 * 17 + 1, 7 * 31 + 4, 7 * 31 + 6, len(ds.shapes) - 1]
     for i in picks:
