@@ -309,9 +309,44 @@ static bool fill_ranges(const MArgs<PMAX>& a, int64_t V, int G, int64_t* cut, in
   return true;
 }
 
+// G contiguous ranges, none above V, each aiming at the average of what is
+// left (the boundary goes to the nearer tile edge), so that every CTA gets
+// work even when the greedy fill at V would need fewer ranges; false if tiles
+// remain after G ranges.
+template <int PMAX>
+static bool fill_even(const MArgs<PMAX>& a, int64_t V, int G, int64_t* cut) {
+  int j = 0;
+  int64_t left = a.count > 0 ? a.p[0].tiles : 0, pos = 0;
+  cut[0] = 0;
+  for (int seg = 0; seg < G; ++seg) {
+    const int64_t target = (a.total_cost - pos + (G - seg) - 1) / (G - seg);
+    int64_t cur = 0;
+    while (j < a.count) {
+      if (left == 0) {
+        if (++j < a.count) left = a.p[j].tiles;
+        continue;
+      }
+      if (cur >= target) break;
+      const int64_t c = a.p[j].nbp;
+      int64_t k = std::min(left, std::min((V - cur) / c, (target - cur) / c));  // >= 0
+      // one tile past the target when that lands nearer to it, within V
+      if (k < left && cur + (k + 1) * c <= V && (cur + k * c == 0 || cur + (k + 1) * c - target < target - cur - k * c))
+        ++k;
+      cur += k * c;
+      pos += k * c;
+      left -= k;
+      if (left > 0) break;  // the range ends inside product j
+    }
+    cut[seg + 1] = pos;
+  }
+  return pos == a.total_cost;
+}
+
 // The smallest largest-range cost V for G contiguous ranges: the equal share
 // rounded up always fits once a whole tile is added, so V is searched in
-// [share, share + largest tile cost].
+// [share, share + largest tile cost].  The ranges are then spread over all G
+// CTAs (fill_even), or, if that does not close, kept as the greedy fill made
+// them.
 template <int PMAX>
 static int balanced_ranges(MArgs<PMAX>& a, int G, int64_t max_tile) {
   int64_t lo = (a.total_cost + G - 1) / G, hi = lo + max_tile;
@@ -321,7 +356,11 @@ static int balanced_ranges(MArgs<PMAX>& a, int G, int64_t max_tile) {
     if (fill_ranges(a, m, G, nullptr, nseg)) hi = m;
     else lo = m + 1;
   }
-  fill_ranges(a, lo, G, a.cut, nseg);
+  if (fill_even(a, lo, G, a.cut)) {
+    nseg = G;
+  } else {
+    fill_ranges(a, lo, G, a.cut, nseg);
+  }
   a.ncut = nseg;
   return nseg;
 }
