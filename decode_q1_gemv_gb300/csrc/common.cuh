@@ -96,15 +96,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Streaming 16-byte read-only load that does not allocate in L1.
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // ---------------------------------------------------------- error record --
 // Sets the thread-local last-error text; returns `code`.
 int fail(int code, const char* fmt, ...);
@@ -118,6 +109,7 @@ int check_product(const char* who, int idx, const q1_product& pr);
 int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, const char* who);
 // Device status word of the product kernels (read and optionally cleared).
 int status_word_dp4a(unsigned* v, int clear);
+int status_word_prod(unsigned* v, int clear);
 
 }  // namespace q1
 

@@ -6,6 +6,10 @@
 // matrix-vector product of row r and vector v.  A thread owns R rows (one per
 // panel) and one lane pair, and keeps V vectors' chains; the activation
 // constants of the V vectors sit in shared memory, chunk by chunk along n.
+// The CTA's R panels arrive a quad of blocks at a time (R x 2.25 KB, two
+// contiguous bulk copies thanks to the packed layout) in a ring of
+// kProdStages shared-memory stages that one thread keeps filled, so the
+// weight loads' latency is hidden without holding the next quad in registers.
 #include <algorithm>
 
 #include "table.cuh"
@@ -13,6 +17,8 @@
 namespace q1 {
 
 constexpr int kThreads = 128;  // 4 warps; thread (row in panel, lane pair)
+constexpr int kProdStages = 3;                 // quads of weights in flight per CTA
+static __device__ unsigned g_status_prod = 0u;  // bit 0: a bounded wait gave up
 
 struct ProdArgs {
   const uint4* bits;     // packed sign words, 16-byte vectors
@@ -28,9 +34,20 @@ struct ProdArgs {
 
 // R panels per CTA (each thread: R rows, one per panel, one lane pair) and
 // V activation vectors per CTA.  1-D grid: bid = panel_group * vgroups + vgroup.
+template <int R>
+__host__ __device__ constexpr int prod_stage_bytes() { return R * (2048 + 256); }
+template <int R, int V>
+__host__ __device__ constexpr int prod_smem_bytes(int kc) {
+  return kProdStages * prod_stage_bytes<R>() + 128 + V * table_bytes(kc);
+}
+
 template <int R, int V>
 __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int SB = prod_stage_bytes<R>();
+  constexpr int S = kProdStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
+  unsigned char* tables = smem + S * SB + 128;
   const int tb = table_bytes(a.kc);
   const int lane = threadIdx.x & 31;
   const int w = lane & 3;                               // word w: lanes w and w+4
@@ -40,6 +57,27 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
   const int pg = blockIdx.x / a.vgroups;
   const int p0 = pg * R;
   const int v0 = vg * V;
+  const int nq = a.nbp / 4;  // quads of blocks along n (the panels are whole: R divides 8)
+  const uint8_t* bits = reinterpret_cast<const uint8_t*>(a.bits);
+  const uint8_t* scales = reinterpret_cast<const uint8_t*>(a.scales);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(smem_addr(&full[s]), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Thread 0 keeps S quads of the CTA's R panels in flight (weights only:
+  // they may be read before the preceding kernel has finished).
+  auto issue = [&](int qd) {
+    const int s = qd % S;
+    const uint32_t bar = smem_addr(&full[s]);
+    mbar_arrive_expect_tx(bar, uint32_t(SB));
+    const uint32_t dst = smem_addr(smem + s * SB);
+    bulk_g2s(dst, bits + quad_bits_offset(p0, qd, a.nbp), R * 2048, bar);
+    bulk_g2s(dst + R * 2048, scales + quad_scales_offset(p0, qd, a.nbp), R * 256, bar);
+  };
+  if (threadIdx.x == 0)
+    for (int qd = 0; qd < S && qd < nq; ++qd) issue(qd);
 
   pdl_wait();
 
@@ -49,40 +87,56 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
 #pragma unroll
     for (int j = 0; j < R; ++j) accE[v][j] = accO[v][j] = 0.0f;
 
-  for (int blk0 = 0; blk0 < a.nbp; blk0 += a.kc) {
+  bool ok = true;
+  int waited = 0;  // quads whose stage this thread has seen complete
+  for (int blk0 = 0; blk0 < a.nbp && ok; blk0 += a.kc) {
     const int kcb = min(a.kc, a.nbp - blk0);
     __syncthreads();
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      unsigned char* t = smem + v * tb;
+      unsigned char* t = tables + v * tb;
       const int vv = min(v0 + v, a.nvec - 1);
       build_table_q<4>(a.q + int64_t(vv) * a.n, a.d1 + int64_t(vv) * (a.n / kSub), a.nb, blk0, kcb, t,
-                    threadIdx.x, kThreads, a.kc);
+                       threadIdx.x, kThreads, a.kc);
     }
     __syncthreads();
 
     for (int b = blk0; b < blk0 + kcb; b += 4) {
+      const int qd = b / 4, s = qd % S;
+      const bool got = mbar_wait(smem_addr(&full[s]), uint32_t(qd / S) & 1u);
+      const unsigned char* st = smem + s * SB;
       uint4 wv[R];
       uint2 sc[R];
 #pragma unroll
       for (int j = 0; j < R; ++j) {
-        const int64_t p = p0 + j;
-        if (p < a.panels) {
-          wv[j] = ldg_stream(a.bits + bits_word_index(p, b, prow, w, a.nbp) / 4);
-          sc[j] = *reinterpret_cast<const uint2*>(a.scales + scale_index(p, b, prow, a.nbp));
-        } else {
-          wv[j] = make_uint4(0u, 0u, 0u, 0u);
-          sc[j] = make_uint2(0u, 0u);
-        }
+        wv[j] = got ? reinterpret_cast<const uint4*>(st + j * 2048)[prow * 4 + w] : make_uint4(0u, 0u, 0u, 0u);
+        sc[j] = got ? reinterpret_cast<const uint2*>(st + R * 2048 + j * 256)[prow] : make_uint2(0u, 0u);
       }
+      // Every thread holds its words: the stage may be refilled.  A wait that
+      // gave up anywhere ends the loop for the whole CTA at the same point.
+      if (__syncthreads_or(!got)) {
+        ok = false;
+        break;
+      }
+      waited = qd + 1;
+      if (threadIdx.x == 0 && qd + S < nq) issue(qd + S);
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const unsigned char* t = smem + v * tb;
+        const unsigned char* t = tables + v * tb;
         quad_all<R>(wv, sc, reinterpret_cast<const uint4*>(t) + (b - blk0) * 16,
                     reinterpret_cast<const float4*>(t + table_dk_offset(a.kc)) + (b - blk0) * 4, w, accE[v],
                     accO[v]);
       }
     }
+  }
+  if (!ok) {
+    // Give the copies still in flight (all issued by thread 0) a bounded
+    // chance to land before the CTA's shared memory goes away.
+    atomicOr(&g_status_prod, kStatusWaitTimeout);
+    if (threadIdx.x == 0)
+      for (int qd = waited; qd < nq && qd < waited + S; ++qd)
+        mbar_wait(smem_addr(&full[qd % S]), uint32_t(qd / S) & 1u, 100000000ull);
+    return;
   }
 
   pdl_launch_dependents();
@@ -92,10 +146,18 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const float r = row_sum(accE[v][j], accO[v][j]);
-      if (w == 0 && p0 + j < a.panels && row < a.rows && v0 + v < a.nvec)
-        a.out[int64_t(v0 + v) * a.rows + row] = r;
+      if (w == 0 && row < a.rows && v0 + v < a.nvec) a.out[int64_t(v0 + v) * a.rows + row] = r;
     }
   }
+}
+
+int status_word_prod(unsigned* v, int clear) {
+  if (int e = cuda_status(cudaMemcpyFromSymbol(v, g_status_prod, sizeof *v), "q1_device_status")) return e;
+  if (clear && *v) {
+    const unsigned zero = 0;
+    return cuda_status(cudaMemcpyToSymbol(g_status_prod, &zero, sizeof zero), "q1_device_status");
+  }
+  return Q1_OK;
 }
 
 template <int R, int V>
@@ -106,7 +168,16 @@ static int launch(const ProdArgs& a0, int64_t panels, cudaStream_t s, const char
   const int64_t pgroups = (panels + R - 1) / R;
   const int64_t grid = pgroups * a.vgroups;
   if (grid > 0x7fffffff) return fail(Q1_ERR_ARG, "%s: matrix too large for one launch", who);
-  const int smem = table_bytes(a.kc) * V;
+  const int smem = prod_smem_bytes<R, V>(a.kc);
+  static int attr_done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_done[dev]) {
+    if (int e = cuda_status(cudaFuncSetAttribute(k_q1_prod<R, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 prod_smem_bytes<R, V>(128)), "cudaFuncSetAttribute"))
+      return e;
+    attr_done[dev] = 1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(kThreads);
