@@ -8,11 +8,17 @@ Input formats:
   Q1_0 weight blocks  uint8 [rows, n/128, 18]: bytes 0-1 the block scale d0 as
                       little-endian IEEE binary16, bytes 2-17 the 128 sign bits
                       (element j in byte 2 + j//8, bit j%8; 1 = +d0, 0 = -d0).
+  Q2_0 weight blocks  uint8 [rows, n/128, 34]: bytes 0-1 the block scale d0 as
+                      above, bytes 2-33 the 128 2-bit codes (element j in byte
+                      2 + j//4, bits 2*(j%4)..2*(j%4)+1; code 0/1/2 = -1/0/+1
+                      times d0)
   activations         float32 [B, n]
   raw q8_0 quants     int8 [B, n] and binary16 scale bits uint16 [B, n/32]
 
 Distributions (the shapes of the workloads the pages and the benchmark name):
   sign bits           Bernoulli(0.5), i.e. uniform random bytes
+  ternary values      -1, 0, +1 with probabilities (1-p0)/2, p0, (1-p0)/2
+                      (p0 = 1/3 unless a test asks otherwise)
   d0 "halfnormal"     |N(0, 0.02)| rounded to binary16 (about 0.24 % of blocks
                       land in the binary16 subnormal range)
   d0 "lognormal"      exp(N(ln 0.02, 1)) rounded to binary16 (scales that vary
@@ -27,6 +33,7 @@ import numpy as np
 QK1 = 128          # weights per Q1_0 block
 QK8 = 32           # activation values per q8_0 scale
 BLOCK_BYTES = 18
+Q2_BLOCK_BYTES = 34
 
 # Llama-3-8B-shaped decode step: per layer q, k, v, o, gate, up, down; then lm_head.
 LLAMA3_8B_LAYER = (
@@ -132,3 +139,38 @@ def raw_quants(rng: np.random.Generator, nvec: int, n: int, scale: str = "lognor
         q[mask] = -128
     d = block_scales(rng, (nvec, n // QK8), scale)
     return q.astype(np.int8), d
+
+
+def ternary_codes(rng: np.random.Generator, shape, p_zero: float = 1.0 / 3.0) -> np.ndarray:
+    """uint8 codes 0/1/2 (values -1/0/+1): zero with probability p_zero, the
+    two signs equally likely otherwise."""
+    u = rng.random(shape)
+    half = (1.0 - p_zero) / 2.0
+    return np.where(u < half, 0, np.where(u < half + p_zero, 1, 2)).astype(np.uint8)
+
+
+def assemble_ternary_blocks(scale_bits: np.ndarray, codes: np.ndarray) -> np.ndarray:
+    """Lay out [rows, nb] scale bits and [rows, nb, 128] codes as 34-byte blocks."""
+    rows, nb = scale_bits.shape
+    codes = np.asarray(codes, dtype=np.uint8)
+    if codes.shape != (rows, nb, 128) or codes.max(initial=0) > 3:
+        raise ValueError("codes must be [rows, nb, 128] values 0..3")
+    c = codes.reshape(rows, nb, 32, 4)
+    packed = c[..., 0] | (c[..., 1] << 2) | (c[..., 2] << 4) | (c[..., 3] << 6)
+    blocks = np.empty((rows, nb, Q2_BLOCK_BYTES), dtype=np.uint8)
+    s = np.ascontiguousarray(scale_bits, dtype=np.uint16)
+    blocks[:, :, 0] = (s & 0xFF).astype(np.uint8)
+    blocks[:, :, 1] = (s >> 8).astype(np.uint8)
+    blocks[:, :, 2:] = packed
+    return blocks
+
+
+def ternary_blocks(rng: np.random.Generator, rows: int, n: int, scale: str = "halfnormal",
+                   p_zero: float = 1.0 / 3.0) -> np.ndarray:
+    """Random Q2_0 weight blocks uint8 [rows, n/128, 34]."""
+    if n % QK1:
+        raise ValueError("n must be a multiple of 128")
+    nb = n // QK1
+    codes = ternary_codes(rng, (rows, nb, QK1), p_zero)
+    scales = block_scales(rng, (rows, nb), scale)
+    return assemble_ternary_blocks(scales, codes)

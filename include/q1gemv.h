@@ -53,8 +53,8 @@ extern "C" {
 const char *q1_last_error(void);
 
 /* Bytes of the packed weight buffer q1_0_pack writes for a rows x n matrix
- * (18 bytes per 128 weights, rows padded to a multiple of 32 and blocks per
- * row to a multiple of 8).  Returns a negative Q1_ERR_ARG for a bad shape.
+ * (18 bytes per 128 weights, rows padded to a multiple of 256 and blocks per
+ * row to a multiple of 4).  Returns a negative Q1_ERR_ARG for a bad shape.
  * Host-only; touches no device. */
 int64_t q1_0_packed_bytes(int64_t rows, int64_t n);
 

@@ -8,6 +8,8 @@ and the passages of bankML's "docs/modules/gpu.md" it follows.
 
 Every function takes and returns numpy arrays:
   blocks  uint8  [rows, n/128, 18]   Q1_0 blocks (fp16 scale LE + 16 sign bytes)
+  tblocks uint8  [rows, n/128, 34]   Q2_0 blocks (fp16 scale LE + 32 bytes of 2-bit
+                                     codes 0/1/2 = -1/0/+1), the q2_* functions
   q       int8   [n] or [B, n]       q8_0 quants
   d       uint16 [n/32] or [B, n/32] fp16 scale bits
 """
@@ -83,6 +85,16 @@ def _load():
         lib.q1o_rows_sampled.restype = None
         lib.q1o_gemv_threaded.argtypes = [P, I64, I64, P, P, P, ctypes.c_int]
         lib.q1o_gemv_threaded.restype = ctypes.c_longlong
+        lib.q2o_weight.argtypes = [P, I64, I64, I64]
+        lib.q2o_weight.restype = ctypes.c_float
+        lib.q2o_dot_row.argtypes = [P, I64, P, P]
+        lib.q2o_dot_row.restype = ctypes.c_float
+        lib.q2o_lane_sums.argtypes = [P, I64, P, P]
+        lib.q2o_lane_sums.restype = None
+        lib.q2o_gemv.argtypes = [P, I64, I64, P, P, P]
+        lib.q2o_gemv.restype = None
+        lib.q2o_rows_sampled.argtypes = [P, I64, I64, P, P, P, P]
+        lib.q2o_rows_sampled.restype = None
         _lib = lib
         return lib
 
@@ -250,3 +262,63 @@ def gemv_threaded(blocks: np.ndarray, q: np.ndarray, d: np.ndarray, threads: int
         raise ValueError("out must be contiguous float32 with at least `rows` elements")
     done = _load().q1o_gemv_threaded(_ptr(blocks), rows, n, _ptr(q), _ptr(d), _ptr(out), int(threads))
     return out, int(done)
+
+
+# ------------------------------------------------------- Q2_0 (ternary) --
+def _check_tblocks(tblocks: np.ndarray):
+    if tblocks.ndim != 3 or tblocks.shape[2] != 34:
+        raise ValueError("tblocks must be uint8 [rows, n/128, 34]")
+    return tblocks.shape[0], tblocks.shape[1] * 128
+
+
+def q2_weight(tblocks: np.ndarray, r: int, j: int) -> float:
+    rows, n = _check_tblocks(tblocks)
+    tblocks = _c(tblocks, np.uint8)
+    return float(_load().q2o_weight(_ptr(tblocks), n, int(r), int(j)))
+
+
+def q2_dot_row(tblocks_row: np.ndarray, q: np.ndarray, d: np.ndarray) -> np.float32:
+    """One Q2_0 row: tblocks_row uint8 [nb, 34]."""
+    tblocks_row = _c(tblocks_row, np.uint8)
+    q = _c(q, np.int8)
+    d = _c(d, np.uint16)
+    nb = tblocks_row.shape[0]
+    if q.size != nb * 128 or d.size != nb * 4:
+        raise ValueError("shape mismatch")
+    return np.float32(_load().q2o_dot_row(_ptr(tblocks_row), nb, _ptr(q), _ptr(d)))
+
+
+def q2_lane_sums(tblocks_row: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """Exact integer lane sums of one Q2_0 row, int32 [nb, 4, 8]."""
+    tblocks_row = _c(tblocks_row, np.uint8)
+    q = _c(q, np.int8)
+    nb = tblocks_row.shape[0]
+    out = np.empty((nb, 4, 8), dtype=np.int32)
+    _load().q2o_lane_sums(_ptr(tblocks_row), nb, _ptr(q), _ptr(out))
+    return out
+
+
+def q2_gemv(tblocks: np.ndarray, q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    rows, n = _check_tblocks(tblocks)
+    tblocks = _c(tblocks, np.uint8)
+    q = _c(q, np.int8).ravel()
+    d = _c(d, np.uint16).ravel()
+    if q.size != n or d.size != n // 32:
+        raise ValueError("activation shape mismatch")
+    out = np.empty(rows, dtype=np.float32)
+    _load().q2o_gemv(_ptr(tblocks), rows, n, _ptr(q), _ptr(d), _ptr(out))
+    return out
+
+
+def q2_rows_sampled(tblocks: np.ndarray, idx, q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """out[i] = dot(row idx[i], (q, d)) for a Q2_0 matrix."""
+    rows, n = _check_tblocks(tblocks)
+    tblocks = np.ascontiguousarray(tblocks)
+    idx = _c(idx, np.int64)
+    if idx.size and (idx.min() < 0 or idx.max() >= rows):
+        raise ValueError("row index out of range")
+    q = _c(q, np.int8).ravel()
+    d = _c(d, np.uint16).ravel()
+    out = np.empty(idx.size, dtype=np.float32)
+    _load().q2o_rows_sampled(_ptr(tblocks), n, idx.size, _ptr(idx), _ptr(q), _ptr(d), _ptr(out))
+    return out

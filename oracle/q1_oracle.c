@@ -31,6 +31,8 @@
  *   OPEN-6  horizontal sum read as ((a0+a4)+(a2+a6)) + ((a1+a5)+(a3+a7)).
  *   OPEN-7  no flush-to-zero anywhere.
  *
+ * The Q2_0 (ternary) section below carries its own readings, OPEN-10/11.
+ *
  * Build: plain C11, -O2 -ffp-contract=off -fno-fast-math (no contraction of
  * a*b+c into an fma; every fma below is an explicit call to fmaf).
  */
@@ -342,6 +344,106 @@ void q1o_rows_sampled(const uint8_t *blocks, int64_t n, int64_t count,
         out[i] = q1o_dot_row(blocks + idx[i] * nb * Q1O_BLOCK_BYTES, nb,
                              q + v * n, d + v * (n / Q1O_QBLOCK));
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q2_0 (ternary) weights                                                    */
+/* ------------------------------------------------------------------------ */
+/* The pages name a ternary sibling format, Q2_0, as the next GPU kernel
+ * ("Advantages and efficiency", where optimization goes next; "Limitations":
+ * no Q2_0 GPU kernel yet) and give its size only as 2.13 GB per 8B token
+ * (par.md, benchmarks).  What it is here:
+ *   OPEN-10 block = 2-byte little-endian fp16 scale d0, then 32 bytes of
+ *           2-bit codes; element j's code is (qs[j>>2] >> 2*(j&3)) & 3 and its
+ *           value t = code - 1, so 0, 1, 2 mean -1, 0, +1 (code 3 is not a
+ *           weight); weight = t*d0.  34 bytes per 128 weights.
+ *   OPEN-11 the row product is the Q1_0 chain with the lane sum taken over
+ *           ternary values: +1 contributes q, -1 the wrapped negation of q,
+ *           0 nothing.  Blocks, sub-blocks, lanes, the fma chain, the
+ *           starting +0 and the horizontal sum are those of Q1_0 above. */
+#define Q2O_BLOCK_BYTES 34
+
+static int q2o_code(const uint8_t *blk, int j)
+{
+    return (blk[2 + (j >> 2)] >> (2 * (j & 3))) & 3;
+}
+
+/* Dequantized weight (row r, column j) of a rows x n Q2_0 matrix; NaN for
+ * code 3. */
+float q2o_weight(const uint8_t *blocks, int64_t n, int64_t r, int64_t j)
+{
+    const uint8_t *blk = blocks + (r * (n / Q1O_BLOCK) + j / Q1O_BLOCK) * Q2O_BLOCK_BYTES;
+    int c = q2o_code(blk, (int)(j % Q1O_BLOCK));
+    if (c == 3)
+        return NAN;
+    float d0 = q1o_f16_to_f32(q1o_block_scale_bits(blk));
+    return (float)(c - 1) * d0;
+}
+
+/* Exact integer lane sum of sub-block k, lane l (OPEN-5, OPEN-11). */
+static int32_t q2o_lane_sum(const uint8_t *blk, const int8_t *qb, int k, int l)
+{
+    int32_t s = 0;
+    for (int i = 0; i < 4; ++i) {
+        int j = Q1O_QBLOCK * k + 4 * l + i;
+        int c = q2o_code(blk, j);
+        if (c == 2)
+            s += qb[j];
+        else if (c == 0)
+            s += q1o_neg_i8(qb[j]);
+    }
+    return s;
+}
+
+/* One output row of a Q2_0 matrix: nb 34-byte blocks against (q, d). */
+float q2o_dot_row(const uint8_t *row_blocks, int64_t nb, const int8_t *q, const uint16_t *d)
+{
+    float acc[Q1O_LANES];
+    for (int l = 0; l < Q1O_LANES; ++l)
+        acc[l] = 0.0f;                                   /* OPEN-4 */
+    for (int64_t b = 0; b < nb; ++b) {                   /* blocks in order */
+        const uint8_t *blk = row_blocks + b * Q2O_BLOCK_BYTES;
+        const int8_t *qb = q + b * Q1O_BLOCK;
+        float d0 = q1o_f16_to_f32(q1o_block_scale_bits(blk));
+        for (int l = 0; l < Q1O_LANES; ++l) {
+            float ab = 0.0f;
+            for (int k = 0; k < 4; ++k) {
+                float d1 = q1o_f16_to_f32(d[b * 4 + k]);
+                float t = (float)q2o_lane_sum(blk, qb, k, l);  /* exact: |s| <= 512 */
+                ab = (k == 0) ? d1 * t : fmaf(d1, t, ab);
+            }
+            acc[l] = fmaf(d0, ab, acc[l]);
+        }
+    }
+    return ((acc[0] + acc[4]) + (acc[2] + acc[6])) + ((acc[1] + acc[5]) + (acc[3] + acc[7]));
+}
+
+/* Exact integer lane sums s[b][k][l] of one Q2_0 row. */
+void q2o_lane_sums(const uint8_t *row_blocks, int64_t nb, const int8_t *q, int32_t *s_out)
+{
+    for (int64_t b = 0; b < nb; ++b)
+        for (int k = 0; k < 4; ++k)
+            for (int l = 0; l < Q1O_LANES; ++l)
+                s_out[(b * 4 + k) * Q1O_LANES + l] =
+                    q2o_lane_sum(row_blocks + b * Q2O_BLOCK_BYTES, q + b * Q1O_BLOCK, k, l);
+}
+
+/* out[r] = dot(row r, (q, d)) for every row of a rows x n Q2_0 matrix. */
+void q2o_gemv(const uint8_t *blocks, int64_t rows, int64_t n, const int8_t *q,
+              const uint16_t *d, float *out)
+{
+    int64_t nb = n / Q1O_BLOCK;
+    for (int64_t r = 0; r < rows; ++r)
+        out[r] = q2o_dot_row(blocks + r * nb * Q2O_BLOCK_BYTES, nb, q, d);
+}
+
+/* Rows listed in `idx` only: out[i] = dot(row idx[i], (q, d)). */
+void q2o_rows_sampled(const uint8_t *blocks, int64_t n, int64_t count, const int64_t *idx,
+                      const int8_t *q, const uint16_t *d, float *out)
+{
+    int64_t nb = n / Q1O_BLOCK;
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = q2o_dot_row(blocks + idx[i] * nb * Q2O_BLOCK_BYTES, nb, q, d);
 }
 
 /* ------------------------------------------------------------------------ */
