@@ -32,7 +32,7 @@ Q1_MISMATCH = 2
 # Every symbol include/q1gemv.h declares (checked by the tests).
 EXPORTS = ("q1_last_error", "q1_0_packed_bytes", "q1_0_pack", "q1_0_unpack", "q8_quantize_act",
            "q1_0_gemv", "q1_0_gemv_multi", "q1_0_gemv_multi_plan", "q1_0_gemm_small", "q1_0_verify",
-           "q1_device_status")
+           "q1_device_status", "q2_0_packed_bytes", "q2_0_pack", "q2_0_unpack", "q2_0_gemv", "q2_0_gemv_multi")
 
 MAX_PRODUCTS = 256
 
@@ -92,6 +92,16 @@ def load():
         lib.q1_0_gemv_multi_plan.argtypes = [ctypes.POINTER(Product), I, I, ctypes.POINTER(MultiPlan),
                                              ctypes.POINTER(I64), I]
         lib.q1_0_gemv_multi_plan.restype = I
+        lib.q2_0_packed_bytes.argtypes = [I64, I64]
+        lib.q2_0_packed_bytes.restype = I64
+        lib.q2_0_pack.argtypes = [P, I64, I64, P, P]
+        lib.q2_0_pack.restype = I
+        lib.q2_0_unpack.argtypes = [P, I64, I64, P, P]
+        lib.q2_0_unpack.restype = I
+        lib.q2_0_gemv.argtypes = [P, I64, I64, P, P, P, P]
+        lib.q2_0_gemv.restype = I
+        lib.q2_0_gemv_multi.argtypes = [ctypes.POINTER(Product), I, P]
+        lib.q2_0_gemv_multi.restype = I
         lib.q1_0_gemm_small.argtypes = [P, I64, I64, I64, P, P, P, P]
         lib.q1_0_gemm_small.restype = I
         lib.q1_device_status.argtypes = [I]
@@ -233,6 +243,62 @@ def multi_plan(shapes, sms: int = 0) -> dict:
            "q1_0_gemv_multi_plan")
     return {"rows_per_thread": plan.rows_per_thread, "grid": plan.grid, "total_cost": plan.total_cost,
             "max_range_cost": plan.max_range_cost, "cuts": list(cuts[:plan.grid + 1])}
+
+
+# ------------------------------------------------------- Q2_0 (ternary) --
+def q2_packed_bytes(rows: int, n: int) -> int:
+    v = load().q2_0_packed_bytes(int(rows), int(n))
+    if v < 0:
+        raise Q1Error(int(v), last_error())
+    return int(v)
+
+
+def q2_pack(blocks: torch.Tensor, rows: int, n: int, packed: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """Pack Q2_0 blocks (uint8, rows*(n/128) 34-byte blocks) into the device layout."""
+    nbytes = q2_packed_bytes(rows, n)
+    if blocks.numel() != rows * (n // 128) * 34:
+        raise ValueError("blocks must hold rows*(n/128) 34-byte blocks")
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=blocks.device)
+    if packed.numel() * packed.element_size() < nbytes:
+        raise ValueError("packed buffer too small")
+    _check(load().q2_0_pack(_dev(blocks, "blocks", (torch.uint8,)), rows, n,
+                            _dev(packed, "packed", (torch.uint8,)), _stream_ptr(stream)), "q2_0_pack")
+    return packed
+
+
+def q2_unpack(packed: torch.Tensor, rows: int, n: int, blocks: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    q2_packed_bytes(rows, n)
+    if blocks is None:
+        blocks = torch.empty((rows, n // 128, 34), dtype=torch.uint8, device=packed.device)
+    if blocks.numel() != rows * (n // 128) * 34:
+        raise ValueError("blocks must hold rows*(n/128) 34-byte blocks")
+    _check(load().q2_0_unpack(_dev(packed, "packed", (torch.uint8,)), rows, n,
+                              _dev(blocks, "blocks", (torch.uint8,)), _stream_ptr(stream)), "q2_0_unpack")
+    return blocks
+
+
+def q2_gemv(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tensor,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if q.numel() != n or d.numel() != n // 32:
+        raise ValueError("q must hold n quants and d n/32 scales")
+    if out is None:
+        out = torch.empty(rows, dtype=torch.float32, device=q.device)
+    if out.numel() != rows:
+        raise ValueError("out must hold rows values")
+    _check(load().q2_0_gemv(_dev(packed, "packed", (torch.uint8,)), rows, n, _dev(q, "q", (torch.int8,)),
+                            _dev(d, "d", _SCALE_DTYPES), _dev(out, "out", (torch.float32,)),
+                            _stream_ptr(stream)), "q2_0_gemv")
+    return out
+
+
+def q2_gemv_multi(items=None, stream=None, array=None):
+    """One launch for several independent Q2_0 products (items as product_array
+    takes them, with packed buffers from q2_pack)."""
+    arr = array if array is not None else product_array(items)
+    _check(load().q2_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q2_0_gemv_multi")
 
 
 def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tensor,

@@ -3,7 +3,7 @@
 #include <cstdio>
 #include <string>
 
-#include "common.cuh"
+#include "q2.cuh"
 
 namespace q1 {
 
@@ -35,6 +35,15 @@ extern "C" int64_t q1_0_packed_bytes(int64_t rows, int64_t n) {
                     (long long)rows, (long long)n);
   q1::g_last_error.clear();
   return q1::layout_of(rows, n).total_bytes;
+}
+
+extern "C" int64_t q2_0_packed_bytes(int64_t rows, int64_t n) {
+  if (rows < 1 || rows > (int64_t(1) << 26) || n < 128 || n > (int64_t(1) << 24) || n % 128)
+    return q1::fail(Q1_ERR_ARG, "q2_0_packed_bytes: bad shape rows=%lld n=%lld (rows in 1..2^26, "
+                                "n a multiple of 128 in 128..2^24)",
+                    (long long)rows, (long long)n);
+  q1::g_last_error.clear();
+  return q1::layout_q2(rows, n).total_bytes;
 }
 
 extern "C" int q1_device_status(int clear) {

@@ -27,7 +27,11 @@
 // status word instead of hanging.
 #include <algorithm>
 
-#include "table.cuh"
+#include "q2.cuh"
+
+#ifndef Q2_BIG_ROWS
+#define Q2_BIG_ROWS 4
+#endif
 
 namespace q1 {
 
@@ -44,8 +48,30 @@ template <int R>
 __host__ __device__ constexpr int consumers() { return 32 * consumer_warps<R>(); }
 template <int R>
 __host__ __device__ constexpr int multi_threads() { return consumers<R>() + 32; }
-constexpr int kQuadBits = 2048;    // one panel x one quad of blocks: 32 rows x 4 blocks x 16 B
 constexpr int kQuadScales = 256;   // 32 rows x 4 blocks x 2 B
+
+// The two weight formats the kernel streams.  Q1_0: one sign word per lane
+// word (2 KB per panel and quad).  Q2_0: a P and an N word (4 KB), see q2.cuh.
+struct FmtQ1 {
+  static constexpr int kQuadBits = 2048;  // one panel x one quad of blocks: 32 rows x 4 blocks x 16 B
+  static constexpr bool kTwoPlanes = false;
+  static constexpr int kBigRows = 8;      // rows per thread of the launches that fill every CTA
+  using Consts = ConstsQ1;
+  static __host__ __device__ __forceinline__ int64_t quad_bits_offset(int64_t p, int64_t qd, int64_t nbp) {
+    return q1::quad_bits_offset(p, qd, nbp);
+  }
+  static Layout layout(int64_t rows, int64_t n) { return layout_of(rows, n); }
+};
+struct FmtQ2 {
+  static constexpr int kQuadBits = kQ2QuadBits;
+  static constexpr bool kTwoPlanes = true;
+  static constexpr int kBigRows = Q2_BIG_ROWS;
+  using Consts = ConstsQ2;
+  static __host__ __device__ __forceinline__ int64_t quad_bits_offset(int64_t p, int64_t qd, int64_t nbp) {
+    return q2_quad_bits_offset(p, qd, nbp);
+  }
+  static Layout layout(int64_t rows, int64_t n) { return layout_q2(rows, n); }
+};
 constexpr int kConsumerBarrier = 1;
 constexpr int kMaxKc = 128;        // blocks of activation held in the table (n <= 16384 in one chunk)
 
@@ -73,15 +99,17 @@ struct MArgs {
 };
 
 // Ring of stages: a stage is one quad of blocks for the tile's slots*R panels;
-// about 74 KB of weights in flight per CTA whatever R is.
-template <int R>
-__host__ __device__ constexpr int ring_stages() { return 32 / (slots_of<R>() * R); }
-template <int R>
-__host__ __device__ constexpr int stage_bytes() { return slots_of<R>() * R * (kQuadBits + kQuadScales); }
+// about 72 KB of weights in flight per CTA (at least two stages).
+template <int R, class F>
+__host__ __device__ constexpr int stage_bytes() { return slots_of<R>() * R * (F::kQuadBits + kQuadScales); }
+template <int R, class F>
+__host__ __device__ constexpr int ring_stages() {
+  return 73728 / stage_bytes<R, F>() > 2 ? 73728 / stage_bytes<R, F>() : 2;
+}
 
-template <int R>
+template <int R, class F>
 __host__ __device__ constexpr int multi_smem_bytes(int kc) {
-  return ring_stages<R>() * stage_bytes<R>() + table_bytes(kc) + 2 * ring_stages<R>() * 8;
+  return ring_stages<R, F>() * stage_bytes<R, F>() + table_bytes(kc) + 2 * ring_stages<R, F>() * 8;
 }
 
 // Tiles [t_lo, t_hi) of product p that fall in this CTA's cost range.
@@ -110,15 +138,15 @@ __device__ __forceinline__ int first_product(const MArgs<PMAX>& a, int64_t v) {
   return l;
 }
 
-template <int R, int PMAX>
+template <int R, int PMAX, class F>
 __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid_constant__ MArgs<PMAX> a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int S = ring_stages<R>();
-  constexpr int SB = stage_bytes<R>();
+  constexpr int S = ring_stages<R, F>();
+  constexpr int SB = stage_bytes<R, F>();
   constexpr int kSlots = slots_of<R>();
   constexpr int kConsumerWarps = consumer_warps<R>();
   constexpr int kConsumers = consumers<R>();
-  constexpr int TB = kSlots * R * kQuadBits;  // bits part of a stage
+  constexpr int TB = kSlots * R * F::kQuadBits;  // bits part of a stage
   constexpr int kTableBatch = R >= 8 ? 8 : 4;  // load rounds in flight while a table is built
   unsigned char* table = smem + S * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(table + table_bytes(a.kc));
@@ -164,7 +192,7 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
             const uint32_t full = smem_addr(&bars[s]);
             mbar_arrive_expect_tx(full, uint32_t(SB));
             const uint32_t dst = smem_addr(smem + s * SB);
-            bulk_g2s(dst, bits + quad_bits_offset(p0, qd, nbp), TB, full);
+            bulk_g2s(dst, bits + F::quad_bits_offset(p0, qd, nbp), TB, full);
             bulk_g2s(dst + TB, scales + quad_scales_offset(p0, qd, nbp), kSlots * R * kQuadScales, full);
           }
         }
@@ -213,8 +241,8 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
     const bool one_chunk = pnbp <= kc;
     if (one_chunk) {
       named_barrier(kConsumerBarrier, kConsumers);  // previous product's table no longer read
-      if (px) build_table_x<kTableBatch>(px, pnb, 0, pnbp, table, tid, kConsumers, kc);
-      else build_table_q<kTableBatch>(pq, pd, pnb, 0, pnbp, table, tid, kConsumers, kc);
+      if (px) build_table_x<kTableBatch, typename F::Consts>(px, pnb, 0, pnbp, table, tid, kConsumers, kc);
+      else build_table_q<kTableBatch, typename F::Consts>(pq, pd, pnb, 0, pnbp, table, tid, kConsumers, kc);
       named_barrier(kConsumerBarrier, kConsumers);
     }
     for (int t = t_lo; t < t_hi && ok; ++t) {
@@ -228,8 +256,8 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
         if (!one_chunk && b0 % kc == 0) {
           named_barrier(kConsumerBarrier, kConsumers);
           const int kcb = min(kc, pnbp - b0);
-          if (px) build_table_x<kTableBatch>(px, pnb, b0, kcb, table, tid, kConsumers, kc);
-          else build_table_q<kTableBatch>(pq, pd, pnb, b0, kcb, table, tid, kConsumers, kc);
+          if (px) build_table_x<kTableBatch, typename F::Consts>(px, pnb, b0, kcb, table, tid, kConsumers, kc);
+          else build_table_q<kTableBatch, typename F::Consts>(pq, pd, pnb, b0, kcb, table, tid, kConsumers, kc);
           named_barrier(kConsumerBarrier, kConsumers);
         }
         const int gb = one_chunk ? b0 : b0 % kc;  // block index within the table
@@ -239,18 +267,20 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
           break;
         }
         const unsigned char* st = smem + s * SB;
-        uint4 wv[R];
+        uint4 wv[R], nv[F::kTwoPlanes ? R : 1];
         uint2 sc[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const int tp = kSlots * r + ps;
-          wv[r] = reinterpret_cast<const uint4*>(st + tp * kQuadBits)[prow * 4 + w];
+          wv[r] = reinterpret_cast<const uint4*>(st + tp * F::kQuadBits)[prow * 4 + w];
+          if constexpr (F::kTwoPlanes) nv[r] = reinterpret_cast<const uint4*>(st + tp * F::kQuadBits + 2048)[prow * 4 + w];
           sc[r] = reinterpret_cast<const uint2*>(st + TB + tp * kQuadScales)[prow];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&bars[S + s]));  // stage consumed
 
-        quad_all<R>(wv, sc, QC + gb * 16, DK + gb * 4, w, accE, accO);
+        if constexpr (F::kTwoPlanes) q2_quad_all<R>(wv, nv, sc, QC + gb * 16, DK + gb * 4, w, accE, accO);
+        else quad_all<R>(wv, sc, QC + gb * 16, DK + gb * 4, w, accE, accO);
       }
       if (!ok) break;
 #pragma unroll
@@ -265,14 +295,14 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
 }
 
 // ---------------------------------------------------------------- host ----
-template <int R, int PMAX>
+template <int R, int PMAX, class F>
 static int set_smem_attr() {
   static int done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (!done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_q1_multi<R, PMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         multi_smem_bytes<R>(kMaxKc));
+    cudaError_t e = cudaFuncSetAttribute(k_q1_multi<R, PMAX, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         multi_smem_bytes<R, F>(kMaxKc));
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute");
     done[dev] = 1;
   }
@@ -367,13 +397,13 @@ static int balanced_ranges(MArgs<PMAX>& a, int G, int64_t max_tile) {
 
 // The launch plan of k_q1_multi<R, PMAX> for `count` products on `sms` SMs:
 // the kernel arguments and the grid.
-template <int R, int PMAX>
+template <int R, int PMAX, class F>
 static void plan_multi(const q1_product* prods, int count, int sms, MArgs<PMAX>& a, int& grid) {
   int64_t cost = 0;
   int64_t total_tiles = 0;
   int max_nbp = 8;
   for (int j = 0; j < count; ++j) {
-    const Layout L = layout_of(prods[j].rows, prods[j].n);
+    const Layout L = F::layout(prods[j].rows, prods[j].n);
     MProd& p = a.p[j];
     p.packed = static_cast<const uint8_t*>(prods[j].packed);
     p.x = prods[j].x;
@@ -405,23 +435,23 @@ static void plan_multi(const q1_product* prods, int count, int sms, MArgs<PMAX>&
   }
 }
 
-template <int R, int PMAX>
+template <int R, int PMAX, class F>
 static int launch_multi(const q1_product* prods, int count, cudaStream_t s, const char* who) {
-  if (int e = set_smem_attr<R, PMAX>()) return e;
+  if (int e = set_smem_attr<R, PMAX, F>()) return e;
   MArgs<PMAX> a;
   int grid = 0;
-  plan_multi<R, PMAX>(prods, count, num_sms(), a, grid);
+  plan_multi<R, PMAX, F>(prods, count, num_sms(), a, grid);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(multi_threads<R>());
-  cfg.dynamicSmemBytes = size_t(multi_smem_bytes<R>(a.kc));
+  cfg.dynamicSmemBytes = size_t(multi_smem_bytes<R, F>(a.kc));
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_multi<R, PMAX>, a), who);
+  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_multi<R, PMAX, F>, a), who);
 }
 
 // The plan reported by q1_0_gemv_multi_plan: the CTA ranges exactly as the
@@ -431,7 +461,7 @@ static int report_plan(const q1_product* prods, int count, int sms, q1_multi_pla
                        int max_cuts) {
   MArgs<PMAX>* a = new MArgs<PMAX>;
   int grid = 0;
-  plan_multi<R, PMAX>(prods, count, sms, *a, grid);
+  plan_multi<R, PMAX, FmtQ1>(prods, count, sms, *a, grid);
   out->rows_per_thread = R;
   out->grid = grid;
   out->total_cost = a->total_cost;
@@ -456,27 +486,29 @@ static int report_plan(const q1_product* prods, int count, int sms, q1_multi_pla
   return Q1_OK;
 }
 
-// Rows per thread: the largest R whose tiles still give every CTA some work.
+// Rows per thread: the largest R whose tiles still give every CTA some work
+// (the 8-panel tiles take the format's big-launch rows per thread).
+template <class F>
 static int rows_per_thread(const q1_product* prods, int count, int sms) {
   int64_t panels = 0;
   for (int j = 0; j < count; ++j) panels += (prods[j].rows + kPanel - 1) / kPanel;
   const int64_t ctas = 2 * int64_t(sms);
-  return panels >= 8 * ctas ? 8 : panels >= 4 * ctas ? 2 : 1;
+  return panels >= 8 * ctas ? F::kBigRows : panels >= 4 * ctas ? 2 : 1;
 }
 
-template <int PMAX>
+template <int PMAX, class F>
 static int dispatch(const q1_product* prods, int count, cudaStream_t s, const char* who) {
-  switch (rows_per_thread(prods, count, num_sms())) {
-    case 8: return launch_multi<8, PMAX>(prods, count, s, who);
-    case 2: return launch_multi<2, PMAX>(prods, count, s, who);
-    default: return launch_multi<1, PMAX>(prods, count, s, who);
+  switch (rows_per_thread<F>(prods, count, num_sms())) {
+    case F::kBigRows: return launch_multi<F::kBigRows, PMAX, F>(prods, count, s, who);
+    case 2: return launch_multi<2, PMAX, F>(prods, count, s, who);
+    default: return launch_multi<1, PMAX, F>(prods, count, s, who);
   }
 }
 
 template <int PMAX>
 static int dispatch_plan(const q1_product* prods, int count, int sms, q1_multi_plan* out, int64_t* cuts,
                          int max_cuts) {
-  switch (rows_per_thread(prods, count, sms)) {
+  switch (rows_per_thread<FmtQ1>(prods, count, sms)) {
     case 8: return report_plan<8, PMAX>(prods, count, sms, out, cuts, max_cuts);
     case 2: return report_plan<2, PMAX>(prods, count, sms, out, cuts, max_cuts);
     default: return report_plan<1, PMAX>(prods, count, sms, out, cuts, max_cuts);
@@ -506,10 +538,15 @@ int check_product(const char* who, int idx, const q1_product& pr) {
   return Q1_OK;
 }
 
+template <class F>
+static int launch_products(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+  if (count == 1) return dispatch<1, F>(prods, count, s, who);
+  if (count <= 8) return dispatch<8, F>(prods, count, s, who);
+  return dispatch<Q1_MAX_PRODUCTS, F>(prods, count, s, who);
+}
+
 int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, const char* who) {
-  if (count == 1) return dispatch<1>(prods, count, s, who);
-  if (count <= 8) return dispatch<8>(prods, count, s, who);
-  return dispatch<Q1_MAX_PRODUCTS>(prods, count, s, who);
+  return launch_products<FmtQ1>(prods, count, s, who);
 }
 
 int status_word_dp4a(unsigned* v, int clear) {
@@ -558,4 +595,20 @@ extern "C" int q1_0_gemv_multi(const q1_product* products, int count, void* stre
   for (int j = 0; j < count; ++j)
     if (int e = check_product("q1_0_gemv_multi", j, products[j])) return e;
   return launch_products_dp4a(products, count, static_cast<cudaStream_t>(stream), "q1_0_gemv_multi launch");
+}
+
+extern "C" int q2_0_gemv(const void* packed, int64_t rows, int64_t n, const int8_t* q, const uint16_t* d,
+                         float* out, void* stream) {
+  q1_product p = {packed, rows, n, nullptr, q, d, out};
+  if (!q || !d) return fail(Q1_ERR_ARG, "q2_0_gemv: null pointer");
+  if (int e = check_product("q2_0_gemv", 0, p)) return e;
+  return launch_products<FmtQ2>(&p, 1, static_cast<cudaStream_t>(stream), "q2_0_gemv launch");
+}
+
+extern "C" int q2_0_gemv_multi(const q1_product* products, int count, void* stream) {
+  if (!products || count < 1 || count > Q1_MAX_PRODUCTS)
+    return fail(Q1_ERR_ARG, "q2_0_gemv_multi: count=%d outside 1..%d (or null list)", count, Q1_MAX_PRODUCTS);
+  for (int j = 0; j < count; ++j)
+    if (int e = check_product("q2_0_gemv_multi", j, products[j])) return e;
+  return launch_products<FmtQ2>(products, count, static_cast<cudaStream_t>(stream), "q2_0_gemv_multi launch");
 }

@@ -1,6 +1,8 @@
 // pack.cu -- q1_0_pack / q1_0_unpack: 18-byte Q1_0 blocks <-> the packed
-// device layout documented in common.cuh.  Runs once per weight matrix.
-#include "common.cuh"
+// device layout documented in common.cuh; q2_0_pack / q2_0_unpack: 34-byte
+// Q2_0 blocks <-> the two-plane layout documented in q2.cuh.  Runs once per
+// weight matrix.
+#include "q2.cuh"
 
 namespace q1 {
 
@@ -72,6 +74,81 @@ __global__ void k_unpack(const uint32_t* __restrict__ bits, const uint16_t* __re
   for (int j = 0; j < 16; ++j) blk[2 + j] = qs[j];
 }
 
+// Q2_0: one thread per (padded row, padded block); codes 0/1/2 become the N
+// (weight -1) and P (+1) sign planes, each in the Q1_0 bit order.  A code 3
+// (not a weight) sets g_q2_bad_code and is packed as 0.
+static __device__ unsigned g_q2_bad_code = 0u;
+
+__global__ void k_pack_q2(const uint8_t* __restrict__ blocks, int64_t rows, int64_t nb, int64_t nbp,
+                          int64_t rows_pad, uint32_t* __restrict__ bits, uint16_t* __restrict__ scales) {
+  int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= rows_pad * nbp) return;
+  int64_t r = idx / nbp, b = idx % nbp;
+  int64_t p = r / kPanel;
+  int rr = int(r % kPanel);
+  uint32_t pw[4] = {0u, 0u, 0u, 0u}, nw[4] = {0u, 0u, 0u, 0u};
+  uint16_t sc = 0;
+  if (r < rows && b < nb) {
+    const uint8_t* blk = blocks + (r * nb + b) * 34;
+    sc = uint16_t(blk[0] | (blk[1] << 8));
+    uint8_t qs[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) qs[j] = blk[2 + j];
+    bool bad = false;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+#pragma unroll
+      for (int pl = 0; pl < 8; ++pl)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = elem_of(w, pl, i);
+          const uint32_t c = (qs[e >> 2] >> (2 * (e & 3))) & 3u;
+          pw[w] |= uint32_t(c == 2u) << (8 * i + pl);
+          nw[w] |= uint32_t(c == 0u) << (8 * i + pl);
+          bad |= c == 3u;
+        }
+    if (bad) atomicOr(&g_q2_bad_code, 1u);
+  }
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    bits[q2_bits_word_index(p, b, rr, w, nbp, 0)] = pw[w];
+    bits[q2_bits_word_index(p, b, rr, w, nbp, 1)] = nw[w];
+  }
+  scales[scale_index(p, b, rr, nbp)] = sc;
+}
+
+__global__ void k_unpack_q2(const uint32_t* __restrict__ bits, const uint16_t* __restrict__ scales,
+                            int64_t rows, int64_t nb, int64_t nbp, uint8_t* __restrict__ blocks) {
+  int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= rows * nb) return;
+  int64_t r = idx / nb, b = idx % nb;
+  int64_t p = r / kPanel;
+  int rr = int(r % kPanel);
+  uint8_t qs[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) qs[j] = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t P = bits[q2_bits_word_index(p, b, rr, w, nbp, 0)];
+    const uint32_t N = bits[q2_bits_word_index(p, b, rr, w, nbp, 1)];
+#pragma unroll
+    for (int pl = 0; pl < 8; ++pl)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = elem_of(w, pl, i);
+        const uint32_t pos = (P >> (8 * i + pl)) & 1u, neg = (N >> (8 * i + pl)) & 1u;
+        const uint32_t c = pos ? 2u : (neg ? 0u : 1u);
+        qs[e >> 2] |= uint8_t(c << (2 * (e & 3)));
+      }
+  }
+  const uint16_t sc = scales[scale_index(p, b, rr, nbp)];
+  uint8_t* blk = blocks + idx * 34;
+  blk[0] = uint8_t(sc & 0xff);
+  blk[1] = uint8_t(sc >> 8);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) blk[2 + j] = qs[j];
+}
+
 static int check_pack_args(const char* who, const void* blocks, int64_t rows, int64_t n, const void* packed) {
   if (rows < 1 || rows > (int64_t(1) << 26) || n < 128 || n > (int64_t(1) << 24) || n % 128)
     return fail(Q1_ERR_ARG, "%s: bad shape rows=%lld n=%lld", who, (long long)rows, (long long)n);
@@ -113,4 +190,39 @@ extern "C" int q1_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t*
   k_unpack<<<dim3(unsigned(grid)), threads, 0, static_cast<cudaStream_t>(stream)>>>(
       bits, scales, rows, L.nb, L.nbp, blocks);
   return cuda_status(cudaGetLastError(), "q1_0_unpack launch");
+}
+
+extern "C" int q2_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* packed, void* stream) {
+  if (int e = check_pack_args("q2_0_pack", blocks, rows, n, packed)) return e;
+  const unsigned zero = 0;
+  if (int e = cuda_status(cudaMemcpyToSymbol(g_q2_bad_code, &zero, sizeof zero), "q2_0_pack")) return e;
+  Layout L = layout_q2(rows, n);
+  uint32_t* bits = static_cast<uint32_t*>(packed);
+  uint16_t* scales = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(packed) + L.bits_bytes);
+  int64_t total = L.rows_pad * L.nbp;
+  int threads = 256;
+  int64_t grid = (total + threads - 1) / threads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  k_pack_q2<<<dim3(unsigned(grid)), threads, 0, s>>>(blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales);
+  if (int e = cuda_status(cudaGetLastError(), "q2_0_pack launch")) return e;
+  // Synchronous for the same reason as q1_0_pack; the code check needs it too.
+  if (int e = cuda_status(cudaStreamSynchronize(s), "q2_0_pack")) return e;
+  unsigned bad = 0;
+  if (int e = cuda_status(cudaMemcpyFromSymbol(&bad, g_q2_bad_code, sizeof bad), "q2_0_pack")) return e;
+  if (bad) return fail(Q1_ERR_ARG, "q2_0_pack: a block holds the code 3, which is not a ternary weight");
+  return Q1_OK;
+}
+
+extern "C" int q2_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t* blocks, void* stream) {
+  if (int e = check_pack_args("q2_0_unpack", blocks, rows, n, packed)) return e;
+  Layout L = layout_q2(rows, n);
+  const uint32_t* bits = static_cast<const uint32_t*>(packed);
+  const uint16_t* scales =
+      reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(packed) + L.bits_bytes);
+  int64_t total = rows * L.nb;
+  int threads = 256;
+  int64_t grid = (total + threads - 1) / threads;
+  k_unpack_q2<<<dim3(unsigned(grid)), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      bits, scales, rows, L.nb, L.nbp, blocks);
+  return cuda_status(cudaGetLastError(), "q2_0_unpack launch");
 }

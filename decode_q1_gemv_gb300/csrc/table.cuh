@@ -49,13 +49,24 @@ __device__ __forceinline__ void scale_consts(float d1, int k, int par, float& dp
   K = -__fmul_rn(dprime, kMagic);
 }
 
+// The Q1_0 constants as the table builders take them (another format passes
+// its own pair; the table's geometry is shared).
+struct ConstsQ1 {
+  static __device__ __forceinline__ void lane(uint32_t word, int k, int par, uint32_t& qp, uint32_t& ci) {
+    lane_consts(word, k, par, qp, ci);
+  }
+  static __device__ __forceinline__ void scale(float d1, int k, int par, float& dprime, float& K) {
+    scale_consts(d1, k, par, dprime, K);
+  }
+};
+
 // Table for blocks [blk0, blk0 + kcb) from a quantized activation (q int8 [n],
 // d fp16 [n/32]).  Sub-blocks past the activation's end get zero constants.
 // Both builders issue the global loads of kTableBatch rounds (a round: one
 // entry per thread) before using any of them, so their latencies overlap; a
 // larger batch holds more registers across the call, and the caller picks the
 // largest that its kernel affords without spilling.
-template <int kTableBatch>
+template <int kTableBatch, class C = ConstsQ1>
 static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, const uint16_t* __restrict__ d1,
                                               int nb, int blk0, int kcb, unsigned char* table, int tid,
                                               int nthreads, int kc) {
@@ -82,7 +93,7 @@ static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, 
       const int g = t >> 2, w = t & 3;
       uint32_t qp[2], ci[2];
 #pragma unroll
-      for (int par = 0; par < 2; ++par) lane_consts(wb[u][par], g & 3, par, qp[par], ci[par]);
+      for (int par = 0; par < 2; ++par) C::lane(wb[u][par], g & 3, par, qp[par], ci[par]);
       QC[g * 4 + w] = make_uint4(qp[0], qp[1], ci[0], ci[1]);
     }
   }
@@ -100,8 +111,8 @@ static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, 
       if (g >= kcb * 4) break;
       const float dv = __half2float(__ushort_as_half(hb[u]));
       float de, dodd, ke, ko;
-      scale_consts(dv, g & 3, 0, de, ke);
-      scale_consts(dv, g & 3, 1, dodd, ko);
+      C::scale(dv, g & 3, 0, de, ke);
+      C::scale(dv, g & 3, 1, dodd, ko);
       DK[g] = make_float4(de, dodd, ke, ko);
     }
   }
@@ -112,7 +123,7 @@ static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, 
 // amax/127, id = d ? 1/d : 0, q = roundf(x*id), scale fp16(d)).  One thread per
 // (sub-block, lane); the 8 threads of a sub-block are consecutive in a warp.
 // nthreads must be a multiple of 32 and every thread of the group must call.
-template <int kTableBatch>
+template <int kTableBatch, class C = ConstsQ1>
 static __device__ __noinline__ void build_table_x(const float* __restrict__ x, int nb, int blk0, int kcb,
                                               unsigned char* table, int tid, int nthreads, int kc) {
   uint32_t* QCw = reinterpret_cast<uint32_t*>(table);
@@ -149,12 +160,12 @@ static __device__ __noinline__ void build_table_x(const float* __restrict__ x, i
       if (t < total) {
         const int k = g & 3, par = l >> 2, w = l & 3;
         uint32_t qp, ci;
-        lane_consts(word, k, par, qp, ci);
+        C::lane(word, k, par, qp, ci);
         QCw[(g * 4 + w) * 4 + par] = qp;
         QCw[(g * 4 + w) * 4 + 2 + par] = ci;
         if ((l & 3) == 0) {
           float dprime, K;
-          scale_consts(G < nsub ? d1 : 0.0f, k, par, dprime, K);
+          C::scale(G < nsub ? d1 : 0.0f, k, par, dprime, K);
           DKf[g * 4 + par] = dprime;
           DKf[g * 4 + 2 + par] = K;
         }

@@ -18,7 +18,9 @@ Input formats:
 Distributions (the shapes of the workloads the pages and the benchmark name):
   sign bits           Bernoulli(0.5), i.e. uniform random bytes
   ternary values      -1, 0, +1 with probabilities (1-p0)/2, p0, (1-p0)/2
-                      (p0 = 1/3 unless a test asks otherwise)
+                      (p0 = 1/3 unless a test asks otherwise); for the
+                      full-size sets, uniform random bytes with the code 3
+                      read as 1 (p0 = 1/2), which is cheap at 7.5 G weights
   d0 "halfnormal"     |N(0, 0.02)| rounded to binary16 (about 0.24 % of blocks
                       land in the binary16 subnormal range)
   d0 "lognormal"      exp(N(ln 0.02, 1)) rounded to binary16 (scales that vary
@@ -174,3 +176,20 @@ def ternary_blocks(rng: np.random.Generator, rows: int, n: int, scale: str = "ha
     codes = ternary_codes(rng, (rows, nb, QK1), p_zero)
     scales = block_scales(rng, (rows, nb), scale)
     return assemble_ternary_blocks(scales, codes)
+
+
+def ternary_blocks_fast(rng: np.random.Generator, rows: int, n: int, scale: str = "halfnormal") -> np.ndarray:
+    """Random Q2_0 blocks for full-size sets: uniform random code bytes with
+    every code 3 replaced by 1, i.e. P(-1) = P(+1) = 1/4, P(0) = 1/2."""
+    if n % QK1:
+        raise ValueError("n must be a multiple of 128")
+    nb = n // QK1
+    b = rng.integers(0, 256, size=(rows, nb, 32), dtype=np.uint8)
+    both = b & (b >> 1) & np.uint8(0x55)      # low bit of every 2-bit field that is 3
+    b &= ~(both << 1).astype(np.uint8)        # 3 -> 1
+    blocks = np.empty((rows, nb, Q2_BLOCK_BYTES), dtype=np.uint8)
+    sbits = block_scales(rng, (rows, nb), scale)
+    blocks[:, :, 0] = (sbits & 0xFF).astype(np.uint8)
+    blocks[:, :, 1] = (sbits >> 8).astype(np.uint8)
+    blocks[:, :, 2:] = b
+    return blocks

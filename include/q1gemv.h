@@ -161,6 +161,47 @@ int q1_0_gemv_multi_plan(const q1_product *products, int count, int sms, q1_mult
 int q1_0_gemm_small(const void *packed, int64_t rows, int64_t n, int64_t nvec, const int8_t *q,
                     const uint16_t *d, float *out, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Q2_0 (ternary) weights: the sibling format the pages name as the next GPU
+ * kernel ("Advantages and efficiency", where optimization goes next;
+ * "Limitations": no Q2_0 GPU kernel yet) without giving its layout or
+ * arithmetic.  This library's reading:
+ *   block (34 bytes) = fp16 scale d0 (little-endian), then 32 bytes of 2-bit
+ *     codes: element j's code is (qs[j/4] >> 2*(j%4)) & 3, and codes 0, 1, 2
+ *     mean the weights -d0, 0, +d0 (code 3 is not a weight);
+ *   row product = the Q1_0 definition at the top of this file with the lane
+ *     sum taken over ternary values: +1 contributes q, -1 the negation of q
+ *     (-(-128) stays -128), 0 nothing.
+ * Every output is bit-identical to that CPU definition.  Same conventions as
+ * the Q1_0 calls.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the packed Q2_0 buffer for a rows x n matrix (34 bytes per 128
+ * weights, rows padded to a multiple of 256 and blocks per row to a multiple
+ * of 4).  Host-only; negative Q1_ERR_ARG for a bad shape. */
+int64_t q2_0_packed_bytes(int64_t rows, int64_t n);
+
+/* Repack Q2_0 weights once into the library's device layout (two sign planes,
+ * +1 and -1, in the Q1_0 bit order).
+ *   blocks : device, rows*(n/128) consecutive 34-byte blocks, row-major, as
+ *            above; only 2-byte alignment is required.
+ *   packed : device, q2_0_packed_bytes(rows, n) bytes, written entirely.
+ * Synchronous.  Returns Q1_ERR_ARG if any element holds the code 3 (the buffer
+ * is then written with those elements as 0), or for a bad shape or pointer. */
+int q2_0_pack(const uint8_t *blocks, int64_t rows, int64_t n, void *packed, void *stream);
+
+/* Inverse of q2_0_pack: writes rows*(n/128) 34-byte blocks identical to the
+ * ones that were packed (codes 0..2). */
+int q2_0_unpack(const void *packed, int64_t rows, int64_t n, uint8_t *blocks, void *stream);
+
+/* Q2_0 matrix-vector product: as q1_0_gemv, with `packed` from q2_0_pack. */
+int q2_0_gemv(const void *packed, int64_t rows, int64_t n, const int8_t *q, const uint16_t *d,
+              float *out, void *stream);
+
+/* Several independent Q2_0 products in one launch: as q1_0_gemv_multi, each
+ * descriptor's `packed` from q2_0_pack(rows, n). */
+int q2_0_gemv_multi(const q1_product *products, int count, void *stream);
+
 /* Device status word of the library's kernels on the current device.  A
  * kernel whose bounded internal wait gives up (it never should: every wait is
  * for work the same kernel issued) sets bit 0 instead of hanging, and skips

@@ -217,3 +217,26 @@ def test_multi_plan_rejects_bad_arguments(lib):
         binding.multi_plan([(32, 100)], sms=4)
     with pytest.raises(binding.Q1Error):
         binding.multi_plan([(32, 128)], sms=-1)
+
+
+# ----------------------------------------------------------- Q2_0 sizes --
+@pytest.mark.parametrize("rows,n,expect", [
+    (1, 128, 256 * 4 * 34),
+    (257, 1024, 512 * 8 * 34),
+    (4096, 14336, 4096 * 112 * 34),
+    (100, 640, 256 * 8 * 34),
+])
+def test_q2_packed_bytes(lib, rows, n, expect):
+    assert binding.q2_packed_bytes(rows, n) == expect
+
+
+@pytest.mark.parametrize("rows,n", [(0, 128), (1, 100), (1, 0), (1 << 27, 128)])
+def test_q2_packed_bytes_rejects_bad_shapes(lib, rows, n):
+    with pytest.raises(binding.Q1Error):
+        binding.q2_packed_bytes(rows, n)
+
+
+def test_q2_null_pointers_rejected_on_host(lib):
+    assert lib.q2_0_pack(None, 32, 128, None, None) == binding.Q1_ERR_ARG
+    assert lib.q2_0_gemv(None, 32, 128, None, None, None, None) == binding.Q1_ERR_ARG
+    assert lib.q2_0_gemv_multi(None, 1, None) == binding.Q1_ERR_ARG
