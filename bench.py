@@ -292,6 +292,46 @@ def time_other_configs(dev, reps: int = 15):
     return res
 
 
+def time_q2_set(dev, steps: int, layers: int = 32):
+    """The same decode set with Q2_0 (ternary) weights, one q2_0_gemv_multi
+    launch per step, timed like the headline (graph replays, inputs larger
+    than L2)."""
+    import torch
+    from decode_q1_gemv_gb300 import synth
+    from decode_q1_gemv_gb300.decode_set import DecodeSet
+
+    shapes = synth.decode_set_shapes()
+    if layers < synth.LLAMA3_8B_LAYERS:
+        shapes = shapes[:7 * layers]
+    ds = DecodeSet(seed=3, device=str(dev), shapes=shapes, fmt="q2")
+    g = ds._capture(lambda: ds.step(schedule="set"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ms = _time_graph(g, steps, torch.cuda.current_stream(dev))
+    wb = ds.weight_bytes
+    peak, _ = measured_peaks()
+    launch_bytes = wb + ds.activation_bytes + ds.output_bytes
+    res = {"products": len(ds.shapes), "weight_bytes": wb, "us": round(ms * 1e3, 2),
+           "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 2),
+           "hbm_frac_of_measured": round(wb / (ms * 1e-3) / 1e9 / peak, 4),
+           "roofline_frac": round(launch_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+           "kernel": "k_q1_multi<8,256,FmtQ2> (q2_0_gemv_multi)",
+           "data": "synthetic ternary: P(-1) = P(+1) = 1/4, P(0) = 1/2; halfnormal fp16 scales"}
+    del ds, g
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_q2_only(args):
+    import torch
+    from decode_q1_gemv_gb300 import binding
+    binding.load()
+    dev = torch.device("cuda:0")
+    print(json.dumps({"q2_0_decode_set": time_q2_set(dev, args.steps, args.layers)}), flush=True)
+    return 0
+
+
 def run_configs_only(args):
     import torch
 
@@ -395,6 +435,9 @@ def run_ours(args):
     other = None
     if rank == 0 and args.configs:
         other = time_other_configs(dev)
+    q2 = None
+    if rank == 0 and args.q2:
+        q2 = time_q2_set(dev, max(args.steps // 2, 20), args.layers)
 
     wb = ds.weight_bytes
     peak, peak_kind = measured_peaks()
@@ -421,6 +464,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_set": round(step_ms * 1e3, 2),
             "other_configs_cold_l2": other,
+            "q2_0_decode_set": q2,
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "us_per_set_by_schedule": sched_us,
             "launches_by_schedule": {sch: ds.launches(sch) for sch in schedules},
@@ -453,6 +497,10 @@ def main():
                     help="skip timing the single-product and batched configurations")
     ap.add_argument("--configs-only", action="store_true",
                     help="time only the single-product and batched configurations (for profiling)")
+    ap.add_argument("--no-q2", dest="q2", action="store_false",
+                    help="skip timing the decode set with Q2_0 (ternary) weights")
+    ap.add_argument("--q2-only", action="store_true",
+                    help="time only the Q2_0 decode set (for profiling)")
     ap.add_argument("--layers", type=int, default=32, help="layers of the decode set (32 = full set with lm_head)")
     ap.add_argument("--schedules", default="grouped,decode,separate",
                     help="schedules timed besides 'set' (comma list; empty for none)")
@@ -463,6 +511,8 @@ def main():
         return run_reference(args)
     if args.configs_only:
         return run_configs_only(args)
+    if args.q2_only:
+        return run_q2_only(args)
     return run_ours(args)
 
 

@@ -17,6 +17,9 @@ per product.  Schedules of the same work:
 Every schedule can be captured once as a CUDA graph and replayed; the kernels
 use programmatic dependent launch, so each launch's weight streaming begins
 while the previous kernel drains.
+
+fmt="q2" builds the same set with Q2_0 (ternary) weights (q2_0_* calls,
+34 bytes per 128 weights, synth.ternary_blocks_fast).
 """
 from __future__ import annotations
 
@@ -34,7 +37,15 @@ def _round_up(x: int, a: int) -> int:
 
 class DecodeSet:
     def __init__(self, seed: int = 3, device: str = "cuda", shapes=None, scale: str = "halfnormal",
-                 outliers: float = 0.0):
+                 outliers: float = 0.0, fmt: str = "q1"):
+        if fmt not in ("q1", "q2"):
+            raise ValueError(f"unknown weight format {fmt!r}")
+        self.fmt = fmt
+        self.block_bytes = synth.BLOCK_BYTES if fmt == "q1" else synth.Q2_BLOCK_BYTES
+        self._packed_bytes = binding.packed_bytes if fmt == "q1" else binding.q2_packed_bytes
+        self._pack = binding.pack if fmt == "q1" else binding.q2_pack
+        self._gemv = binding.gemv if fmt == "q1" else binding.q2_gemv
+        self._gemv_multi = binding.gemv_multi if fmt == "q1" else binding.q2_gemv_multi
         self.seed = seed
         self.device = torch.device(device)
         self.shapes = list(shapes) if shapes is not None else synth.decode_set_shapes()
@@ -45,14 +56,14 @@ class DecodeSet:
         total = 0
         for _, rows, n in self.shapes:
             self.offsets.append(total)
-            total += _round_up(binding.packed_bytes(rows, n), ALIGN)
+            total += _round_up(self._packed_bytes(rows, n), ALIGN)
         self.packed = torch.empty(total, dtype=torch.uint8, device=self.device)
-        self.weight_bytes = sum(rows * n * 18 // 128 for _, rows, n in self.shapes)
+        self.weight_bytes = sum(rows * n * self.block_bytes // 128 for _, rows, n in self.shapes)
         for i, (_, rows, n) in enumerate(self.shapes):
             blocks = torch.from_numpy(self.host_blocks(i)).to(self.device)
-            nbytes = binding.packed_bytes(rows, n)
+            nbytes = self._packed_bytes(rows, n)
             view = self.packed[self.offsets[i]:self.offsets[i] + nbytes]
-            binding.pack(blocks, rows, n, view)
+            self._pack(blocks, rows, n, view)
             del blocks
         # Activations (f32 inputs), their q8_0 form, and outputs: one contiguous
         # buffer each (so a host round trip is one copy in and one copy out),
@@ -83,6 +94,8 @@ class DecodeSet:
     # -------------------------------------------------------- host inputs --
     def host_blocks(self, i: int) -> np.ndarray:
         _, rows, n = self.shapes[i]
+        if self.fmt == "q2":
+            return synth.ternary_blocks_fast(synth.rng_for(self.seed, i, 0, 2), rows, n, self.scale)
         return synth.weight_blocks(synth.rng_for(self.seed, i, 0), rows, n, self.scale)
 
     def host_x(self, i: int) -> np.ndarray:
@@ -92,7 +105,7 @@ class DecodeSet:
     # ------------------------------------------------------------ compute --
     def packed_view(self, i: int) -> torch.Tensor:
         _, rows, n = self.shapes[i]
-        return self.packed[self.offsets[i]:self.offsets[i] + binding.packed_bytes(rows, n)]
+        return self.packed[self.offsets[i]:self.offsets[i] + self._packed_bytes(rows, n)]
 
     SCHEDULES = ("set", "grouped", "decode", "separate")
 
@@ -140,15 +153,15 @@ class DecodeSet:
         if schedule == "separate":
             for i, (_, rows, n) in enumerate(self.shapes):
                 binding.quantize(self.x[i], self.q[i], self.d[i], stream=stream)
-                binding.gemv(self.packed_view(i), rows, n, self.q[i], self.d[i], self.out[i], stream=stream)
+                self._gemv(self.packed_view(i), rows, n, self.q[i], self.d[i], self.out[i], stream=stream)
             return
         for arr in self._arrays(schedule):
-            binding.gemv_multi(array=arr, stream=stream)
+            self._gemv_multi(array=arr, stream=stream)
 
     def products(self, stream=None):
         """Enqueue the products alone (activations already quantized)."""
         for i, (_, rows, n) in enumerate(self.shapes):
-            binding.gemv(self.packed_view(i), rows, n, self.q[i], self.d[i], self.out[i], stream=stream)
+            self._gemv(self.packed_view(i), rows, n, self.q[i], self.d[i], self.out[i], stream=stream)
 
     def _capture(self, fn):
         s = torch.cuda.Stream(self.device)
