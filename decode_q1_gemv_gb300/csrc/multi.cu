@@ -194,6 +194,11 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
         }
       }
       if (!ok) atomicOr(&g_status_dp4a, kStatusWaitTimeout);
+      // The CTA's shared memory must outlive every copy issued into it: wait
+      // (bounded) until the last S stages have landed.  On the normal path the
+      // consumers have already waited for them and this returns at once.
+      for (int k = it > S ? it - S : 0; k < it; ++k)
+        mbar_wait(smem_addr(&bars[k % S]), uint32_t(k / S) & 1u, 100000000ull);
     }
     return;
   }
@@ -222,6 +227,11 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
   }
   if (last_j < 0) pdl_launch_dependents();
 
+  // A consumer wait can only give up on a stage whose copy never lands.  Every
+  // consumer warp needs that stage before its next named barrier, so all of
+  // them give up at the same stage and leave without reaching a barrier the
+  // others wait at; the lanes of a warp poll the same barrier and clock in
+  // step, so they decide together.
   bool ok = true;
   int it = 0;
   for (int j = j_first; j < a.count && a.p[j].cost_begin < hi && ok; ++j) {
