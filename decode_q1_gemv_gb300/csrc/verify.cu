@@ -6,7 +6,8 @@
 // Mirrors bankML "docs/modules/gpu.md", "How it is verified": random weights
 // and activations including -128 quants, plus a layer-shaped regime with
 // per-block scales that make products inexact in f32; one line per kernel and
-// shape, or the first differing row.
+// shape, or the first differing row.  The Q2_0 (ternary) product is checked
+// the same way (the pages list it for --verify among the next steps).
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -14,7 +15,7 @@
 #include <string>
 #include <vector>
 
-#include "common.cuh"
+#include "q2.cuh"
 
 namespace q1 {
 namespace {
@@ -43,6 +44,32 @@ float h_row(const uint8_t* row, int64_t nb, const int8_t* q, const uint16_t* d) 
           const int qq = q[b * kBlock + j];
           const bool plus = (blk[2 + j / 8] >> (j % 8)) & 1;
           s += plus ? qq : (qq == -128 ? -128 : -qq);
+        }
+        const float d1 = h_half(d[b * 4 + k]);
+        ab = (k == 0) ? d1 * float(s) : std::fmaf(d1, float(s), ab);
+      }
+      a[l] = std::fmaf(d0, ab, a[l]);
+    }
+  }
+  return ((a[0] + a[4]) + (a[2] + a[6])) + ((a[1] + a[5]) + (a[3] + a[7]));
+}
+
+// Q2_0 row: 34-byte blocks, codes 0/1/2 = -1/0/+1 (q2.cuh).
+float h_row_q2(const uint8_t* row, int64_t nb, const int8_t* q, const uint16_t* d) {
+  float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int64_t b = 0; b < nb; ++b) {
+    const uint8_t* blk = row + b * 34;
+    const float d0 = h_half(uint16_t(blk[0] | (blk[1] << 8)));
+    for (int l = 0; l < 8; ++l) {
+      float ab = 0.0f;
+      for (int k = 0; k < 4; ++k) {
+        int s = 0;
+        for (int i = 0; i < 4; ++i) {
+          const int j = 32 * k + 4 * l + i;
+          const int qq = q[b * kBlock + j];
+          const int code = (blk[2 + j / 4] >> (2 * (j % 4))) & 3;
+          if (code == 2) s += qq;
+          else if (code == 0) s += (qq == -128 ? -128 : -qq);
         }
         const float d1 = h_half(d[b * 4 + k]);
         ab = (k == 0) ? d1 * float(s) : std::fmaf(d1, float(s), ab);
@@ -87,7 +114,7 @@ uint16_t scale_bits(Rng& r, bool layer) {
 }
 
 struct Case {
-  const char* kernel;  // "gemv" or "gemm_small"
+  const char* kernel;  // "q1_0_gemv", "q1_0_gemm_small" or "q2_0_gemv"
   int64_t rows, n, nvec;
   bool layer;          // layer-shaped regime: raw quants (with -128), log-normal scales
 };
@@ -127,14 +154,20 @@ uint32_t fbits(float f) {
 // Returns Q1_OK, Q1_MISMATCH or an error.
 int run_case(const Case& c, uint64_t seed, Report& rep) {
   Rng rng{seed};
+  const bool ternary = std::strcmp(c.kernel, "q2_0_gemv") == 0;
   const int64_t nb = c.n / kBlock;
-  std::vector<uint8_t> blocks(size_t(c.rows * nb * kBlockBytes));
+  const int64_t bbytes = ternary ? 34 : kBlockBytes;
+  std::vector<uint8_t> blocks(size_t(c.rows * nb * bbytes));
   for (int64_t i = 0; i < c.rows * nb; ++i) {
-    uint8_t* blk = &blocks[size_t(i * kBlockBytes)];
+    uint8_t* blk = &blocks[size_t(i * bbytes)];
     const uint16_t s = scale_bits(rng, c.layer);
     blk[0] = uint8_t(s & 0xff);
     blk[1] = uint8_t(s >> 8);
-    for (int j = 0; j < 16; ++j) blk[2 + j] = uint8_t(rng.next());
+    for (int j = 2; j < bbytes; ++j) {
+      uint8_t v = uint8_t(rng.next());
+      if (ternary) v &= uint8_t(~((v & (v >> 1) & 0x55) << 1));  // code 3 -> 1 (a zero weight)
+      blk[j] = v;
+    }
   }
   std::vector<int8_t> q(size_t(c.nvec * c.n));
   std::vector<uint16_t> d(size_t(c.nvec * c.n / kSub));
@@ -150,7 +183,7 @@ int run_case(const Case& c, uint64_t seed, Report& rep) {
   }
 
   Dev dev;
-  const int64_t pbytes = q1_0_packed_bytes(c.rows, c.n);
+  const int64_t pbytes = ternary ? q2_0_packed_bytes(c.rows, c.n) : q1_0_packed_bytes(c.rows, c.n);
   uint8_t* d_blocks = static_cast<uint8_t*>(dev.get(blocks.size()));
   void* d_packed = dev.get(size_t(pbytes));
   int8_t* d_q = static_cast<int8_t*>(dev.get(q.size()));
@@ -161,7 +194,9 @@ int run_case(const Case& c, uint64_t seed, Report& rep) {
     return fail(Q1_ERR_NOMEM, "q1_0_verify: device allocation failed");
 
   if (int e = cuda_status(cudaMemcpy(d_blocks, blocks.data(), blocks.size(), cudaMemcpyHostToDevice), "q1_0_verify copy")) return e;
-  if (int e = q1_0_pack(d_blocks, c.rows, c.n, d_packed, nullptr)) return e;
+  if (int e = ternary ? q2_0_pack(d_blocks, c.rows, c.n, d_packed, nullptr)
+                      : q1_0_pack(d_blocks, c.rows, c.n, d_packed, nullptr))
+    return e;
   if (x.empty()) {
     if (int e = cuda_status(cudaMemcpy(d_q, q.data(), q.size(), cudaMemcpyHostToDevice), "q1_0_verify copy")) return e;
     if (int e = cuda_status(cudaMemcpy(d_d, d.data(), d.size() * 2, cudaMemcpyHostToDevice), "q1_0_verify copy")) return e;
@@ -183,7 +218,8 @@ int run_case(const Case& c, uint64_t seed, Report& rep) {
         return Q1_MISMATCH;
       }
   }
-  int e = (std::strcmp(c.kernel, "gemv") == 0)
+  int e = ternary ? q2_0_gemv(d_packed, c.rows, c.n, d_q, d_d, d_out, nullptr)
+          : (std::strcmp(c.kernel, "q1_0_gemv") == 0)
               ? q1_0_gemv(d_packed, c.rows, c.n, d_q, d_d, d_out, nullptr)
               : q1_0_gemm_small(d_packed, c.rows, c.n, c.nvec, d_q, d_d, d_out, nullptr);
   if (e) return e;
@@ -191,16 +227,19 @@ int run_case(const Case& c, uint64_t seed, Report& rep) {
   if (int e2 = cuda_status(cudaMemcpy(out.data(), d_out, out.size() * 4, cudaMemcpyDeviceToHost), "q1_0_verify result")) return e2;
   for (int64_t v = 0; v < c.nvec; ++v)
     for (int64_t r = 0; r < c.rows; ++r) {
-      const float want = h_row(&blocks[size_t(r * nb * kBlockBytes)], nb, &q[size_t(v * c.n)], &d[size_t(v * c.n / kSub)]);
+      const uint8_t* row = &blocks[size_t(r * nb * bbytes)];
+      const int8_t* qv = &q[size_t(v * c.n)];
+      const uint16_t* dv = &d[size_t(v * c.n / kSub)];
+      const float want = ternary ? h_row_q2(row, nb, qv, dv) : h_row(row, nb, qv, dv);
       const float got = out[size_t(v * c.rows + r)];
       if (fbits(want) != fbits(got)) {
-        rep.add("q1_0_%s %lldx%lld nvec=%lld %s: row %lld differs (vector %lld: gpu 0x%08x, cpu 0x%08x)\n", c.kernel,
+        rep.add("%s %lldx%lld nvec=%lld %s: row %lld differs (vector %lld: gpu 0x%08x, cpu 0x%08x)\n", c.kernel,
                 (long long)c.rows, (long long)c.n, (long long)c.nvec, c.layer ? "layer-shaped" : "quantized",
                 (long long)r, (long long)v, fbits(got), fbits(want));
         return Q1_MISMATCH;
       }
     }
-  rep.add("q1_0_%s %lldx%lld nvec=%lld %s: bit-exact\n", c.kernel, (long long)c.rows, (long long)c.n,
+  rep.add("%s %lldx%lld nvec=%lld %s: bit-exact\n", c.kernel, (long long)c.rows, (long long)c.n,
           (long long)c.nvec, c.layer ? "layer-shaped" : "quantized");
   return Q1_OK;
 }
@@ -213,14 +252,16 @@ extern "C" int q1_0_verify(int flags, char* report, size_t report_len) {
   Report rep{report, report_len, 0};
   if (report && report_len) report[0] = 0;
   static const Case quick[] = {
-      {"gemv", 64, 128, 1, true},
-      {"gemv", 100, 384, 1, false},
+      {"q1_0_gemv", 64, 128, 1, true},
+      {"q1_0_gemv", 100, 384, 1, false},
+      {"q2_0_gemv", 64, 256, 1, true},
   };
   static const Case full[] = {
-      {"gemv", 64, 128, 1, true},       {"gemv", 100, 384, 1, false},   {"gemv", 256, 1024, 1, false},
-      {"gemv", 1000, 4096, 1, true},    {"gemv", 33, 14336, 1, true},   {"gemv", 4096, 4096, 1, false},
-      {"gemv", 9999, 1152, 1, true},    {"gemm_small", 300, 1024, 3, true},
-      {"gemm_small", 200, 4096, 16, false}, {"gemm_small", 64, 512, 64, true},
+      {"q1_0_gemv", 64, 128, 1, true},       {"q1_0_gemv", 100, 384, 1, false},   {"q1_0_gemv", 256, 1024, 1, false},
+      {"q1_0_gemv", 1000, 4096, 1, true},    {"q1_0_gemv", 33, 14336, 1, true},   {"q1_0_gemv", 4096, 4096, 1, false},
+      {"q1_0_gemv", 9999, 1152, 1, true},    {"q1_0_gemm_small", 300, 1024, 3, true},
+      {"q1_0_gemm_small", 200, 4096, 16, false}, {"q1_0_gemm_small", 64, 512, 64, true},
+      {"q2_0_gemv", 64, 128, 1, true},    {"q2_0_gemv", 1000, 4096, 1, false}, {"q2_0_gemv", 33, 14336, 1, true},
   };
   const Case* cs = (flags & 1) ? quick : full;
   const size_t nc = (flags & 1) ? sizeof quick / sizeof quick[0] : sizeof full / sizeof full[0];

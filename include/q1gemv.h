@@ -212,7 +212,8 @@ int q1_device_status(int clear);
 
 /* On-card self-check ("How it is verified": verify_q1_0 compares every kernel
  * and shape with the CPU bits, including -128 quants and a layer-shaped regime
- * whose per-block scales make products inexact in f32).  Runs synchronously on
+ * whose per-block scales make products inexact in f32; the Q2_0 product is
+ * checked the same way).  Runs synchronously on
  * the current device with its own allocations, against a host-side reference
  * compiled into the library.
  *   flags  : 0 = default shape set; 1 = quick (two small shapes).

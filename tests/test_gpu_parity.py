@@ -59,7 +59,10 @@ def gpu_gemm(blocks: np.ndarray, q: np.ndarray, d: np.ndarray) -> np.ndarray:
 def test_library_self_check():
     rc, report = binding.verify(quick=False)
     assert rc == binding.Q1_OK, report
-    assert "bit-exact" in report
+    lines = report.strip().splitlines()
+    assert len(lines) == 13 and all(line.endswith("bit-exact") for line in lines), report
+    for kernel in ("q1_0_gemv ", "q1_0_gemm_small ", "q2_0_gemv "):
+        assert any(line.startswith(kernel) for line in lines), (kernel, report)
 
 
 # --------------------------------------------------------------- packing --
