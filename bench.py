@@ -166,6 +166,59 @@ def cpu_oracle_sample(layers: int, budget_s: float, threads: int, seed: int = 3)
     return gbs, desc, threads
 
 
+def cpu_context(seed: int = 3):
+    """Host-side context for the CPU baseline: the single-thread oracle on the
+    256x1024 and 4096x4096 products, on 14336x4096 with 16 vectors and on layer
+    0 of the decode set; and a streaming read of a 768 MiB buffer (far larger
+    than the caches) at 1..all threads, the memory floor a CPU decode is held
+    to (bankML "docs/modules/par.md", benchmarks: bench_memory_floor)."""
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    import oracle
+    from decode_q1_gemv_gb300 import synth
+
+    oracle.build()
+    single = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return (time.perf_counter() - t0) * 1e6
+
+    for name, rows, n, nvec, outl in (("gemv_256x1024", 256, 1024, 1, 0.0), ("gemv_4096x4096", 4096, 4096, 1, 0.01),
+                                      ("b16_14336x4096", 14336, 4096, 16, 0.0)):
+        blocks = synth.weight_blocks(synth.rng_for(seed, rows, n, 0), rows, n)
+        x = synth.activations(synth.rng_for(seed, rows, n, 1), nvec, n, outliers=outl)
+        q, d = oracle.q8_quantize(x)
+        fn = (lambda: oracle.gemv(blocks, q[0], d[0])) if nvec == 1 else (lambda: oracle.gemm(blocks, q, d))
+        single[name] = round(timed(fn), 1)
+    layer = [(synth.weight_blocks(synth.rng_for(seed, i, 0), rows, n), synth.activations(synth.rng_for(seed, i, 1), 1, n))
+             for i, (_, rows, n) in enumerate(synth.decode_set_shapes()[:7])]
+
+    def one_layer():
+        for blocks, x in layer:
+            q, d = oracle.q8_quantize(x)
+            oracle.gemv(blocks, q[0], d[0])
+    single["decode_set_layer0"] = round(timed(one_layer), 1)
+
+    buf = np.ones(768 * 1024 * 1024 // 8, dtype=np.float64)
+    floor = {}
+    ncpu = os.cpu_count() or 1
+    for t in sorted({1, 2, 4, 8, ncpu} & set(range(1, ncpu + 1))):
+        parts = np.array_split(buf, t)
+        with cf.ThreadPoolExecutor(t) as ex:
+            list(ex.map(np.sum, parts))  # warm
+            t0 = time.perf_counter()
+            list(ex.map(np.sum, parts))
+            dt = time.perf_counter() - t0
+        floor[str(t)] = round(buf.nbytes / dt / 1e9, 2)
+    del buf
+    return {"oracle_single_thread_us": single, "memory_floor_read_gbs_by_threads": floor,
+            "memory_floor_buffer_bytes": 768 * 1024 * 1024}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -447,10 +500,11 @@ def run_ours(args):
     traffic = recorded_traffic()
     clocks = sampler.summary()
 
-    cpu = None
+    cpu = ctx = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, desc, cores = cpu_oracle_sample(layers=4, budget_s=args.cpu_budget, threads=os.cpu_count() or 1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+        ctx = cpu_context()
 
     if rank == 0:
         line = {
@@ -478,6 +532,7 @@ def run_ours(args):
             "gpu_launches": ds.launches("set") * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "cpu_context": ctx,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
