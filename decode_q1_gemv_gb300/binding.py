@@ -126,11 +126,13 @@ def _stream_ptr(stream) -> int:
     return int(s.cuda_stream)
 
 
-def _dev(t: torch.Tensor, name: str, dtypes) -> int:
+def _dev(t: torch.Tensor, name: str, dtypes, host_ok: bool = False) -> int:
+    """Pointer of a contiguous CUDA tensor (or, where host_ok, of a pinned
+    host tensor, which the kernels address directly)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if t.dtype not in dtypes:
         raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
     if not t.is_contiguous():
@@ -204,7 +206,8 @@ def gemv(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tens
 
 def product_array(items):
     """Build a ctypes q1_product array from tuples
-    (packed, rows, n, x_or_None, q_or_None, d_or_None, out) of CUDA tensors."""
+    (packed, rows, n, x_or_None, q_or_None, d_or_None, out) of CUDA tensors;
+    x, q, d and out may also be pinned host tensors."""
     arr = (Product * len(items))()
     for i, (packed, rows, n, x, q, d, out) in enumerate(items):
         if x is None and (q is None or d is None):
@@ -216,10 +219,10 @@ def product_array(items):
         if out.numel() != rows:
             raise ValueError("out must hold rows values")
         arr[i] = Product(_dev(packed, "packed", (torch.uint8,)), int(rows), int(n),
-                         _dev(x, "x", (torch.float32,)) if x is not None else None,
-                         _dev(q, "q", (torch.int8,)) if q is not None else None,
-                         _dev(d, "d", _SCALE_DTYPES) if d is not None else None,
-                         _dev(out, "out", (torch.float32,)))
+                         _dev(x, "x", (torch.float32,), True) if x is not None else None,
+                         _dev(q, "q", (torch.int8,), True) if q is not None else None,
+                         _dev(d, "d", _SCALE_DTYPES, True) if d is not None else None,
+                         _dev(out, "out", (torch.float32,), True))
     return arr
 
 

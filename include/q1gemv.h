@@ -22,7 +22,12 @@
  *     rows <= 1<<26.
  *   - Pointers are DEVICE pointers owned by the caller unless noted; the
  *     library keeps no reference to them after the call returns.  Buffers must
- *     be 16-byte aligned and must not overlap.
+ *     be 16-byte aligned and must not overlap.  The activation and output
+ *     pointers of the products (x, q, d, out) may instead point into pinned
+ *     host memory (cudaHostAlloc / cudaHostRegister) where the device can
+ *     address it (unified addressing; on a GB300 the kernels then read and
+ *     write it over NVLink-C2C, so a host round trip needs no separate copy).
+ *     Packed weights must be device memory.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     only enqueue work; nothing blocks the host unless noted.
  *   - Return value: Q1_OK (0) on success, a negative Q1_ERR_* code on a

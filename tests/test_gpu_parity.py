@@ -308,6 +308,28 @@ def test_gemv_multi_fused_equals_quantize_then_gemv():
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+def test_gemv_multi_host_activations_and_outputs():
+    """Activations and outputs in pinned host memory, read and written by the
+    kernel directly: the same bits as device buffers."""
+    shapes = [(4096, 4096), (1024, 4096), (300, 14336)]
+    items_dev, items_host = [], []
+    for i, (rows, n) in enumerate(shapes):
+        rng = synth.rng_for(140, i)
+        blocks = synth.weight_blocks(rng, rows, n)
+        packed = binding.pack(dev(blocks), rows, n)
+        x = synth.activations(rng, 1, n)[0]
+        items_dev.append((packed, rows, n, dev(x), None, None, torch.empty(rows, device="cuda")))
+        hx = torch.from_numpy(x).pin_memory()
+        items_host.append((packed, rows, n, hx, None, None, torch.full((rows,), float("nan")).pin_memory()))
+    binding.gemv_multi(items_dev)
+    binding.gemv_multi(items_host)
+    torch.cuda.synchronize()
+    for a, b in zip(items_dev, items_host):
+        assert torch.equal(a[-1].cpu().view(torch.int32), b[-1].view(torch.int32))
+    with pytest.raises(ValueError):
+        binding.product_array([(items_dev[0][0], 4096, 4096, torch.zeros(4096), None, None, items_dev[0][-1])])
+
+
 def test_gemv_multi_rejects_bad_lists():
     rows, n = 32, 128
     packed = torch.empty(binding.packed_bytes(rows, n), dtype=torch.uint8, device="cuda")
