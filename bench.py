@@ -58,11 +58,18 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the streaming kernel's code with comments and blank space
+    removed: a recorded ncu capture stays valid across comment edits and is
+    dropped by any change to the code itself."""
+    import re
     h = hashlib.sha256()
     for rel in ("decode_q1_gemv_gb300/csrc/multi.cu", "decode_q1_gemv_gb300/csrc/table.cuh",
-                "decode_q1_gemv_gb300/csrc/common.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+                "decode_q1_gemv_gb300/csrc/common.cuh", "decode_q1_gemv_gb300/csrc/q2.cuh"):
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

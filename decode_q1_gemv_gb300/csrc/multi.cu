@@ -1,5 +1,6 @@
-// multi.cu -- the streaming matrix-vector kernel: q1_0_gemv (one product) and
-// q1_0_gemv_multi (up to Q1_MAX_PRODUCTS independent products in one launch).
+// multi.cu -- the streaming matrix-vector kernel: q1_0_gemv / q2_0_gemv (one
+// product) and q1_0_gemv_multi / q2_0_gemv_multi (up to Q1_MAX_PRODUCTS
+// independent products in one launch).
 //
 // Definition (bankML "docs/modules/gpu.md", "kernels.rs -- the Q1_0 kernels",
 // first and second bullets): each output row is one dot product of 128-weight
@@ -7,24 +8,26 @@
 // wraps -128 to -128), ab = d1*s then fma(d1, s, ab), acc = fma(d0, ab, acc),
 // and the horizontal sum (a0+a4 + a2+a6) + (a1+a5 + a3+a7).  Lanes are
 // independent chains, so four threads share a row, two lanes each; table.cuh
-// explains how every step keeps the definition's single roundings.
+// explains how every step keeps the definition's single roundings, and q2.cuh
+// the same for the ternary Q2_0 format (the kernel is a template over the
+// format: FmtQ1, FmtQ2).
 //
 // Structure.  A CTA is one producer warp and four consumer warps per panel
-// slot (two slots for R <= 4 rows per thread, one for R = 8).  The producer
+// slot (two slots for R <= 2 rows per thread, one for R = 8).  The producer
 // streams packed weights HBM -> shared memory with 1-D bulk copies into a
 // ring of stages (mbarrier full/empty pairs).  A stage is one quad of blocks
 // (4 x 128 weights per row) for the CTA's current tile of slots*R panels (8
-// panels = 256 rows for the large launches): 2 KB of sign words and 256 B of
-// scales per panel, two contiguous copies thanks to the packed layout.
-// Consumer thread (row, lane pair) handles R rows of a tile.  CTAs are
-// persistent: the
-// products' tiles are split into contiguous ranges of equal weight bytes, one
-// range per CTA, and the producer runs ahead across tile and product
-// boundaries.  The producer reads only weights, so it starts before
-// griddepcontrol.wait; consumers wait for the preceding kernel before reading
-// the activation (f32, quantized here exactly as q8_quantize_act does, or
-// already quantized).  Every wait is bounded and reports through the device
-// status word instead of hanging.
+// panels = 256 rows for the large launches): 2 KB (Q2_0: 4 KB) of sign words
+// and 256 B of scales per panel, two contiguous copies thanks to the packed
+// layout.  Consumer thread (row, lane pair) handles R rows of a tile.  CTAs
+// are persistent: the products' tiles lie on one cost axis, each CTA owns a
+// contiguous range of it (placed by the host for many-product launches) and
+// starts at its first product by binary search; the producer runs ahead
+// across tile and product boundaries.  The producer reads only weights, so it
+// starts before griddepcontrol.wait; consumers wait for the preceding kernel
+// before reading the activation (f32, quantized here exactly as
+// q8_quantize_act does, or already quantized).  Every wait is bounded and
+// reports through the device status word instead of hanging.
 #include <algorithm>
 
 #include "q2.cuh"
@@ -34,8 +37,8 @@ namespace q1 {
 static __device__ unsigned g_status_dp4a = 0u;
 
 // Panels computed side by side (4 consumer warps = 32 rows each): two for
-// R <= 4 rows per thread, one for R = 8 (same 8-panel tile, twice the rows
-// per thread, half the warps).
+// R <= 2 rows per thread, one for R = 8 (an 8-panel tile with half the warps
+// of two slots of four rows, which measured slower).
 template <int R>
 __host__ __device__ constexpr int slots_of() { return R >= 8 ? 1 : 2; }
 template <int R>
