@@ -48,7 +48,10 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
   constexpr int S = kProdStages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
   unsigned char* tables = smem + S * SB + 128;
-  const int tb = table_bytes(a.kc);
+  // Table capacity in blocks, a compile-time stride between the vectors'
+  // tables (the chunk a.kc never exceeds it).
+  constexpr int KCM = (128 / V) / 8 * 8 > 8 ? (128 / V) / 8 * 8 : 8;
+  constexpr int tb = table_bytes(KCM);
   const int lane = threadIdx.x & 31;
   const int w = lane & 3;                               // word w: lanes w and w+4
   const int prow = (threadIdx.x >> 5) * 8 + (lane >> 2);  // row within the panel
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
       unsigned char* t = tables + v * tb;
       const int vv = min(v0 + v, a.nvec - 1);
       build_table_q<4>(a.q + int64_t(vv) * a.n, a.d1 + int64_t(vv) * (a.n / kSub), a.nb, blk0, kcb, t,
-                       threadIdx.x, kThreads, a.kc);
+                       threadIdx.x, kThreads, KCM);
     }
     __syncthreads();
 
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(kThreads) k_q1_prod(ProdArgs a) {
       for (int v = 0; v < V; ++v) {
         const unsigned char* t = tables + v * tb;
         quad_all<R>(wv, sc, reinterpret_cast<const uint4*>(t) + (b - blk0) * 16,
-                    reinterpret_cast<const float4*>(t + table_dk_offset(a.kc)) + (b - blk0) * 4, w, accE[v],
+                    reinterpret_cast<const float4*>(t + table_dk_offset(KCM)) + (b - blk0) * 4, w, accE[v],
                     accO[v]);
       }
     }
@@ -168,7 +171,7 @@ static int launch(const ProdArgs& a0, int64_t panels, cudaStream_t s, const char
   const int64_t pgroups = (panels + R - 1) / R;
   const int64_t grid = pgroups * a.vgroups;
   if (grid > 0x7fffffff) return fail(Q1_ERR_ARG, "%s: matrix too large for one launch", who);
-  const int smem = prod_smem_bytes<R, V>(a.kc);
+  const int smem = prod_smem_bytes<R, V>(std::max(8, (128 / V) / 8 * 8));
   static int attr_done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
