@@ -56,9 +56,11 @@ def test_pack_rejects_code_three():
     binding.q2_pack(dev(ok), rows, n)  # the flag does not stick to the next call
 
 
-@pytest.mark.parametrize("rows,n", [(1, 128), (7, 256), (33, 384), (300, 1024), (1000, 4096), (513, 14336)])
+@pytest.mark.parametrize("rows,n", [(1, 128), (7, 256), (33, 384), (300, 1024), (1000, 4096), (513, 14336),
+                                    (70, 17408), (2600, 20480)])
 @pytest.mark.parametrize("regime", ["halfnormal", "lognormal"])
 def test_gemv_parity(rows, n, regime):
+    """n above 16384 builds the activation table in chunks inside the tile loop."""
     rng = synth.rng_for(410, rows, n, len(regime))
     tb = synth.ternary_blocks(rng, rows, n, regime)
     q, d = synth.raw_quants(rng, 1, n, scale=regime, m128_frac=0.03)
