@@ -327,10 +327,11 @@ def device_status(clear: bool = True) -> int:
     return v
 
 
-def verify(quick: bool = False) -> tuple[int, str]:
-    """Run the on-card self-check; returns (status, report text)."""
+def verify(quick: bool = False, corrupt: bool = False) -> tuple[int, str]:
+    """Run the on-card self-check; returns (status, report text).  corrupt=True
+    runs the negative control (one row's packed scales doubled per case)."""
     buf = ctypes.create_string_buffer(16384)
-    rc = load().q1_0_verify(1 if quick else 0, buf, len(buf))
+    rc = load().q1_0_verify((1 if quick else 0) | (2 if corrupt else 0), buf, len(buf))
     return rc, buf.value.decode(errors="replace")
 
 

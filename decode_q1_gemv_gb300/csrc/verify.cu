@@ -151,8 +151,10 @@ uint32_t fbits(float f) {
   return u;
 }
 
-// Returns Q1_OK, Q1_MISMATCH or an error.
-int run_case(const Case& c, uint64_t seed, Report& rep) {
+// Returns Q1_OK, Q1_MISMATCH or an error.  With `corrupt`, the packed scales
+// of one row whose reference output is nonzero are doubled after packing (a
+// negative control: the check must then report that row).
+int run_case(const Case& c, uint64_t seed, bool corrupt, Report& rep) {
   Rng rng{seed};
   const bool ternary = std::strcmp(c.kernel, "q2_0_gemv") == 0;
   const int64_t nb = c.n / kBlock;
@@ -197,6 +199,25 @@ int run_case(const Case& c, uint64_t seed, Report& rep) {
   if (int e = ternary ? q2_0_pack(d_blocks, c.rows, c.n, d_packed, nullptr)
                       : q1_0_pack(d_blocks, c.rows, c.n, d_packed, nullptr))
     return e;
+  if (corrupt && c.nvec == 1) {
+    int64_t r0 = c.rows / 2;
+    auto ref = [&](int64_t r) {
+      const uint8_t* row = &blocks[size_t(r * nb * bbytes)];
+      return ternary ? h_row_q2(row, nb, q.data(), d.data()) : h_row(row, nb, q.data(), d.data());
+    };
+    while (r0 + 1 < c.rows && ref(r0) == 0.0f) ++r0;
+    const Layout L = ternary ? layout_q2(c.rows, c.n) : layout_of(c.rows, c.n);
+    uint16_t* sc = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(d_packed) + L.bits_bytes);
+    for (int64_t b = 0; b < nb; ++b) {
+      uint16_t* at = sc + scale_index(r0 / kPanel, b, int(r0 % kPanel), L.nbp);
+      uint16_t h = 0;
+      if (int e = cuda_status(cudaMemcpy(&h, at, 2, cudaMemcpyDeviceToHost), "q1_0_verify corrupt")) return e;
+      if ((h & 0x7c00) != 0 && (h & 0x7c00) < 0x7800) h = uint16_t(h + 0x0400);  // x2, stays finite
+      if (int e = cuda_status(cudaMemcpy(at, &h, 2, cudaMemcpyHostToDevice), "q1_0_verify corrupt")) return e;
+    }
+    rep.add("%s %lldx%lld: scales of row %lld doubled after packing\n", c.kernel, (long long)c.rows,
+            (long long)c.n, (long long)r0);
+  }
   if (x.empty()) {
     if (int e = cuda_status(cudaMemcpy(d_q, q.data(), q.size(), cudaMemcpyHostToDevice), "q1_0_verify copy")) return e;
     if (int e = cuda_status(cudaMemcpy(d_d, d.data(), d.size() * 2, cudaMemcpyHostToDevice), "q1_0_verify copy")) return e;
@@ -267,7 +288,7 @@ extern "C" int q1_0_verify(int flags, char* report, size_t report_len) {
   const size_t nc = (flags & 1) ? sizeof quick / sizeof quick[0] : sizeof full / sizeof full[0];
   int status = Q1_OK;
   for (size_t i = 0; i < nc; ++i) {
-    int e = run_case(cs[i], 0x51ED5EEDull + 7919ull * i, rep);
+    int e = run_case(cs[i], 0x51ED5EEDull + 7919ull * i, (flags & 2) != 0, rep);
     if (e < 0) {
       rep.add("%s\n", q1_last_error());
       return e;

@@ -221,7 +221,11 @@ int q1_device_status(int clear);
  * checked the same way).  Runs synchronously on
  * the current device with its own allocations, against a host-side reference
  * compiled into the library.
- *   flags  : 0 = default shape set; 1 = quick (two small shapes).
+ *   flags  : 0 = default shape set; bit 0 (1) = quick set (three small shapes);
+ *            bit 1 (2) = negative control: in every one-vector case the
+ *            packed scales of one row (nonzero reference output, about the
+ *            middle row) are doubled after packing, so the check must report
+ *            that row as the first differing one and return Q1_MISMATCH.
  *   report : host buffer receiving one line per kernel and shape, or the first
  *            differing row ("row i differs ..."); may be NULL.
  * Returns Q1_OK if every output is bit-identical, Q1_MISMATCH (2) if any

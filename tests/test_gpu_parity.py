@@ -65,6 +65,19 @@ def test_library_self_check():
         assert any(line.startswith(kernel) for line in lines), (kernel, report)
 
 
+def test_library_self_check_negative_control():
+    """A corrupted packed buffer (one row's scales doubled after packing) must
+    fail the self-check, and the report must name that row as the first that
+    differs, case by case."""
+    import re
+    rc, report = binding.verify(quick=False, corrupt=True)
+    assert rc == binding.Q1_MISMATCH, report
+    corrupted = re.findall(r"^(\S+) (\d+)x(\d+): scales of row (\d+) doubled", report, re.M)
+    differs = re.findall(r"^(\S+) (\d+)x(\d+) nvec=1 \S+: row (\d+) differs", report, re.M)
+    assert len(corrupted) == 10 and corrupted == differs, report
+    assert "nvec=16" in report and "bit-exact" in report  # the batched cases are left intact
+
+
 # --------------------------------------------------------------- packing --
 @pytest.mark.parametrize("rows,n", [(1, 128), (31, 384), (33, 1024), (100, 1152), (257, 4096), (64, 14336)])
 def test_pack_unpack_round_trip(rows, n):
