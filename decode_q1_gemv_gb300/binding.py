@@ -327,11 +327,13 @@ def device_status(clear: bool = True) -> int:
     return v
 
 
-def verify(quick: bool = False, corrupt: bool = False) -> tuple[int, str]:
+def verify(quick: bool = False, corrupt: bool = False, wait_probe: bool = False) -> tuple[int, str]:
     """Run the on-card self-check; returns (status, report text).  corrupt=True
-    runs the negative control (one row's packed scales doubled per case)."""
+    runs the negative control (one row's packed scales doubled per case);
+    wait_probe=True first lets a bounded wait run out on purpose."""
     buf = ctypes.create_string_buffer(16384)
-    rc = load().q1_0_verify((1 if quick else 0) | (2 if corrupt else 0), buf, len(buf))
+    flags = (1 if quick else 0) | (2 if corrupt else 0) | (4 if wait_probe else 0)
+    rc = load().q1_0_verify(flags, buf, len(buf))
     return rc, buf.value.decode(errors="replace")
 
 

@@ -265,6 +265,42 @@ int run_case(const Case& c, uint64_t seed, bool corrupt, Report& rep) {
   return Q1_OK;
 }
 
+// The bounded wait every product kernel uses, on an mbarrier nothing will
+// complete: it must give up after about limit_ns and let the kernel return.
+__global__ void k_wait_probe(unsigned long long limit_ns, unsigned long long* result) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const uint64_t t0 = globaltimer();
+  const bool got = mbar_wait(smem_addr(&bar), 0u, limit_ns);  // phase 0 never completes
+  const uint64_t t1 = globaltimer();
+  if (threadIdx.x == 0) {
+    result[0] = got ? 1ull : 0ull;
+    result[1] = t1 - t0;
+  }
+}
+
+int run_wait_probe(Report& rep) {
+  Dev dev;
+  auto* d_res = static_cast<unsigned long long*>(dev.get(16));
+  if (!d_res) return fail(Q1_ERR_NOMEM, "q1_0_verify: device allocation failed");
+  const unsigned long long limit = 20000000ull;  // 20 ms
+  k_wait_probe<<<1, 32>>>(limit, d_res);
+  if (int e = cuda_status(cudaGetLastError(), "q1_0_verify wait probe")) return e;
+  unsigned long long res[2] = {0, 0};
+  if (int e = cuda_status(cudaMemcpy(res, d_res, 16, cudaMemcpyDeviceToHost), "q1_0_verify wait probe")) return e;
+  if (res[0] != 0 || res[1] < limit) {
+    rep.add("bounded wait: did not give up as it should (returned %llu after %.2f ms)\n", res[0], res[1] * 1e-6);
+    return Q1_MISMATCH;
+  }
+  rep.add("bounded wait on a barrier nothing completes: gave up after %.2f ms (limit %.0f ms)\n", res[1] * 1e-6,
+          limit * 1e-6);
+  return Q1_OK;
+}
+
 }  // namespace
 }  // namespace q1
 
@@ -284,6 +320,13 @@ extern "C" int q1_0_verify(int flags, char* report, size_t report_len) {
       {"q1_0_gemm_small", 200, 4096, 16, false}, {"q1_0_gemm_small", 64, 512, 64, true},
       {"q2_0_gemv", 64, 128, 1, true},    {"q2_0_gemv", 1000, 4096, 1, false}, {"q2_0_gemv", 33, 14336, 1, true},
   };
+  if (flags & 4) {  // the failure path first; the shape cases after it show the context still works
+    if (int e = run_wait_probe(rep)) {
+      if (e < 0) return e;
+      fail(Q1_MISMATCH, "q1_0_verify: the bounded-wait probe did not give up");
+      return e;
+    }
+  }
   const Case* cs = (flags & 1) ? quick : full;
   const size_t nc = (flags & 1) ? sizeof quick / sizeof quick[0] : sizeof full / sizeof full[0];
   int status = Q1_OK;

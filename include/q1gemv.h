@@ -225,7 +225,11 @@ int q1_device_status(int clear);
  *            bit 1 (2) = negative control: in every one-vector case the
  *            packed scales of one row (nonzero reference output, about the
  *            middle row) are doubled after packing, so the check must report
- *            that row as the first differing one and return Q1_MISMATCH.
+ *            that row as the first differing one and return Q1_MISMATCH;
+ *            bit 2 (4) = before the cases, run the library's bounded wait on an
+ *            mbarrier nothing completes (20 ms limit): it must give up and let
+ *            its kernel return, and the cases that follow show the device still
+ *            works (the failure path of every product kernel's waits).
  *   report : host buffer receiving one line per kernel and shape, or the first
  *            differing row ("row i differs ..."); may be NULL.
  * Returns Q1_OK if every output is bit-identical, Q1_MISMATCH (2) if any

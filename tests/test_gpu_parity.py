@@ -78,6 +78,16 @@ def test_library_self_check_negative_control():
     assert "nvec=16" in report and "bit-exact" in report  # the batched cases are left intact
 
 
+def test_bounded_wait_gives_up_and_device_stays_usable():
+    """The wait every product kernel uses, on a barrier nothing completes, gives
+    up after its limit; the status is read on the host, and the product cases
+    run right after it are bit-exact."""
+    rc, report = binding.verify(quick=True, wait_probe=True)
+    assert rc == binding.Q1_OK, report
+    assert "gave up after" in report and report.count("bit-exact") == 3, report
+    assert binding.device_status() == 0
+
+
 # --------------------------------------------------------------- packing --
 @pytest.mark.parametrize("rows,n", [(1, 128), (31, 384), (33, 1024), (100, 1152), (257, 4096), (64, 14336)])
 def test_pack_unpack_round_trip(rows, n):
