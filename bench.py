@@ -64,7 +64,8 @@ def kernel_source_hash() -> str:
     import re
     h = hashlib.sha256()
     for rel in ("decode_q1_gemv_gb300/csrc/multi.cu", "decode_q1_gemv_gb300/csrc/table.cuh",
-                "decode_q1_gemv_gb300/csrc/common.cuh", "decode_q1_gemv_gb300/csrc/q2.cuh"):
+                "decode_q1_gemv_gb300/csrc/common.cuh", "decode_q1_gemv_gb300/csrc/q2.cuh",
+                "decode_q1_gemv_gb300/csrc/formats.cuh"):
         with open(os.path.join(ROOT, rel)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)

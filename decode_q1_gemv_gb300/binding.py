@@ -32,7 +32,8 @@ Q1_MISMATCH = 2
 # Every symbol include/q1gemv.h declares (checked by the tests).
 EXPORTS = ("q1_last_error", "q1_0_packed_bytes", "q1_0_pack", "q1_0_unpack", "q8_quantize_act",
            "q1_0_gemv", "q1_0_gemv_multi", "q1_0_gemv_multi_plan", "q1_0_gemm_small", "q1_0_verify",
-           "q1_device_status", "q2_0_packed_bytes", "q2_0_pack", "q2_0_unpack", "q2_0_gemv", "q2_0_gemv_multi")
+           "q1_device_status", "q2_0_packed_bytes", "q2_0_pack", "q2_0_unpack", "q2_0_gemv", "q2_0_gemv_multi",
+           "q2_0_gemv_multi_plan")
 
 MAX_PRODUCTS = 256
 
@@ -47,7 +48,7 @@ class Product(ctypes.Structure):
 class MultiPlan(ctypes.Structure):
     """Mirror of q1_multi_plan (include/q1gemv.h)."""
     _fields_ = [("rows_per_thread", ctypes.c_int), ("grid", ctypes.c_int), ("total_cost", ctypes.c_int64),
-                ("max_range_cost", ctypes.c_int64)]
+                ("max_range_cost", ctypes.c_int64), ("panel_warps", ctypes.c_int)]
 
 
 class Q1Error(RuntimeError):
@@ -92,6 +93,8 @@ def load():
         lib.q1_0_gemv_multi_plan.argtypes = [ctypes.POINTER(Product), I, I, ctypes.POINTER(MultiPlan),
                                              ctypes.POINTER(I64), I]
         lib.q1_0_gemv_multi_plan.restype = I
+        lib.q2_0_gemv_multi_plan.argtypes = lib.q1_0_gemv_multi_plan.argtypes
+        lib.q2_0_gemv_multi_plan.restype = I
         lib.q2_0_packed_bytes.argtypes = [I64, I64]
         lib.q2_0_packed_bytes.restype = I64
         lib.q2_0_pack.argtypes = [P, I64, I64, P, P]
@@ -233,19 +236,23 @@ def gemv_multi(items=None, stream=None, array=None):
     _check(load().q1_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q1_0_gemv_multi")
 
 
-def multi_plan(shapes, sms: int = 0) -> dict:
-    """The work split q1_0_gemv_multi would make for products of the given
-    (rows, n) shapes, in list order, on `sms` SMs (0 = the current device).
-    Nothing is launched; needs no GPU when sms > 0."""
+def multi_plan(shapes, sms: int = 0, fmt: str = "q1") -> dict:
+    """The work split q1_0_gemv_multi (fmt "q1") or q2_0_gemv_multi ("q2")
+    would make for products of the given (rows, n) shapes, in list order, on
+    `sms` SMs (0 = the current device).  Nothing is launched; needs no GPU when
+    sms > 0."""
+    if fmt not in ("q1", "q2"):
+        raise ValueError("fmt must be 'q1' or 'q2'")
     arr = (Product * len(shapes))()
     for i, (rows, n) in enumerate(shapes):
         arr[i] = Product(None, int(rows), int(n), None, None, None, None)
     plan = MultiPlan()
     cuts = (ctypes.c_int64 * (2 * max(int(sms), 4096) + 1))()
-    _check(load().q1_0_gemv_multi_plan(arr, len(arr), int(sms), ctypes.byref(plan), cuts, len(cuts)),
-           "q1_0_gemv_multi_plan")
+    fn = load().q1_0_gemv_multi_plan if fmt == "q1" else load().q2_0_gemv_multi_plan
+    _check(fn(arr, len(arr), int(sms), ctypes.byref(plan), cuts, len(cuts)), f"{fmt}_0_gemv_multi_plan")
     return {"rows_per_thread": plan.rows_per_thread, "grid": plan.grid, "total_cost": plan.total_cost,
-            "max_range_cost": plan.max_range_cost, "cuts": list(cuts[:plan.grid + 1])}
+            "max_range_cost": plan.max_range_cost, "panel_warps": plan.panel_warps,
+            "cuts": list(cuts[:plan.grid + 1]) if plan.panel_warps == 0 else []}
 
 
 # ------------------------------------------------------- Q2_0 (ternary) --

@@ -1,0 +1,40 @@
+// formats.cuh -- the two weight formats as the matrix-vector kernels see
+// them.  Q1_0: one sign word per lane word (2 KB per panel and quad, layout in
+// common.cuh).  Q2_0: a P and an N word (4 KB), see q2.cuh.
+#pragma once
+
+#include "q2.cuh"
+
+namespace q1 {
+
+struct FmtQ1 {
+  static constexpr int kQuadBits = 2048;  // one panel x one quad of blocks: 32 rows x 4 blocks x 16 B
+  static constexpr bool kTwoPlanes = false;
+  static constexpr int kBigRows = 8;      // rows per thread of the streaming launches that fill every CTA
+  using Consts = ConstsQ1;
+  static __host__ __device__ __forceinline__ int64_t quad_bits_offset(int64_t p, int64_t qd, int64_t nbp) {
+    return q1::quad_bits_offset(p, qd, nbp);
+  }
+  static Layout layout(int64_t rows, int64_t n) { return layout_of(rows, n); }
+};
+struct FmtQ2 {
+  static constexpr int kQuadBits = kQ2QuadBits;
+  static constexpr bool kTwoPlanes = true;
+  static constexpr int kBigRows = 8;      // 168 registers, no spills; 4 rows x 2 slots measured 0.7 % slower
+  using Consts = ConstsQ2;
+  static __host__ __device__ __forceinline__ int64_t quad_bits_offset(int64_t p, int64_t qd, int64_t nbp) {
+    return q2_quad_bits_offset(p, qd, nbp);
+  }
+  static Layout layout(int64_t rows, int64_t n) { return layout_q2(rows, n); }
+};
+
+// panel.cu: the kernel for one product of few rows (one CTA per panel).
+// panel_warps: warps per CTA for the shape, 0 when the streaming kernel serves
+// it (n too long for the CTA's shared memory, or more panels than one wave of
+// CTAs).
+template <class F>
+int panel_warps(int64_t rows, int64_t n, int sms);
+template <class F>
+int launch_panel(const q1_product& pr, int warps, cudaStream_t s, const char* who);
+
+}  // namespace q1

@@ -30,7 +30,7 @@
 // reports through the device status word instead of hanging.
 #include <algorithm>
 
-#include "q2.cuh"
+#include "formats.cuh"
 
 namespace q1 {
 
@@ -49,28 +49,6 @@ template <int R>
 __host__ __device__ constexpr int multi_threads() { return consumers<R>() + 32; }
 constexpr int kQuadScales = 256;   // 32 rows x 4 blocks x 2 B
 
-// The two weight formats the kernel streams.  Q1_0: one sign word per lane
-// word (2 KB per panel and quad).  Q2_0: a P and an N word (4 KB), see q2.cuh.
-struct FmtQ1 {
-  static constexpr int kQuadBits = 2048;  // one panel x one quad of blocks: 32 rows x 4 blocks x 16 B
-  static constexpr bool kTwoPlanes = false;
-  static constexpr int kBigRows = 8;      // rows per thread of the launches that fill every CTA
-  using Consts = ConstsQ1;
-  static __host__ __device__ __forceinline__ int64_t quad_bits_offset(int64_t p, int64_t qd, int64_t nbp) {
-    return q1::quad_bits_offset(p, qd, nbp);
-  }
-  static Layout layout(int64_t rows, int64_t n) { return layout_of(rows, n); }
-};
-struct FmtQ2 {
-  static constexpr int kQuadBits = kQ2QuadBits;
-  static constexpr bool kTwoPlanes = true;
-  static constexpr int kBigRows = 8;      // 168 registers, no spills; 4 rows x 2 slots measured 0.7 % slower
-  using Consts = ConstsQ2;
-  static __host__ __device__ __forceinline__ int64_t quad_bits_offset(int64_t p, int64_t qd, int64_t nbp) {
-    return q2_quad_bits_offset(p, qd, nbp);
-  }
-  static Layout layout(int64_t rows, int64_t n) { return layout_q2(rows, n); }
-};
 constexpr int kConsumerBarrier = 1;
 constexpr int kMaxKc = 128;        // blocks of activation held in the table (n <= 16384 in one chunk)
 
@@ -465,13 +443,14 @@ static int launch_multi(const q1_product* prods, int count, cudaStream_t s, cons
 
 // The plan reported by q1_0_gemv_multi_plan: the CTA ranges exactly as the
 // kernel derives them from the arguments, and their tile costs.
-template <int R, int PMAX>
+template <int R, int PMAX, class F>
 static int report_plan(const q1_product* prods, int count, int sms, q1_multi_plan* out, int64_t* cuts,
                        int max_cuts) {
   MArgs<PMAX>* a = new MArgs<PMAX>;
   int grid = 0;
-  plan_multi<R, PMAX, FmtQ1>(prods, count, sms, *a, grid);
+  plan_multi<R, PMAX, F>(prods, count, sms, *a, grid);
   out->rows_per_thread = R;
+  out->panel_warps = 0;
   out->grid = grid;
   out->total_cost = a->total_cost;
   out->max_range_cost = 0;
@@ -514,13 +493,13 @@ static int dispatch(const q1_product* prods, int count, cudaStream_t s, const ch
   }
 }
 
-template <int PMAX>
+template <int PMAX, class F>
 static int dispatch_plan(const q1_product* prods, int count, int sms, q1_multi_plan* out, int64_t* cuts,
                          int max_cuts) {
-  switch (rows_per_thread<FmtQ1>(prods, count, sms)) {
-    case 8: return report_plan<8, PMAX>(prods, count, sms, out, cuts, max_cuts);
-    case 2: return report_plan<2, PMAX>(prods, count, sms, out, cuts, max_cuts);
-    default: return report_plan<1, PMAX>(prods, count, sms, out, cuts, max_cuts);
+  switch (rows_per_thread<F>(prods, count, sms)) {
+    case F::kBigRows: return report_plan<F::kBigRows, PMAX, F>(prods, count, sms, out, cuts, max_cuts);
+    case 2: return report_plan<2, PMAX, F>(prods, count, sms, out, cuts, max_cuts);
+    default: return report_plan<1, PMAX, F>(prods, count, sms, out, cuts, max_cuts);
   }
 }
 
@@ -549,7 +528,10 @@ int check_product(const char* who, int idx, const q1_product& pr) {
 
 template <class F>
 static int launch_products(const q1_product* prods, int count, cudaStream_t s, const char* who) {
-  if (count == 1) return dispatch<1, F>(prods, count, s, who);
+  if (count == 1) {
+    if (const int w = panel_warps<F>(prods[0].rows, prods[0].n, num_sms())) return launch_panel<F>(prods[0], w, s, who);
+    return dispatch<1, F>(prods, count, s, who);
+  }
   if (count <= 8) return dispatch<8, F>(prods, count, s, who);
   return dispatch<Q1_MAX_PRODUCTS, F>(prods, count, s, who);
 }
@@ -579,23 +561,44 @@ extern "C" int q1_0_gemv(const void* packed, int64_t rows, int64_t n, const int8
   return launch_products_dp4a(&p, 1, static_cast<cudaStream_t>(stream), "q1_0_gemv launch");
 }
 
-extern "C" int q1_0_gemv_multi_plan(const q1_product* products, int count, int sms, q1_multi_plan* plan,
-                                    int64_t* cuts, int max_cuts) {
+template <class F>
+static int multi_plan(const char* who, const q1_product* products, int count, int sms, q1_multi_plan* plan,
+                      int64_t* cuts, int max_cuts) {
   if (!products || !plan || count < 1 || count > Q1_MAX_PRODUCTS)
-    return fail(Q1_ERR_ARG, "q1_0_gemv_multi_plan: count=%d outside 1..%d (or null list/plan)", count,
-                Q1_MAX_PRODUCTS);
-  if (sms < 0 || sms > 4096) return fail(Q1_ERR_ARG, "q1_0_gemv_multi_plan: sms=%d outside 0..4096", sms);
+    return fail(Q1_ERR_ARG, "%s: count=%d outside 1..%d (or null list/plan)", who, count, Q1_MAX_PRODUCTS);
+  if (sms < 0 || sms > 4096) return fail(Q1_ERR_ARG, "%s: sms=%d outside 0..4096", who, sms);
   for (int j = 0; j < count; ++j) {
     const q1_product& pr = products[j];
     if (pr.rows < 1 || pr.rows > (int64_t(1) << 26) || pr.n < 128 || pr.n > (int64_t(1) << 24) || pr.n % 128)
-      return fail(Q1_ERR_ARG, "q1_0_gemv_multi_plan: product %d: bad shape rows=%lld n=%lld", j,
-                  (long long)pr.rows, (long long)pr.n);
+      return fail(Q1_ERR_ARG, "%s: product %d: bad shape rows=%lld n=%lld", who, j, (long long)pr.rows,
+                  (long long)pr.n);
   }
-  if (cuts && max_cuts < 0) return fail(Q1_ERR_ARG, "q1_0_gemv_multi_plan: max_cuts=%d < 0", max_cuts);
+  if (cuts && max_cuts < 0) return fail(Q1_ERR_ARG, "%s: max_cuts=%d < 0", who, max_cuts);
   const int n_sms = sms > 0 ? sms : num_sms();
-  if (count == 1) return dispatch_plan<1>(products, count, n_sms, plan, cuts, max_cuts);
-  if (count <= 8) return dispatch_plan<8>(products, count, n_sms, plan, cuts, max_cuts);
-  return dispatch_plan<Q1_MAX_PRODUCTS>(products, count, n_sms, plan, cuts, max_cuts);
+  if (count == 1) {
+    if (const int w = panel_warps<F>(products[0].rows, products[0].n, n_sms)) {
+      const Layout L = F::layout(products[0].rows, products[0].n);
+      plan->rows_per_thread = 4;
+      plan->grid = int(L.panels);
+      plan->total_cost = 0;
+      plan->max_range_cost = 0;
+      plan->panel_warps = w;
+      return Q1_OK;
+    }
+    return dispatch_plan<1, F>(products, count, n_sms, plan, cuts, max_cuts);
+  }
+  if (count <= 8) return dispatch_plan<8, F>(products, count, n_sms, plan, cuts, max_cuts);
+  return dispatch_plan<Q1_MAX_PRODUCTS, F>(products, count, n_sms, plan, cuts, max_cuts);
+}
+
+extern "C" int q1_0_gemv_multi_plan(const q1_product* products, int count, int sms, q1_multi_plan* plan,
+                                    int64_t* cuts, int max_cuts) {
+  return multi_plan<FmtQ1>("q1_0_gemv_multi_plan", products, count, sms, plan, cuts, max_cuts);
+}
+
+extern "C" int q2_0_gemv_multi_plan(const q1_product* products, int count, int sms, q1_multi_plan* plan,
+                                    int64_t* cuts, int max_cuts) {
+  return multi_plan<FmtQ2>("q2_0_gemv_multi_plan", products, count, sms, plan, cuts, max_cuts);
 }
 
 extern "C" int q1_0_gemv_multi(const q1_product* products, int count, void* stream) {

@@ -1,0 +1,281 @@
+// panel.cu -- the matrix-vector product for one product of few rows: one CTA
+// per 32-row panel, the panel's block quads shared out among its warps, which
+// work on them at the same time.
+//
+// Row product (bankML "docs/modules/gpu.md", "kernels.rs -- the Q1_0
+// kernels", first and second bullets): per lane, ab_b = d1*s summed over the
+// four sub-blocks of block b, then acc = fma(d0_b, ab_b, acc) over the blocks
+// in increasing order, then the fixed horizontal sum of the eight lanes.  Only
+// the outer chain is sequential; ab_b depends on block b alone.
+//
+// The streaming kernel gives a tile of rows to one CTA, which walks all of n
+// in sequence.  A product of a few thousand rows has fewer tiles than the GPU
+// has SMs, and the few warps of each busy CTA mostly wait on their own
+// dependences.  Here warp k of a panel's CTA takes a contiguous range of the
+// quads: it loads their sign words and scales straight from global memory
+// (issued before griddepcontrol.wait, as weights do not depend on the
+// preceding kernel), builds the activation table entries of its own blocks
+// (no CTA-wide barrier), forms ab_b for its blocks with the streaming kernel's
+// quad step at four rows a thread (rows lane/4 + 8j, word lane%4), and leaves
+// ab_b and d0_b in shared memory.  After one barrier the first four warps run
+// the outer chain over all blocks in order and the horizontal sum: the same
+// operations in the same order as the streaming kernel, so the same bits.
+//
+// Shared memory per CTA: the activation table of the whole row, ab as
+// [block][row][word] float pairs (lanes w, w + 4) and d0 as [block][row]:
+// 1472 bytes per block, so n up to 156 * 128 = 19968.  There are no waits on
+// other CTAs or on asynchronous copies.
+#include "formats.cuh"
+
+namespace q1 {
+
+namespace {
+
+constexpr int kPanelBytesPerBlock = 4 * (4 * 16 + 16) + 128 * 8 + 32 * 4;  // table + ab + d0
+constexpr int kPanelMaxNbp = 156;
+constexpr int kPanelSmemPerSm = 233472;  // shared memory of an SM
+constexpr int kPanelSmemPerCta = 1024;   // reserved by the system per resident CTA
+
+struct PanelArgs {
+  const uint8_t* packed;
+  const float* x;        // f32 activation, or null
+  const int8_t* q;       // q8_0 quants (when x is null)
+  const uint16_t* d;     // q8_0 scales (when x is null)
+  float* out;
+  int64_t bits_bytes;
+  int rows, nb, nbp;
+};
+
+__host__ __device__ constexpr int panel_smem_bytes(int nbp) { return nbp * kPanelBytesPerBlock; }
+
+// fp16 scale w (0..3) of a quad held as 4 halves in a uint2.
+__device__ __forceinline__ float quad_scale_at(const uint2& v, int w) {
+  const uint32_t h = (w < 2) ? v.x : v.y;
+  return __half2float(__ushort_as_half(uint16_t((w & 1) ? (h >> 16) : (h & 0xffffu))));
+}
+
+// Block BQ of a quad for four rows and word w: ab for lanes w (abE) and
+// w + 4 (abO) of each row, stored to the CTA's ab array at [block][row][w].
+template <class F, int BQ>
+__device__ __forceinline__ void block_ab(const uint4 (&wv)[4], const uint4 (&nv)[4], const uint4* QCq,
+                                         const float4* DKq, int w, int r0, float2* abq) {
+  float abE[4], abO[4];
+  if constexpr (F::kTwoPlanes) {
+    q2_quad_subblock<4, BQ, 0>(wv, nv, QCq, DKq, w, abE, abO);
+    q2_quad_subblock<4, BQ, 1>(wv, nv, QCq, DKq, w, abE, abO);
+    q2_quad_subblock<4, BQ, 2>(wv, nv, QCq, DKq, w, abE, abO);
+    q2_quad_subblock<4, BQ, 3>(wv, nv, QCq, DKq, w, abE, abO);
+  } else {
+    quad_subblock<4, BQ, 0>(wv, QCq, DKq, w, abE, abO);
+    quad_subblock<4, BQ, 1>(wv, QCq, DKq, w, abE, abO);
+    quad_subblock<4, BQ, 2>(wv, QCq, DKq, w, abE, abO);
+    quad_subblock<4, BQ, 3>(wv, QCq, DKq, w, abE, abO);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) abq[(BQ * 32 + r0 + 8 * j) * 4 + w] = make_float2(abE[j], abO[j]);
+}
+
+// A quad for rows r0 + 8j (j < 4) and word w: ab of its four blocks, and the
+// scale of block w of each row to the d0 array at [block][row].
+template <class F>
+__device__ __forceinline__ void quad_ab(const uint4 (&wv)[4], const uint4 (&nv)[4], const uint2 (&sc)[4],
+                                        const uint4* QCq, const float4* DKq, int w, int r0, float2* abq,
+                                        float* d0q) {
+  block_ab<F, 0>(wv, nv, QCq, DKq, w, r0, abq);
+  block_ab<F, 1>(wv, nv, QCq, DKq, w, r0, abq);
+  block_ab<F, 2>(wv, nv, QCq, DKq, w, r0, abq);
+  block_ab<F, 3>(wv, nv, QCq, DKq, w, r0, abq);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d0q[w * 32 + r0 + 8 * j] = quad_scale_at(sc[j], w);
+}
+
+// Registers a thread may use (the prefetched words of PF quads dominate), and
+// the CTAs of W warps an SM then holds by registers.
+template <class F>
+__host__ __device__ constexpr int panel_regs() { return F::kTwoPlanes ? 128 : 80; }
+template <class F>
+__host__ __device__ constexpr int panel_ctas_by_regs(int W) {
+  return 65536 / (panel_regs<F>() * 32 * W) > 0 ? 65536 / (panel_regs<F>() * 32 * W) : 1;
+}
+
+// W warps; warp k takes the contiguous quads [k m, k m + m) of the panel
+// (m = ceil(quads / W)), four rows a thread, keeps the words of PF quads in
+// flight, and builds the activation table entries of its own blocks.
+template <class F, int W, int PF>
+__global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(const __grid_constant__ PanelArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int nbp = a.nbp, nq = nbp / 4;
+  unsigned char* table = smem;
+  float2* ab = reinterpret_cast<float2*>(smem + table_bytes(nbp));  // [block][row][word]
+  float* d0s = reinterpret_cast<float*>(ab + nbp * 128);            // [block][row]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = lane >> 2, w = lane & 3;  // rows r0 + 8j of the panel, word w
+  const int64_t p = blockIdx.x;
+  const uint8_t* bits = a.packed;
+  const uint8_t* scales = a.packed + a.bits_bytes;
+  const int m = (nq + W - 1) / W;
+  const int q0 = warp * m < nq ? warp * m : nq;
+  const int mine = q0 + m < nq ? m : nq - q0;  // quads [q0, q0 + mine) of this warp
+
+  // Sign words are loaded ahead; the block scales, needed only when a quad's
+  // products are stored, are loaded as its step starts.
+  uint4 wv[PF][4], nv[PF][4];
+  auto load = [&](int i0) {
+#pragma unroll
+    for (int u = 0; u < PF; ++u) {
+      if (i0 + u < mine) {
+        const int qd = q0 + i0 + u;
+        const uint4* rec = reinterpret_cast<const uint4*>(bits + F::quad_bits_offset(p, qd, nbp));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          wv[u][j] = __ldg(rec + (r0 + 8 * j) * 4 + w);
+          if constexpr (F::kTwoPlanes) nv[u][j] = __ldg(rec + 128 + (r0 + 8 * j) * 4 + w);
+        }
+      }
+    }
+  };
+  load(0);
+
+  pdl_wait();  // the activation may be written by the preceding kernel
+  if (mine > 0) {  // this warp's own table entries: blocks 4 q0 .. 4 (q0 + mine) - 1
+    // Inlined, so that the sign-word loads above stay in flight meanwhile.
+    if (a.x) table_x_body<4, typename F::Consts>(a.x, a.nb, 4 * q0, 4 * mine, table, lane, 32, nbp, 4 * q0);
+    else table_q_body<4, typename F::Consts>(a.q, a.d, a.nb, 4 * q0, 4 * mine, table, lane, 32, nbp, 4 * q0);
+  }
+  __syncwarp();
+
+  const uint4* QC = reinterpret_cast<const uint4*>(table);
+  const float4* DK = reinterpret_cast<const float4*>(table + table_dk_offset(nbp));
+  for (int i0 = 0; i0 < mine; i0 += PF) {
+    if (i0 > 0) load(i0);
+#pragma unroll
+    for (int u = 0; u < PF; ++u) {
+      if (i0 + u < mine) {
+        const int qd = q0 + i0 + u;
+        const uint2* srec = reinterpret_cast<const uint2*>(scales + quad_scales_offset(p, qd, nbp));
+        uint2 sc[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[j] = __ldg(srec + r0 + 8 * j);
+        quad_ab<F>(wv[u], nv[u], sc, QC + qd * 64, DK + qd * 16, w, r0, ab + qd * 4 * 128, d0s + qd * 4 * 32);
+      }
+    }
+  }
+  pdl_launch_dependents();
+  __syncthreads();
+
+  if (tid < 128) {  // outer chain over all blocks in order: row, lanes w and w + 4
+    const int row = tid >> 2;
+    float accE = 0.0f, accO = 0.0f;
+    const float2* abr = ab + row * 4 + w;
+    const float* d0r = d0s + row;
+    // Four blocks at a time, the next four loaded while these are chained.
+    float2 v[4];
+    float dd[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k] = abr[k * 128];
+      dd[k] = d0r[k * 32];
+    }
+    for (int b0 = 0; b0 < nbp; b0 += 4) {
+      float2 vn[4];
+      float dn[4];
+      const int bn = b0 + 4 < nbp ? b0 + 4 : b0;  // the last round reloads its own blocks
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        vn[k] = abr[(bn + k) * 128];
+        dn[k] = d0r[(bn + k) * 32];
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        accE = __fmaf_rn(dd[k], v[k].x, accE);
+        accO = __fmaf_rn(dd[k], v[k].y, accO);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[k] = vn[k];
+        dd[k] = dn[k];
+      }
+    }
+    const float sum = row_sum(accE, accO);
+    const int64_t r = p * kPanel + row;
+    if (w == 0 && r < a.rows) a.out[r] = sum;
+  }
+}
+
+template <class F, int W>
+int launch_panel_w(const q1_product& pr, cudaStream_t s, const char* who) {
+  constexpr int PF = 2;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_done[dev]) {
+    if (int e = cuda_status(cudaFuncSetAttribute(k_q1_panel<F, W, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 panel_smem_bytes(kPanelMaxNbp)),
+                            "cudaFuncSetAttribute"))
+      return e;
+    attr_done[dev] = true;
+  }
+  const Layout L = F::layout(pr.rows, pr.n);
+  PanelArgs a;
+  a.packed = static_cast<const uint8_t*>(pr.packed);
+  a.x = pr.x;
+  a.q = pr.q;
+  a.d = pr.d;
+  a.out = pr.out;
+  a.bits_bytes = L.bits_bytes;
+  a.rows = int(pr.rows);
+  a.nb = int(L.nb);
+  a.nbp = int(L.nbp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(L.panels));
+  cfg.blockDim = dim3(unsigned(32 * W));
+  cfg.dynamicSmemBytes = size_t(panel_smem_bytes(a.nbp));
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_panel<F, W, PF>, a), who);
+}
+
+// Warps per CTA for the shape, or 0: the most warps (16, 8, 4; at most the
+// quads rounded up) whose grid of one CTA per panel is still one wave.
+template <class F>
+int panel_warps_for(int64_t rows, int64_t n, int sms) {
+  const Layout L = layout_of(rows, n);
+  if (L.nbp > kPanelMaxNbp) return 0;
+  const int nq = int(L.nbp / 4);
+  const int by_smem = kPanelSmemPerSm / (panel_smem_bytes(int(L.nbp)) + kPanelSmemPerCta);
+  for (int W = nq > 8 ? 16 : nq > 4 ? 8 : 4; W >= 4; W >>= 1) {
+    const int by_threads = 2048 / (32 * W);
+    int per_sm = panel_ctas_by_regs<F>(W);
+    per_sm = per_sm < by_threads ? per_sm : by_threads;
+    per_sm = per_sm < by_smem ? per_sm : by_smem;
+    if (L.panels <= int64_t(per_sm) * sms) return W;
+  }
+  return 0;
+}
+
+}  // namespace
+
+template <class F>
+int panel_warps(int64_t rows, int64_t n, int sms) {
+  return panel_warps_for<F>(rows, n, sms);
+}
+template int panel_warps<FmtQ1>(int64_t, int64_t, int);
+template int panel_warps<FmtQ2>(int64_t, int64_t, int);
+
+template <class F>
+int launch_panel(const q1_product& pr, int warps, cudaStream_t s, const char* who) {
+  switch (warps) {
+    case 16: return launch_panel_w<F, 16>(pr, s, who);
+    case 8: return launch_panel_w<F, 8>(pr, s, who);
+    case 4: return launch_panel_w<F, 4>(pr, s, who);
+    default: return fail(Q1_ERR_ARG, "%s: %d warps per panel", who, warps);
+  }
+}
+template int launch_panel<FmtQ1>(const q1_product&, int, cudaStream_t, const char*);
+template int launch_panel<FmtQ2>(const q1_product&, int, cudaStream_t, const char*);
+
+}  // namespace q1

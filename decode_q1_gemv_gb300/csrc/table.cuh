@@ -61,17 +61,21 @@ struct ConstsQ1 {
 };
 
 // Table for blocks [blk0, blk0 + kcb) from a quantized activation (q int8 [n],
-// d fp16 [n/32]).  Sub-blocks past the activation's end get zero constants.
+// d fp16 [n/32]), written at table positions tpos0 .. tpos0 + kcb - 1 of a
+// table of kc blocks.  Sub-blocks past the activation's end get zero constants.
 // Both builders issue the global loads of kTableBatch rounds (a round: one
 // entry per thread) before using any of them, so their latencies overlap; a
 // larger batch holds more registers across the call, and the caller picks the
 // largest that its kernel affords without spilling.
-template <int kTableBatch, class C = ConstsQ1>
-static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, const uint16_t* __restrict__ d1,
-                                              int nb, int blk0, int kcb, unsigned char* table, int tid,
-                                              int nthreads, int kc) {
-  uint4* QC = reinterpret_cast<uint4*>(table);
-  float4* DK = reinterpret_cast<float4*>(table + table_dk_offset(kc));
+// table_q_body is the builder itself, for kernels that inline it (loads the
+// caller has in flight then stay in flight); build_table_q is the same as an
+// out-of-line call.
+template <int kTableBatch, class C>
+__device__ __forceinline__ void table_q_body(const int8_t* __restrict__ q, const uint16_t* __restrict__ d1, int nb,
+                                             int blk0, int kcb, unsigned char* table, int tid, int nthreads, int kc,
+                                             int tpos0) {
+  uint4* QC = reinterpret_cast<uint4*>(table) + tpos0 * 16;
+  float4* DK = reinterpret_cast<float4*>(table + table_dk_offset(kc)) + tpos0 * 4;
   const int nsub = nb * 4;
   for (int base = 0; base < kcb * 16; base += kTableBatch * nthreads) {
     uint32_t wb[kTableBatch][2];
@@ -118,16 +122,25 @@ static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, 
   }
 }
 
-// Table for blocks [blk0, blk0 + kcb) from an f32 activation x [n], quantizing
+template <int kTableBatch, class C = ConstsQ1>
+static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, const uint16_t* __restrict__ d1,
+                                              int nb, int blk0, int kcb, unsigned char* table, int tid,
+                                              int nthreads, int kc) {
+  table_q_body<kTableBatch, C>(q, d1, nb, blk0, kcb, table, tid, nthreads, kc, 0);
+}
+
+// Table for blocks [blk0, blk0 + kcb) (at table positions from tpos0, as
+// above) from an f32 activation x [n], quantizing
 // it on the way exactly as q8_quantize_act does (per 32 values: amax, d =
 // amax/127, id = d ? 1/d : 0, q = roundf(x*id), scale fp16(d)).  One thread per
 // (sub-block, lane); the 8 threads of a sub-block are consecutive in a warp.
 // nthreads must be a multiple of 32 and every thread of the group must call.
-template <int kTableBatch, class C = ConstsQ1>
-static __device__ __noinline__ void build_table_x(const float* __restrict__ x, int nb, int blk0, int kcb,
-                                              unsigned char* table, int tid, int nthreads, int kc) {
-  uint32_t* QCw = reinterpret_cast<uint32_t*>(table);
-  float* DKf = reinterpret_cast<float*>(table + table_dk_offset(kc));
+// table_x_body inlined, build_table_x out of line, as for the quantized form.
+template <int kTableBatch, class C>
+__device__ __forceinline__ void table_x_body(const float* __restrict__ x, int nb, int blk0, int kcb,
+                                             unsigned char* table, int tid, int nthreads, int kc, int tpos0) {
+  uint32_t* QCw = reinterpret_cast<uint32_t*>(table) + tpos0 * 64;
+  float* DKf = reinterpret_cast<float*>(table + table_dk_offset(kc)) + tpos0 * 16;
   const int nsub = nb * 4;
   const int total = kcb * 4 * 8;
   for (int base = 0; base < total; base += kTableBatch * nthreads) {  // same trip count for every thread
@@ -172,6 +185,12 @@ static __device__ __noinline__ void build_table_x(const float* __restrict__ x, i
       }
     }
   }
+}
+
+template <int kTableBatch, class C = ConstsQ1>
+static __device__ __noinline__ void build_table_x(const float* __restrict__ x, int nb, int blk0, int kcb,
+                                              unsigned char* table, int tid, int nthreads, int kc) {
+  table_x_body<kTableBatch, C>(x, nb, blk0, kcb, table, tid, nthreads, kc, 0);
 }
 
 template <int I>

@@ -153,6 +153,11 @@ typedef struct q1_multi_plan {
   int grid;               /* CTAs launched                                          */
   int64_t total_cost;     /* sum over products of tiles x padded blocks per row     */
   int64_t max_range_cost; /* largest tile cost owned by one CTA                     */
+  int panel_warps;        /* 0: the streaming kernel above.  Else the call is a
+                             single product of few rows, run as one CTA per
+                             32-row panel whose panel_warps warps share out its
+                             block quads (grid = panels, rows_per_thread = 4,
+                             both costs 0, no cuts) */
 } q1_multi_plan;
 
 int q1_0_gemv_multi_plan(const q1_product *products, int count, int sms, q1_multi_plan *plan, int64_t *cuts,
@@ -206,6 +211,12 @@ int q2_0_gemv(const void *packed, int64_t rows, int64_t n, const int8_t *q, cons
 /* Several independent Q2_0 products in one launch: as q1_0_gemv_multi, each
  * descriptor's `packed` from q2_0_pack(rows, n). */
 int q2_0_gemv_multi(const q1_product *products, int count, void *stream);
+
+/* The work split of a q2_0_gemv_multi launch: as q1_0_gemv_multi_plan.  The
+ * kernel choice for a single product can differ from Q1_0's (the Q2_0 panel
+ * kernel keeps more registers a thread, so fewer of its CTAs fit an SM). */
+int q2_0_gemv_multi_plan(const q1_product *products, int count, int sms, q1_multi_plan *plan, int64_t *cuts,
+                         int max_cuts);
 
 /* Device status word of the library's kernels on the current device.  A
  * kernel whose bounded internal wait gives up (it never should: every wait is

@@ -1,0 +1,149 @@
+"""The one-product panel kernel (one CTA per 32-row panel, its warps sharing
+out the panel's block quads) against the CPU oracle and against the streaming
+kernel, through the C ABI.
+
+A single product of few rows goes to the panel kernel; the same product
+launched together with a second one goes to the streaming kernel.  Both must
+give the oracle's bits: every output of the two launches is compared with the
+other, and with the oracle in full for small shapes and on sampled rows (first
+and last included) for the Llama-3-8B shapes.  The shapes cover every warp
+count (16, 8, 4), fewer quads than warps, warps with two quads and with more
+than two, ragged rows, and the longest row the kernel takes (156 blocks).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_q1_gemv_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+    oracle.build()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def bits_equal(got, want):
+    got = np.asarray(got, dtype=np.float32)
+    want = np.asarray(want, dtype=np.float32)
+    assert got.shape == want.shape
+    diff = np.nonzero(got.view(np.uint32) != want.view(np.uint32))[0]
+    assert diff.size == 0, (f"{diff.size} of {got.size} outputs differ; first at {diff[:5]}: "
+                            f"got {got.ravel()[diff[:5]]} want {want.ravel()[diff[:5]]}")
+
+
+# (rows, n, Q1_0 warps per CTA on a 152-SM GB300); the test also requires
+# that the launcher on the device it runs on picks the panel kernel.
+SHAPES = [(1, 128, 4), (33, 384, 4), (256, 1024, 4), (3000, 2048, 4), (1000, 640, 4), (1024, 4096, 8),
+          (4096, 4096, 8), (14336, 4096, 8), (18000, 4096, 4), (8192, 8192, 8), (4096, 14336, 16),
+          (300, 19968, 16)]
+FULL_ORACLE_ROWS = 4096
+
+
+def _sample(rows, rng):
+    if rows <= FULL_ORACLE_ROWS:
+        return np.arange(rows)
+    return np.unique(np.concatenate([[0, rows - 1], rng.choice(rows, 1500, replace=False)]))
+
+
+def _run(fmt, packed, rows, n, x, q, d):
+    """(panel-kernel output, streaming-kernel output) of one product."""
+    alone = torch.full((rows,), float("nan"), device="cuda")
+    paired = torch.full((rows,), float("nan"), device="cuda")
+    dummy_rows, dummy_n = 32, 128
+    if fmt == "q1":
+        dummy = binding.pack(dev(synth.weight_blocks(synth.rng_for(999), dummy_rows, dummy_n)), dummy_rows, dummy_n)
+        multi = binding.gemv_multi
+    else:
+        dummy = binding.q2_pack(dev(synth.ternary_blocks(synth.rng_for(999), dummy_rows, dummy_n)), dummy_rows,
+                                dummy_n)
+        multi = binding.q2_gemv_multi
+    dx = torch.zeros(dummy_n, device="cuda")
+    dout = torch.empty(dummy_rows, device="cuda")
+    multi([(packed, rows, n, x, q, d, alone)])
+    multi([(packed, rows, n, x, q, d, paired), (dummy, dummy_rows, dummy_n, dx, None, None, dout)])
+    torch.cuda.synchronize()
+    return alone.cpu().numpy(), paired.cpu().numpy()
+
+
+@pytest.mark.parametrize("rows,n,warps", SHAPES)
+@pytest.mark.parametrize("act", ["f32", "q8"])
+def test_panel_q1_equals_streaming_and_oracle(rows, n, warps, act):
+    assert binding.multi_plan([(rows, n)], sms=152)["panel_warps"] == warps
+    assert binding.multi_plan([(rows, n)])["panel_warps"] > 0, "this device's launcher takes the streaming kernel"
+    rng = synth.rng_for(501, rows, n, len(act))
+    blocks = synth.weight_blocks(rng, rows, n, "lognormal" if rows % 2 else "halfnormal")
+    packed = binding.pack(dev(blocks), rows, n)
+    if act == "f32":
+        xh = synth.activations(rng, 1, n, outliers=0.01)
+        q, d = oracle.q8_quantize(xh)
+        args = (dev(xh[0]), None, None)
+    else:
+        q, d = synth.raw_quants(rng, 1, n, scale="lognormal", m128_frac=0.03)
+        args = (None, dev(q[0]), dev(d[0].view(np.int16)))
+    alone, paired = _run("q1", packed, rows, n, *args)
+    bits_equal(alone, paired)
+    idx = _sample(rows, rng)
+    want = oracle.gemv(blocks, q[0], d[0]) if rows <= FULL_ORACLE_ROWS else oracle.rows_sampled(blocks, idx, q[0], d[0])
+    bits_equal(alone[idx], want)
+
+
+@pytest.mark.parametrize("rows,n,warps", [s for s in SHAPES if s[0] * s[1] <= 4096 * 14336])
+def test_panel_q2_equals_streaming_and_oracle(rows, n, warps):
+    """Q2_0 keeps up to 128 registers a thread, so its warp counts can be
+    lower than Q1_0's; every shape here stays within its one-wave limit."""
+    assert binding.multi_plan([(rows, n)], fmt="q2")["panel_warps"] > 0
+    rng = synth.rng_for(502, rows, n)
+    if rows * n > 4096 * 4096:
+        tb = synth.ternary_blocks_fast(rng, rows, n)
+    else:
+        tb = synth.ternary_blocks(rng, rows, n, "lognormal")
+    packed = binding.q2_pack(dev(tb), rows, n)
+    xh = synth.activations(rng, 1, n, outliers=0.01)
+    q, d = oracle.q8_quantize(xh)
+    alone, paired = _run("q2", packed, rows, n, dev(xh[0]), None, None)
+    bits_equal(alone, paired)
+    idx = _sample(rows, rng)
+    want = (oracle.q2_gemv(tb, q[0], d[0]) if rows <= FULL_ORACLE_ROWS
+            else oracle.q2_rows_sampled(tb, idx, q[0], d[0]))
+    bits_equal(alone[idx], want)
+
+
+def test_panel_in_graph_with_dependent_launches():
+    """Back-to-back panel launches in a CUDA graph, each reading the previous
+    one's output as its activation (programmatic dependent launch), against
+    the oracle run of the same chain."""
+    rows = n = 4096
+    rng = synth.rng_for(503)
+    blocks = [synth.weight_blocks(rng, rows, n, "halfnormal") for _ in range(3)]
+    packed = [binding.pack(dev(b), rows, n) for b in blocks]
+    x0 = synth.activations(rng, 1, n)[0]
+    bufs = [dev(x0)] + [torch.empty(rows, device="cuda") for _ in range(3)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(3):
+            binding.gemv_multi([(packed[i], rows, n, bufs[i], None, None, bufs[i + 1])], stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    for b in bufs[1:]:
+        b.fill_(float("nan"))
+    with torch.cuda.graph(g):
+        for i in range(3):
+            binding.gemv_multi([(packed[i], rows, n, bufs[i], None, None, bufs[i + 1])])
+    g.replay()
+    torch.cuda.synchronize()
+    x = x0
+    for i in range(3):
+        q, d = oracle.q8_quantize(x[None, :])
+        want = oracle.gemv(blocks[i], q[0], d[0])
+        bits_equal(bufs[i + 1].cpu().numpy(), want)
+        x = want
