@@ -29,12 +29,16 @@ struct FmtQ2 {
 };
 
 // panel.cu: the kernel for one product of few rows (one CTA per panel).
-// panel_warps: warps per CTA for the shape, 0 when the streaming kernel serves
-// it (n too long for the CTA's shared memory, or more panels than one wave of
-// CTAs).
+// panel_config: its shape for a product (warps per CTA, blocks per work
+// unit), {0, 0} when the streaming kernel serves it (n too long for the CTA's
+// shared memory, or more panels than one wave of CTAs).
+struct PanelConfig {
+  int warps = 0;  // W: 16, 8 or 4
+  int unit = 0;   // blocks per work unit: 4 (a quad) or 2 (half a quad)
+};
 template <class F>
-int panel_warps(int64_t rows, int64_t n, int sms);
+PanelConfig panel_config(int64_t rows, int64_t n, int sms);
 template <class F>
-int launch_panel(const q1_product& pr, int warps, cudaStream_t s, const char* who);
+int launch_panel(const q1_product& pr, PanelConfig c, cudaStream_t s, const char* who);
 
 }  // namespace q1

@@ -451,6 +451,7 @@ static int report_plan(const q1_product* prods, int count, int sms, q1_multi_pla
   plan_multi<R, PMAX, F>(prods, count, sms, *a, grid);
   out->rows_per_thread = R;
   out->panel_warps = 0;
+  out->panel_unit_blocks = 0;
   out->grid = grid;
   out->total_cost = a->total_cost;
   out->max_range_cost = 0;
@@ -529,7 +530,8 @@ int check_product(const char* who, int idx, const q1_product& pr) {
 template <class F>
 static int launch_products(const q1_product* prods, int count, cudaStream_t s, const char* who) {
   if (count == 1) {
-    if (const int w = panel_warps<F>(prods[0].rows, prods[0].n, num_sms())) return launch_panel<F>(prods[0], w, s, who);
+    const PanelConfig c = panel_config<F>(prods[0].rows, prods[0].n, num_sms());
+    if (c.warps) return launch_panel<F>(prods[0], c, s, who);
     return dispatch<1, F>(prods, count, s, who);
   }
   if (count <= 8) return dispatch<8, F>(prods, count, s, who);
@@ -576,13 +578,15 @@ static int multi_plan(const char* who, const q1_product* products, int count, in
   if (cuts && max_cuts < 0) return fail(Q1_ERR_ARG, "%s: max_cuts=%d < 0", who, max_cuts);
   const int n_sms = sms > 0 ? sms : num_sms();
   if (count == 1) {
-    if (const int w = panel_warps<F>(products[0].rows, products[0].n, n_sms)) {
+    const PanelConfig c = panel_config<F>(products[0].rows, products[0].n, n_sms);
+    if (c.warps) {
       const Layout L = F::layout(products[0].rows, products[0].n);
       plan->rows_per_thread = 4;
       plan->grid = int(L.panels);
       plan->total_cost = 0;
       plan->max_range_cost = 0;
-      plan->panel_warps = w;
+      plan->panel_warps = c.warps;
+      plan->panel_unit_blocks = c.unit;
       return Q1_OK;
     }
     return dispatch_plan<1, F>(products, count, n_sms, plan, cuts, max_cuts);

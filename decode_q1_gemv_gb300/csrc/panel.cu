@@ -75,21 +75,28 @@ __device__ __forceinline__ void block_ab(const uint4 (&wv)[4], const uint4 (&nv)
   for (int j = 0; j < 4; ++j) abq[(BQ * 32 + r0 + 8 * j) * 4 + w] = make_float2(abE[j], abO[j]);
 }
 
-// A quad for rows r0 + 8j (j < 4) and word w: ab of its four blocks, and the
-// scale of block w of each row to the d0 array at [block][row].
-template <class F>
-__device__ __forceinline__ void quad_ab(const uint4 (&wv)[4], const uint4 (&nv)[4], const uint2 (&sc)[4],
+// A unit of UB blocks (a quad, UB = 4, or half a quad, UB = 2) for rows
+// r0 + 8j (j < 4) and word w: ab of its blocks, and the scale of block w of
+// each row to the d0 array at [block][row] (threads w < UB).  wv/nv hold the
+// unit's words in their first UB components, sc its scales in its first UB
+// halves.
+template <class F, int UB>
+__device__ __forceinline__ void unit_ab(const uint4 (&wv)[4], const uint4 (&nv)[4], const uint2 (&sc)[4],
                                         const uint4* QCq, const float4* DKq, int w, int r0, float2* abq,
                                         float* d0q) {
   block_ab<F, 0>(wv, nv, QCq, DKq, w, r0, abq);
   block_ab<F, 1>(wv, nv, QCq, DKq, w, r0, abq);
-  block_ab<F, 2>(wv, nv, QCq, DKq, w, r0, abq);
-  block_ab<F, 3>(wv, nv, QCq, DKq, w, r0, abq);
+  if constexpr (UB == 4) {
+    block_ab<F, 2>(wv, nv, QCq, DKq, w, r0, abq);
+    block_ab<F, 3>(wv, nv, QCq, DKq, w, r0, abq);
+  }
+  if (w < UB) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) d0q[w * 32 + r0 + 8 * j] = quad_scale_at(sc[j], w);
+    for (int j = 0; j < 4; ++j) d0q[w * 32 + r0 + 8 * j] = quad_scale_at(sc[j], w);
+  }
 }
 
-// Registers a thread may use (the prefetched words of PF quads dominate), and
+// Registers a thread may use (the prefetched words of PF units dominate), and
 // the CTAs of W warps an SM then holds by registers.
 template <class F>
 __host__ __device__ constexpr int panel_regs() { return F::kTwoPlanes ? 128 : 80; }
@@ -98,13 +105,15 @@ __host__ __device__ constexpr int panel_ctas_by_regs(int W) {
   return 65536 / (panel_regs<F>() * 32 * W) > 0 ? 65536 / (panel_regs<F>() * 32 * W) : 1;
 }
 
-// W warps; warp k takes the contiguous quads [k m, k m + m) of the panel
-// (m = ceil(quads / W)), four rows a thread, keeps the words of PF quads in
-// flight, and builds the activation table entries of its own blocks.
-template <class F, int W, int PF>
+// W warps; the panel's blocks form units of UB blocks (UB = 4: quads; UB = 2:
+// half quads, for rows of few quads, so that more warps get work).  Warp k
+// takes the contiguous units [k m, k m + m) (m = ceil(units / W)), four rows a
+// thread, keeps the words of PF units in flight, and builds the activation
+// table entries of its own blocks.
+template <class F, int W, int PF, int UB>
 __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(const __grid_constant__ PanelArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int nbp = a.nbp, nq = nbp / 4;
+  const int nbp = a.nbp, nu = nbp / UB;
   unsigned char* table = smem;
   float2* ab = reinterpret_cast<float2*>(smem + table_bytes(nbp));  // [block][row][word]
   float* d0s = reinterpret_cast<float*>(ab + nbp * 128);            // [block][row]
@@ -113,23 +122,34 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
   const int64_t p = blockIdx.x;
   const uint8_t* bits = a.packed;
   const uint8_t* scales = a.packed + a.bits_bytes;
-  const int m = (nq + W - 1) / W;
-  const int q0 = warp * m < nq ? warp * m : nq;
-  const int mine = q0 + m < nq ? m : nq - q0;  // quads [q0, q0 + mine) of this warp
+  const int m = (nu + W - 1) / W;
+  const int u0 = warp * m < nu ? warp * m : nu;
+  const int mine = u0 + m < nu ? m : nu - u0;  // units [u0, u0 + mine) of this warp
 
-  // Sign words are loaded ahead; the block scales, needed only when a quad's
-  // products are stored, are loaded as its step starts.
+  // Sign words are loaded ahead; the block scales, needed only when a unit's
+  // products are stored, are loaded as its step starts.  Unit u is quad
+  // u UB / 4, blocks (u UB) % 4 .. + UB - 1 of it.
   uint4 wv[PF][4], nv[PF][4];
   auto load = [&](int i0) {
 #pragma unroll
-    for (int u = 0; u < PF; ++u) {
-      if (i0 + u < mine) {
-        const int qd = q0 + i0 + u;
-        const uint4* rec = reinterpret_cast<const uint4*>(bits + F::quad_bits_offset(p, qd, nbp));
+    for (int v = 0; v < PF; ++v) {
+      if (i0 + v < mine) {
+        const int u = u0 + i0 + v, qd = u * UB / 4, h = (u * UB) % 4 / 2;
+        const uint8_t* rec = bits + F::quad_bits_offset(p, qd, nbp);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          wv[u][j] = __ldg(rec + (r0 + 8 * j) * 4 + w);
-          if constexpr (F::kTwoPlanes) nv[u][j] = __ldg(rec + 128 + (r0 + 8 * j) * 4 + w);
+          const int word = (r0 + 8 * j) * 4 + w;
+          if constexpr (UB == 4) {
+            wv[v][j] = __ldg(reinterpret_cast<const uint4*>(rec) + word);
+            if constexpr (F::kTwoPlanes) nv[v][j] = __ldg(reinterpret_cast<const uint4*>(rec + 2048) + word);
+          } else {
+            const uint2 x2 = __ldg(reinterpret_cast<const uint2*>(rec) + word * 2 + h);
+            wv[v][j] = make_uint4(x2.x, x2.y, 0u, 0u);
+            if constexpr (F::kTwoPlanes) {
+              const uint2 n2 = __ldg(reinterpret_cast<const uint2*>(rec + 2048) + word * 2 + h);
+              nv[v][j] = make_uint4(n2.x, n2.y, 0u, 0u);
+            }
+          }
         }
       }
     }
@@ -137,10 +157,10 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
   load(0);
 
   pdl_wait();  // the activation may be written by the preceding kernel
-  if (mine > 0) {  // this warp's own table entries: blocks 4 q0 .. 4 (q0 + mine) - 1
+  if (mine > 0) {  // this warp's own table entries: blocks UB u0 .. UB (u0 + mine) - 1
     // Inlined, so that the sign-word loads above stay in flight meanwhile.
-    if (a.x) table_x_body<4, typename F::Consts>(a.x, a.nb, 4 * q0, 4 * mine, table, lane, 32, nbp, 4 * q0);
-    else table_q_body<4, typename F::Consts>(a.q, a.d, a.nb, 4 * q0, 4 * mine, table, lane, 32, nbp, 4 * q0);
+    if (a.x) table_x_body<4, typename F::Consts>(a.x, a.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
+    else table_q_body<4, typename F::Consts>(a.q, a.d, a.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
   }
   __syncwarp();
 
@@ -149,14 +169,17 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
   for (int i0 = 0; i0 < mine; i0 += PF) {
     if (i0 > 0) load(i0);
 #pragma unroll
-    for (int u = 0; u < PF; ++u) {
-      if (i0 + u < mine) {
-        const int qd = q0 + i0 + u;
+    for (int v = 0; v < PF; ++v) {
+      if (i0 + v < mine) {
+        const int u = u0 + i0 + v, qd = u * UB / 4, h = (u * UB) % 4 / 2, b0 = u * UB;
         const uint2* srec = reinterpret_cast<const uint2*>(scales + quad_scales_offset(p, qd, nbp));
         uint2 sc[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sc[j] = __ldg(srec + r0 + 8 * j);
-        quad_ab<F>(wv[u], nv[u], sc, QC + qd * 64, DK + qd * 16, w, r0, ab + qd * 4 * 128, d0s + qd * 4 * 32);
+        for (int j = 0; j < 4; ++j) {
+          if constexpr (UB == 4) sc[j] = __ldg(srec + r0 + 8 * j);
+          else sc[j] = make_uint2(__ldg(reinterpret_cast<const uint32_t*>(srec + r0 + 8 * j) + h), 0u);
+        }
+        unit_ab<F, UB>(wv[v], nv[v], sc, QC + b0 * 16, DK + b0 * 4, w, r0, ab + b0 * 128, d0s + b0 * 32);
       }
     }
   }
@@ -202,14 +225,14 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
   }
 }
 
-template <class F, int W>
+template <class F, int W, int UB>
 int launch_panel_w(const q1_product& pr, cudaStream_t s, const char* who) {
   constexpr int PF = 2;
   static bool attr_done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (!attr_done[dev]) {
-    if (int e = cuda_status(cudaFuncSetAttribute(k_q1_panel<F, W, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (int e = cuda_status(cudaFuncSetAttribute(k_q1_panel<F, W, PF, UB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  panel_smem_bytes(kPanelMaxNbp)),
                             "cudaFuncSetAttribute"))
       return e;
@@ -236,46 +259,59 @@ int launch_panel_w(const q1_product& pr, cudaStream_t s, const char* who) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_panel<F, W, PF>, a), who);
+  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_panel<F, W, PF, UB>, a), who);
 }
 
-// Warps per CTA for the shape, or 0: the most warps (16, 8, 4; at most the
-// quads rounded up) whose grid of one CTA per panel is still one wave.
+// The kernel's shape for a product, or {0, 0}: the most warps W (16, 8, 4;
+// starting from the quads rounded up) whose grid of one CTA per panel is one
+// wave; then half-quad units (UB = 2), and twice the warps where that still
+// fits, when they lower the work of the busiest warp.
 template <class F>
-int panel_warps_for(int64_t rows, int64_t n, int sms) {
+PanelConfig panel_config_for(int64_t rows, int64_t n, int sms) {
   const Layout L = layout_of(rows, n);
-  if (L.nbp > kPanelMaxNbp) return 0;
-  const int nq = int(L.nbp / 4);
-  const int by_smem = kPanelSmemPerSm / (panel_smem_bytes(int(L.nbp)) + kPanelSmemPerCta);
-  for (int W = nq > 8 ? 16 : nq > 4 ? 8 : 4; W >= 4; W >>= 1) {
+  if (L.nbp > kPanelMaxNbp) return {};
+  const int nbp = int(L.nbp), nq = nbp / 4;
+  const int by_smem = kPanelSmemPerSm / (panel_smem_bytes(nbp) + kPanelSmemPerCta);
+  auto fits = [&](int W) {
     const int by_threads = 2048 / (32 * W);
     int per_sm = panel_ctas_by_regs<F>(W);
     per_sm = per_sm < by_threads ? per_sm : by_threads;
     per_sm = per_sm < by_smem ? per_sm : by_smem;
-    if (L.panels <= int64_t(per_sm) * sms) return W;
-  }
-  return 0;
+    return L.panels <= int64_t(per_sm) * sms;
+  };
+  auto busiest = [&](int W, int UB) { return (nbp / UB + W - 1) / W * (UB / 2); };  // half quads
+  int W = 0;
+  for (int Wc = nq > 8 ? 16 : nq > 4 ? 8 : 4; Wc >= 4 && !W; Wc >>= 1)
+    if (fits(Wc)) W = Wc;
+  if (!W) return {};
+  PanelConfig c{W, 4};
+  if (busiest(W, 2) < busiest(W, 4)) c.unit = 2;
+  if (2 * W <= 16 && fits(2 * W) && busiest(2 * W, 2) < busiest(c.warps, c.unit)) c = PanelConfig{2 * W, 2};
+  return c;
 }
 
 }  // namespace
 
 template <class F>
-int panel_warps(int64_t rows, int64_t n, int sms) {
-  return panel_warps_for<F>(rows, n, sms);
+PanelConfig panel_config(int64_t rows, int64_t n, int sms) {
+  return panel_config_for<F>(rows, n, sms);
 }
-template int panel_warps<FmtQ1>(int64_t, int64_t, int);
-template int panel_warps<FmtQ2>(int64_t, int64_t, int);
+template PanelConfig panel_config<FmtQ1>(int64_t, int64_t, int);
+template PanelConfig panel_config<FmtQ2>(int64_t, int64_t, int);
 
 template <class F>
-int launch_panel(const q1_product& pr, int warps, cudaStream_t s, const char* who) {
-  switch (warps) {
-    case 16: return launch_panel_w<F, 16>(pr, s, who);
-    case 8: return launch_panel_w<F, 8>(pr, s, who);
-    case 4: return launch_panel_w<F, 4>(pr, s, who);
-    default: return fail(Q1_ERR_ARG, "%s: %d warps per panel", who, warps);
+int launch_panel(const q1_product& pr, PanelConfig c, cudaStream_t s, const char* who) {
+  switch (c.warps * 10 + c.unit) {
+    case 164: return launch_panel_w<F, 16, 4>(pr, s, who);
+    case 162: return launch_panel_w<F, 16, 2>(pr, s, who);
+    case 84: return launch_panel_w<F, 8, 4>(pr, s, who);
+    case 82: return launch_panel_w<F, 8, 2>(pr, s, who);
+    case 44: return launch_panel_w<F, 4, 4>(pr, s, who);
+    case 42: return launch_panel_w<F, 4, 2>(pr, s, who);
+    default: return fail(Q1_ERR_ARG, "%s: %d warps x %d-block units per panel", who, c.warps, c.unit);
   }
 }
-template int launch_panel<FmtQ1>(const q1_product&, int, cudaStream_t, const char*);
-template int launch_panel<FmtQ2>(const q1_product&, int, cudaStream_t, const char*);
+template int launch_panel<FmtQ1>(const q1_product&, PanelConfig, cudaStream_t, const char*);
+template int launch_panel<FmtQ2>(const q1_product&, PanelConfig, cudaStream_t, const char*);
 
 }  // namespace q1

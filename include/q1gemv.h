@@ -156,8 +156,9 @@ typedef struct q1_multi_plan {
   int panel_warps;        /* 0: the streaming kernel above.  Else the call is a
                              single product of few rows, run as one CTA per
                              32-row panel whose panel_warps warps share out its
-                             block quads (grid = panels, rows_per_thread = 4,
-                             both costs 0, no cuts) */
+                             blocks in units of panel_unit_blocks (grid =
+                             panels, rows_per_thread = 4, both costs 0, no cuts) */
+  int panel_unit_blocks;  /* 4 (quads) or 2 (half quads); 0 with the streaming kernel */
 } q1_multi_plan;
 
 int q1_0_gemv_multi_plan(const q1_product *products, int count, int sms, q1_multi_plan *plan, int64_t *cuts,

@@ -210,44 +210,60 @@ def test_multi_plan_matches_exhaustive_optimum(lib, seed):
     assert plan3["max_range_cost"] == _best_max_range(tiles3, ctas)
 
 
-@pytest.mark.parametrize("rows,n,warps", [
-    (4096, 4096, 8), (1024, 4096, 8), (4096, 14336, 16), (14336, 4096, 8), (256, 1024, 4), (1, 128, 4),
-    (8192, 8192, 8), (18000, 4096, 4), (4096, 19968, 16), (5000, 19968, 0), (4096, 20096, 0),
-    (128256, 4096, 0), (40000, 256, 0)])
-def test_multi_plan_one_product_kernel(lib, rows, n, warps):
-    """A single product of few rows goes to the one-CTA-per-panel kernel:
-    W = 16, 8 or 4 warps (the fewest of those that cover the quads, then fewer
-    while the grid of one CTA per panel is more than one wave), n at most 156
-    blocks.  Residency per SM: 80 registers a thread, 2048 threads, 228 KB of
-    shared memory at 1472 bytes per block plus 1 KB per CTA."""
-    plan = binding.multi_plan([(rows, n)], sms=152)
-    assert plan["panel_warps"] == warps
+def _panel_per_sm(warps, nbp, regs):
+    return min(65536 // (regs * 32 * warps), 2048 // (32 * warps), 233472 // (nbp * 1472 + 1024))
+
+
+def _busiest(nbp, warps, unit):
+    """Half quads of work of the busiest warp."""
+    return -(-(nbp // unit) // warps) * (unit // 2)
+
+
+def _check_panel_choice(plan, rows, n, regs):
+    warps, unit = plan["panel_warps"], plan["panel_unit_blocks"]
     panels = -(-rows // 256) * 8
     nbp = -(-(n // 128) // 4) * 4
+    assert plan["grid"] == panels and plan["rows_per_thread"] == 4 and plan["cuts"] == []
+    assert panels <= _panel_per_sm(warps, nbp, regs) * 152 and nbp <= 156
+    # no other (warps, unit) that fits one wave gives the busiest warp less work
+    # with at most 16 warps and no more warps than needed
+    for w2 in (4, 8, 16):
+        for u2 in (4, 2):
+            if panels <= _panel_per_sm(w2, nbp, regs) * 152 and w2 <= max(4, 2 * nbp // 4):
+                assert _busiest(nbp, warps, unit) <= _busiest(nbp, w2, u2)
+
+
+@pytest.mark.parametrize("rows,n,warps,unit", [
+    (4096, 4096, 16, 2), (1024, 4096, 16, 2), (4096, 14336, 16, 4), (14336, 4096, 8, 4), (256, 1024, 4, 2),
+    (1, 128, 4, 2), (300, 384, 4, 2), (300, 1536, 8, 2), (8192, 8192, 8, 4), (18000, 4096, 4, 4),
+    (4096, 19968, 16, 2), (5000, 19968, 0, 0), (4096, 20096, 0, 0), (128256, 4096, 0, 0), (40000, 256, 0, 0)])
+def test_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
+    """A single product of few rows goes to the one-CTA-per-panel kernel:
+    W = 16, 8 or 4 warps sharing out the panel's blocks in quads or half
+    quads, the grid of one CTA per panel one wave (80 registers a thread,
+    2048 threads, 228 KB of shared memory at 1472 bytes per block plus 1 KB
+    per CTA), n at most 156 blocks, and the busiest warp as lightly loaded as
+    those limits allow."""
+    plan = binding.multi_plan([(rows, n)], sms=152)
+    assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
     if warps:
-        assert plan["grid"] == panels and plan["rows_per_thread"] == 4 and plan["cuts"] == []
-        per_sm = min(65536 // (80 * 32 * warps), 2048 // (32 * warps), 233472 // (nbp * 1472 + 1024))
-        assert panels <= per_sm * 152 and nbp <= 156
-        assert warps == 4 or nbp // 4 > warps // 2
+        _check_panel_choice(plan, rows, n, 80 if warps < 16 else 128)
     else:
         assert plan["grid"] > 0 and len(plan["cuts"]) == plan["grid"] + 1
     # two products always take the streaming kernel
     assert binding.multi_plan([(rows, n), (32, 128)], sms=152)["panel_warps"] == 0
 
 
-@pytest.mark.parametrize("rows,n,warps", [
-    (4096, 4096, 8), (1024, 4096, 8), (4096, 14336, 16), (14336, 4096, 4), (1, 128, 4), (8192, 8192, 8),
-    (18000, 4096, 4), (20000, 4096, 0), (4096, 20096, 0)])
-def test_q2_multi_plan_one_product_kernel(lib, rows, n, warps):
+@pytest.mark.parametrize("rows,n,warps,unit", [
+    (4096, 4096, 16, 2), (1024, 4096, 16, 2), (4096, 14336, 16, 4), (14336, 4096, 4, 4), (1, 128, 4, 2),
+    (8192, 8192, 8, 4), (18000, 4096, 4, 4), (20000, 4096, 0, 0), (4096, 20096, 0, 0)])
+def test_q2_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
     """The Q2_0 panel kernel keeps up to 128 registers a thread: 4 CTAs of
     4 warps, 2 of 8 or 1 of 16 an SM by registers."""
     plan = binding.multi_plan([(rows, n)], sms=152, fmt="q2")
-    assert plan["panel_warps"] == warps
+    assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
     if warps:
-        panels = -(-rows // 256) * 8
-        nbp = -(-(n // 128) // 4) * 4
-        per_sm = min(65536 // (128 * 32 * warps), 233472 // (nbp * 1472 + 1024))
-        assert plan["grid"] == panels <= per_sm * 152
+        _check_panel_choice(plan, rows, n, 128)
     q1 = binding.multi_plan([(rows, n), (32, 128)], sms=152)
     q2 = binding.multi_plan([(rows, n), (32, 128)], sms=152, fmt="q2")
     assert q2 == q1  # the streaming split depends on the shapes only

@@ -7,8 +7,9 @@ launched together with a second one goes to the streaming kernel.  Both must
 give the oracle's bits: every output of the two launches is compared with the
 other, and with the oracle in full for small shapes and on sampled rows (first
 and last included) for the Llama-3-8B shapes.  The shapes cover every warp
-count (16, 8, 4), fewer quads than warps, warps with two quads and with more
-than two, ragged rows, and the longest row the kernel takes (156 blocks).
+count (16, 8, 4) with quad and half-quad work units, fewer units than warps,
+warps with several units, ragged rows, and the longest row the kernel takes
+(156 blocks).
 """
 import numpy as np
 import pytest
@@ -41,11 +42,12 @@ def bits_equal(got, want):
                             f"got {got.ravel()[diff[:5]]} want {want.ravel()[diff[:5]]}")
 
 
-# (rows, n, Q1_0 warps per CTA on a 152-SM GB300); the test also requires
-# that the launcher on the device it runs on picks the panel kernel.
-SHAPES = [(1, 128, 4), (33, 384, 4), (256, 1024, 4), (3000, 2048, 4), (1000, 640, 4), (1024, 4096, 8),
-          (4096, 4096, 8), (14336, 4096, 8), (18000, 4096, 4), (8192, 8192, 8), (4096, 14336, 16),
-          (300, 19968, 16)]
+# (rows, n, Q1_0 warps per CTA and blocks per work unit on a 152-SM GB300);
+# the test also requires that the launcher on the device it runs on picks the
+# panel kernel.
+SHAPES = [(1, 128, 4, 2), (33, 384, 4, 2), (256, 1024, 4, 2), (300, 1536, 8, 2), (3000, 2048, 8, 2),
+          (1000, 640, 4, 2), (1024, 4096, 16, 2), (4096, 4096, 16, 2), (14336, 4096, 8, 4),
+          (18000, 4096, 4, 4), (8192, 8192, 8, 4), (4096, 14336, 16, 4), (300, 19968, 16, 2)]
 FULL_ORACLE_ROWS = 4096
 
 
@@ -75,10 +77,11 @@ def _run(fmt, packed, rows, n, x, q, d):
     return alone.cpu().numpy(), paired.cpu().numpy()
 
 
-@pytest.mark.parametrize("rows,n,warps", SHAPES)
+@pytest.mark.parametrize("rows,n,warps,unit", SHAPES)
 @pytest.mark.parametrize("act", ["f32", "q8"])
-def test_panel_q1_equals_streaming_and_oracle(rows, n, warps, act):
-    assert binding.multi_plan([(rows, n)], sms=152)["panel_warps"] == warps
+def test_panel_q1_equals_streaming_and_oracle(rows, n, warps, unit, act):
+    plan = binding.multi_plan([(rows, n)], sms=152)
+    assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
     assert binding.multi_plan([(rows, n)])["panel_warps"] > 0, "this device's launcher takes the streaming kernel"
     rng = synth.rng_for(501, rows, n, len(act))
     blocks = synth.weight_blocks(rng, rows, n, "lognormal" if rows % 2 else "halfnormal")
@@ -97,8 +100,8 @@ def test_panel_q1_equals_streaming_and_oracle(rows, n, warps, act):
     bits_equal(alone[idx], want)
 
 
-@pytest.mark.parametrize("rows,n,warps", [s for s in SHAPES if s[0] * s[1] <= 4096 * 14336])
-def test_panel_q2_equals_streaming_and_oracle(rows, n, warps):
+@pytest.mark.parametrize("rows,n,warps,unit", [s for s in SHAPES if s[0] * s[1] <= 4096 * 14336])
+def test_panel_q2_equals_streaming_and_oracle(rows, n, warps, unit):
     """Q2_0 keeps up to 128 registers a thread, so its warp counts can be
     lower than Q1_0's; every shape here stays within its one-wave limit."""
     assert binding.multi_plan([(rows, n)], fmt="q2")["panel_warps"] > 0
