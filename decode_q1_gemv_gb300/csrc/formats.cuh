@@ -28,17 +28,18 @@ struct FmtQ2 {
   static Layout layout(int64_t rows, int64_t n) { return layout_q2(rows, n); }
 };
 
-// panel.cu: the kernel for one product of few rows (one CTA per panel).
-// panel_config: its shape for a product (warps per CTA, blocks per work
-// unit), {0, 0} when the streaming kernel serves it (n too long for the CTA's
-// shared memory, or more panels than one wave of CTAs).
+// panel.cu: the kernel for launches of few rows in total (one CTA per panel
+// of each of up to 8 products).  panel_config: its shape for a product list
+// (warps per CTA, blocks per work unit), {0, 0} when the streaming kernel
+// serves it (more than 8 products, a row too long for the CTA's shared
+// memory, or more panels than one wave of CTAs).
 struct PanelConfig {
   int warps = 0;  // W: 16, 8 or 4
   int unit = 0;   // blocks per work unit: 4 (a quad) or 2 (half a quad)
 };
 template <class F>
-PanelConfig panel_config(int64_t rows, int64_t n, int sms);
+PanelConfig panel_config(const q1_product* prods, int count, int sms);
 template <class F>
-int launch_panel(const q1_product& pr, PanelConfig c, cudaStream_t s, const char* who);
+int launch_panel(const q1_product* prods, int count, PanelConfig c, cudaStream_t s, const char* who);
 
 }  // namespace q1

@@ -529,11 +529,9 @@ int check_product(const char* who, int idx, const q1_product& pr) {
 
 template <class F>
 static int launch_products(const q1_product* prods, int count, cudaStream_t s, const char* who) {
-  if (count == 1) {
-    const PanelConfig c = panel_config<F>(prods[0].rows, prods[0].n, num_sms());
-    if (c.warps) return launch_panel<F>(prods[0], c, s, who);
-    return dispatch<1, F>(prods, count, s, who);
-  }
+  const PanelConfig c = panel_config<F>(prods, count, num_sms());
+  if (c.warps) return launch_panel<F>(prods, count, c, s, who);
+  if (count == 1) return dispatch<1, F>(prods, count, s, who);
   if (count <= 8) return dispatch<8, F>(prods, count, s, who);
   return dispatch<Q1_MAX_PRODUCTS, F>(prods, count, s, who);
 }
@@ -577,20 +575,19 @@ static int multi_plan(const char* who, const q1_product* products, int count, in
   }
   if (cuts && max_cuts < 0) return fail(Q1_ERR_ARG, "%s: max_cuts=%d < 0", who, max_cuts);
   const int n_sms = sms > 0 ? sms : num_sms();
-  if (count == 1) {
-    const PanelConfig c = panel_config<F>(products[0].rows, products[0].n, n_sms);
-    if (c.warps) {
-      const Layout L = F::layout(products[0].rows, products[0].n);
-      plan->rows_per_thread = 4;
-      plan->grid = int(L.panels);
-      plan->total_cost = 0;
-      plan->max_range_cost = 0;
-      plan->panel_warps = c.warps;
-      plan->panel_unit_blocks = c.unit;
-      return Q1_OK;
-    }
-    return dispatch_plan<1, F>(products, count, n_sms, plan, cuts, max_cuts);
+  const PanelConfig c = panel_config<F>(products, count, n_sms);
+  if (c.warps) {
+    int64_t panels = 0;
+    for (int j = 0; j < count; ++j) panels += F::layout(products[j].rows, products[j].n).panels;
+    plan->rows_per_thread = 4;
+    plan->grid = int(panels);
+    plan->total_cost = 0;
+    plan->max_range_cost = 0;
+    plan->panel_warps = c.warps;
+    plan->panel_unit_blocks = c.unit;
+    return Q1_OK;
   }
+  if (count == 1) return dispatch_plan<1, F>(products, count, n_sms, plan, cuts, max_cuts);
   if (count <= 8) return dispatch_plan<8, F>(products, count, n_sms, plan, cuts, max_cuts);
   return dispatch_plan<Q1_MAX_PRODUCTS, F>(products, count, n_sms, plan, cuts, max_cuts);
 }

@@ -36,7 +36,9 @@ constexpr int kPanelMaxNbp = 156;
 constexpr int kPanelSmemPerSm = 233472;  // shared memory of an SM
 constexpr int kPanelSmemPerCta = 1024;   // reserved by the system per resident CTA
 
-struct PanelArgs {
+constexpr int kPanelMaxProducts = 8;
+
+struct PanelProd {
   const uint8_t* packed;
   const float* x;        // f32 activation, or null
   const int8_t* q;       // q8_0 quants (when x is null)
@@ -44,6 +46,11 @@ struct PanelArgs {
   float* out;
   int64_t bits_bytes;
   int rows, nb, nbp;
+  int panel_begin;       // first CTA of this product
+};
+struct PanelArgs {
+  PanelProd p[kPanelMaxProducts];
+  int count;
 };
 
 __host__ __device__ constexpr int panel_smem_bytes(int nbp) { return nbp * kPanelBytesPerBlock; }
@@ -113,15 +120,18 @@ __host__ __device__ constexpr int panel_ctas_by_regs(int W) {
 template <class F, int W, int PF, int UB>
 __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(const __grid_constant__ PanelArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int nbp = a.nbp, nu = nbp / UB;
+  int j = 0;  // this CTA's product: panels are numbered across the products in list order
+  while (j + 1 < a.count && int(blockIdx.x) >= a.p[j + 1].panel_begin) ++j;
+  const PanelProd& pr = a.p[j];
+  const int nbp = pr.nbp, nu = nbp / UB;
   unsigned char* table = smem;
   float2* ab = reinterpret_cast<float2*>(smem + table_bytes(nbp));  // [block][row][word]
   float* d0s = reinterpret_cast<float*>(ab + nbp * 128);            // [block][row]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r0 = lane >> 2, w = lane & 3;  // rows r0 + 8j of the panel, word w
-  const int64_t p = blockIdx.x;
-  const uint8_t* bits = a.packed;
-  const uint8_t* scales = a.packed + a.bits_bytes;
+  const int64_t p = int(blockIdx.x) - pr.panel_begin;  // panel within the product
+  const uint8_t* bits = pr.packed;
+  const uint8_t* scales = pr.packed + pr.bits_bytes;
   const int m = (nu + W - 1) / W;
   const int u0 = warp * m < nu ? warp * m : nu;
   const int mine = u0 + m < nu ? m : nu - u0;  // units [u0, u0 + mine) of this warp
@@ -159,8 +169,8 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
   pdl_wait();  // the activation may be written by the preceding kernel
   if (mine > 0) {  // this warp's own table entries: blocks UB u0 .. UB (u0 + mine) - 1
     // Inlined, so that the sign-word loads above stay in flight meanwhile.
-    if (a.x) table_x_body<4, typename F::Consts>(a.x, a.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
-    else table_q_body<4, typename F::Consts>(a.q, a.d, a.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
+    if (pr.x) table_x_body<4, typename F::Consts>(pr.x, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
+    else table_q_body<4, typename F::Consts>(pr.q, pr.d, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
   }
   __syncwarp();
 
@@ -221,12 +231,12 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
     }
     const float sum = row_sum(accE, accO);
     const int64_t r = p * kPanel + row;
-    if (w == 0 && r < a.rows) a.out[r] = sum;
+    if (w == 0 && r < pr.rows) pr.out[r] = sum;
   }
 }
 
 template <class F, int W, int UB>
-int launch_panel_w(const q1_product& pr, cudaStream_t s, const char* who) {
+int launch_panel_w(const q1_product* prods, int count, cudaStream_t s, const char* who) {
   constexpr int PF = 2;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -238,21 +248,30 @@ int launch_panel_w(const q1_product& pr, cudaStream_t s, const char* who) {
       return e;
     attr_done[dev] = true;
   }
-  const Layout L = F::layout(pr.rows, pr.n);
-  PanelArgs a;
-  a.packed = static_cast<const uint8_t*>(pr.packed);
-  a.x = pr.x;
-  a.q = pr.q;
-  a.d = pr.d;
-  a.out = pr.out;
-  a.bits_bytes = L.bits_bytes;
-  a.rows = int(pr.rows);
-  a.nb = int(L.nb);
-  a.nbp = int(L.nbp);
+  PanelArgs a = {};
+  a.count = count;
+  int panels = 0, nbp_max = 0;
+  for (int j = 0; j < count; ++j) {
+    const q1_product& pr = prods[j];
+    const Layout L = F::layout(pr.rows, pr.n);
+    PanelProd& d = a.p[j];
+    d.packed = static_cast<const uint8_t*>(pr.packed);
+    d.x = pr.x;
+    d.q = pr.q;
+    d.d = pr.d;
+    d.out = pr.out;
+    d.bits_bytes = L.bits_bytes;
+    d.rows = int(pr.rows);
+    d.nb = int(L.nb);
+    d.nbp = int(L.nbp);
+    d.panel_begin = panels;
+    panels += int(L.panels);
+    nbp_max = nbp_max > d.nbp ? nbp_max : d.nbp;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(L.panels));
+  cfg.gridDim = dim3(unsigned(panels));
   cfg.blockDim = dim3(unsigned(32 * W));
-  cfg.dynamicSmemBytes = size_t(panel_smem_bytes(a.nbp));
+  cfg.dynamicSmemBytes = size_t(panel_smem_bytes(nbp_max));
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -262,22 +281,30 @@ int launch_panel_w(const q1_product& pr, cudaStream_t s, const char* who) {
   return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_panel<F, W, PF, UB>, a), who);
 }
 
-// The kernel's shape for a product, or {0, 0}: the most warps W (16, 8, 4;
-// starting from the quads rounded up) whose grid of one CTA per panel is one
-// wave; then half-quad units (UB = 2), and twice the warps where that still
-// fits, when they lower the work of the busiest warp.
+// The kernel's shape for a list of products, or {0, 0}: the most warps W
+// (16, 8, 4; starting from the longest row's quads rounded up) whose grid of
+// one CTA per panel of every product is one wave; then half-quad units, and
+// twice the warps where that still fits, when they lower the work of the
+// busiest warp.
 template <class F>
-PanelConfig panel_config_for(int64_t rows, int64_t n, int sms) {
-  const Layout L = layout_of(rows, n);
-  if (L.nbp > kPanelMaxNbp) return {};
-  const int nbp = int(L.nbp), nq = nbp / 4;
+PanelConfig panel_config_for(const q1_product* prods, int count, int sms) {
+  if (count < 1 || count > kPanelMaxProducts) return {};
+  int64_t panels = 0;
+  int nbp = 0;
+  for (int j = 0; j < count; ++j) {
+    const Layout L = layout_of(prods[j].rows, prods[j].n);
+    panels += L.panels;
+    nbp = nbp > int(L.nbp) ? nbp : int(L.nbp);
+  }
+  if (nbp > kPanelMaxNbp) return {};
+  const int nq = nbp / 4;
   const int by_smem = kPanelSmemPerSm / (panel_smem_bytes(nbp) + kPanelSmemPerCta);
   auto fits = [&](int W) {
     const int by_threads = 2048 / (32 * W);
     int per_sm = panel_ctas_by_regs<F>(W);
     per_sm = per_sm < by_threads ? per_sm : by_threads;
     per_sm = per_sm < by_smem ? per_sm : by_smem;
-    return L.panels <= int64_t(per_sm) * sms;
+    return panels <= int64_t(per_sm) * sms;
   };
   auto busiest = [&](int W, int UB) { return (nbp / UB + W - 1) / W * (UB / 2); };  // half quads
   int W = 0;
@@ -293,25 +320,26 @@ PanelConfig panel_config_for(int64_t rows, int64_t n, int sms) {
 }  // namespace
 
 template <class F>
-PanelConfig panel_config(int64_t rows, int64_t n, int sms) {
-  return panel_config_for<F>(rows, n, sms);
+PanelConfig panel_config(const q1_product* prods, int count, int sms) {
+  return panel_config_for<F>(prods, count, sms);
 }
-template PanelConfig panel_config<FmtQ1>(int64_t, int64_t, int);
-template PanelConfig panel_config<FmtQ2>(int64_t, int64_t, int);
+template PanelConfig panel_config<FmtQ1>(const q1_product*, int, int);
+template PanelConfig panel_config<FmtQ2>(const q1_product*, int, int);
 
 template <class F>
-int launch_panel(const q1_product& pr, PanelConfig c, cudaStream_t s, const char* who) {
+int launch_panel(const q1_product* prods, int count, PanelConfig c, cudaStream_t s, const char* who) {
+  if (count < 1 || count > kPanelMaxProducts) return fail(Q1_ERR_ARG, "%s: %d products for the panel kernel", who, count);
   switch (c.warps * 10 + c.unit) {
-    case 164: return launch_panel_w<F, 16, 4>(pr, s, who);
-    case 162: return launch_panel_w<F, 16, 2>(pr, s, who);
-    case 84: return launch_panel_w<F, 8, 4>(pr, s, who);
-    case 82: return launch_panel_w<F, 8, 2>(pr, s, who);
-    case 44: return launch_panel_w<F, 4, 4>(pr, s, who);
-    case 42: return launch_panel_w<F, 4, 2>(pr, s, who);
+    case 164: return launch_panel_w<F, 16, 4>(prods, count, s, who);
+    case 162: return launch_panel_w<F, 16, 2>(prods, count, s, who);
+    case 84: return launch_panel_w<F, 8, 4>(prods, count, s, who);
+    case 82: return launch_panel_w<F, 8, 2>(prods, count, s, who);
+    case 44: return launch_panel_w<F, 4, 4>(prods, count, s, who);
+    case 42: return launch_panel_w<F, 4, 2>(prods, count, s, who);
     default: return fail(Q1_ERR_ARG, "%s: %d warps x %d-block units per panel", who, c.warps, c.unit);
   }
 }
-template int launch_panel<FmtQ1>(const q1_product&, PanelConfig, cudaStream_t, const char*);
-template int launch_panel<FmtQ2>(const q1_product&, PanelConfig, cudaStream_t, const char*);
+template int launch_panel<FmtQ1>(const q1_product*, int, PanelConfig, cudaStream_t, const char*);
+template int launch_panel<FmtQ2>(const q1_product*, int, PanelConfig, cudaStream_t, const char*);
 
 }  // namespace q1

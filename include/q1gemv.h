@@ -153,11 +153,12 @@ typedef struct q1_multi_plan {
   int grid;               /* CTAs launched                                          */
   int64_t total_cost;     /* sum over products of tiles x padded blocks per row     */
   int64_t max_range_cost; /* largest tile cost owned by one CTA                     */
-  int panel_warps;        /* 0: the streaming kernel above.  Else the call is a
-                             single product of few rows, run as one CTA per
-                             32-row panel whose panel_warps warps share out its
-                             blocks in units of panel_unit_blocks (grid =
-                             panels, rows_per_thread = 4, both costs 0, no cuts) */
+  int panel_warps;        /* 0: the streaming kernel above.  Else the call (up to
+                             8 products of few rows in total) runs as one CTA per
+                             32-row panel of each product, whose panel_warps
+                             warps share out the panel's blocks in units of
+                             panel_unit_blocks (grid = panels of all products,
+                             rows_per_thread = 4, both costs 0, no cuts) */
   int panel_unit_blocks;  /* 4 (quads) or 2 (half quads); 0 with the streaming kernel */
 } q1_multi_plan;
 

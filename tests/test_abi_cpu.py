@@ -184,7 +184,8 @@ def test_multi_plan_decode_set_is_balanced(lib):
 
 def test_multi_plan_small_lists_split_evenly(lib):
     shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
-    plan = binding.multi_plan(shapes, sms=152)
+    plan = binding.multi_plan(shapes, sms=16)  # too many panels for one wave of the panel kernel
+    assert plan["panel_warps"] == 0
     tiles = _tiles(shapes, plan["rows_per_thread"])
     starts, total = _tile_starts(tiles)
     g = plan["grid"]
@@ -250,8 +251,8 @@ def test_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
         _check_panel_choice(plan, rows, n, 80 if warps < 16 else 128)
     else:
         assert plan["grid"] > 0 and len(plan["cuts"]) == plan["grid"] + 1
-    # two products always take the streaming kernel
-    assert binding.multi_plan([(rows, n), (32, 128)], sms=152)["panel_warps"] == 0
+    # a second product with a row too long for the panel kernel sends the pair to the streaming kernel
+    assert binding.multi_plan([(rows, n), (32, 20096)], sms=152)["panel_warps"] == 0
 
 
 @pytest.mark.parametrize("rows,n,warps,unit", [
@@ -264,9 +265,27 @@ def test_q2_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
     assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
     if warps:
         _check_panel_choice(plan, rows, n, 128)
-    q1 = binding.multi_plan([(rows, n), (32, 128)], sms=152)
-    q2 = binding.multi_plan([(rows, n), (32, 128)], sms=152, fmt="q2")
-    assert q2 == q1  # the streaming split depends on the shapes only
+    q1 = binding.multi_plan([(rows, n), (32, 20096)], sms=152)
+    q2 = binding.multi_plan([(rows, n), (32, 20096)], sms=152, fmt="q2")
+    assert q2 == q1 and q1["panel_warps"] == 0  # the streaming split depends on the shapes only
+
+
+@pytest.mark.parametrize("shapes,warps,unit", [
+    ([(4096, 4096), (1024, 4096), (1024, 4096)], 8, 4),     # q, k, v of one layer
+    ([(2048, 4096), (1000, 14336), (33, 128)], 16, 4),      # unequal rows and n
+    ([(300, 1024)] * 8, 4, 2),                               # eight products
+    ([(14336, 4096), (14336, 4096)], 0, 0),                  # gate and up: 896 panels, more than one wave
+    ([(32, 128)] * 9, 0, 0),                                 # more than eight products
+    ([(64, 4096), (32, 20096)], 0, 0)])                      # a row longer than 156 blocks
+def test_multi_plan_panel_lists(lib, shapes, warps, unit):
+    """Lists of up to 8 products whose panels together fit one wave take the
+    panel kernel, sized by the longest row and the total panels."""
+    plan = binding.multi_plan(shapes, sms=152)
+    assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
+    if warps:
+        panels = sum(-(-r // 256) * 8 for r, _ in shapes)
+        nbp = max(-(-(n // 128) // 4) * 4 for _, n in shapes)
+        assert plan["grid"] == panels <= _panel_per_sm(warps, nbp, 80 if warps < 16 else 128) * 152
 
 
 def test_multi_plan_rejects_bad_arguments(lib):

@@ -3,7 +3,8 @@ out the panel's block quads) against the CPU oracle and against the streaming
 kernel, through the C ABI.
 
 A single product of few rows goes to the panel kernel; the same product
-launched together with a second one goes to the streaming kernel.  Both must
+launched together with one whose row is too long for it goes to the
+streaming kernel.  Both must
 give the oracle's bits: every output of the two launches is compared with the
 other, and with the oracle in full for small shapes and on sampled rows (first
 and last included) for the Llama-3-8B shapes.  The shapes cover every warp
@@ -58,10 +59,12 @@ def _sample(rows, rng):
 
 
 def _run(fmt, packed, rows, n, x, q, d):
-    """(panel-kernel output, streaming-kernel output) of one product."""
+    """(panel-kernel output, streaming-kernel output) of one product: paired
+    with a product whose row is too long for the panel kernel, the launch
+    takes the streaming kernel."""
     alone = torch.full((rows,), float("nan"), device="cuda")
     paired = torch.full((rows,), float("nan"), device="cuda")
-    dummy_rows, dummy_n = 32, 128
+    dummy_rows, dummy_n = 32, 20096
     if fmt == "q1":
         dummy = binding.pack(dev(synth.weight_blocks(synth.rng_for(999), dummy_rows, dummy_n)), dummy_rows, dummy_n)
         multi = binding.gemv_multi
@@ -150,3 +153,38 @@ def test_panel_in_graph_with_dependent_launches():
         want = oracle.gemv(blocks[i], q[0], d[0])
         bits_equal(bufs[i + 1].cpu().numpy(), want)
         x = want
+
+
+@pytest.mark.parametrize("shapes", [
+    [(4096, 4096), (1024, 4096), (1024, 4096)],
+    [(2048, 4096), (1000, 14336), (33, 128)],
+    [(300, 1024), (7, 384), (256, 1152), (1, 128), (100, 2048), (32, 640), (500, 1024), (64, 4096)]])
+def test_panel_product_lists(shapes):
+    """Several products in one panel launch (one CTA per panel of each), f32
+    and q8_0 activations mixed: every output against the oracle and against
+    the same products launched one at a time."""
+    plan = binding.multi_plan(shapes)
+    assert plan["panel_warps"] > 0
+    items, want, alone = [], [], []
+    for i, (rows, n) in enumerate(shapes):
+        rng = synth.rng_for(504, i, rows, n)
+        blocks = synth.weight_blocks(rng, rows, n, "lognormal" if i % 2 else "halfnormal")
+        packed = binding.pack(dev(blocks), rows, n)
+        out = torch.full((rows,), float("nan"), device="cuda")
+        if i % 3 == 1:
+            q, d = synth.raw_quants(rng, 1, n, scale="lognormal", m128_frac=0.03)
+            item = (packed, rows, n, None, dev(q[0]), dev(d[0].view(np.int16)), out)
+        else:
+            xh = synth.activations(rng, 1, n, outliers=0.01)
+            q, d = oracle.q8_quantize(xh)
+            item = (packed, rows, n, dev(xh[0]), None, None, out)
+        items.append(item)
+        want.append(oracle.gemv(blocks, q[0], d[0]))
+        one = torch.full((rows,), float("nan"), device="cuda")
+        binding.gemv_multi([item[:-1] + (one,)])
+        alone.append(one)
+    binding.gemv_multi(items)
+    torch.cuda.synchronize()
+    for item, w, one in zip(items, want, alone):
+        bits_equal(item[-1].cpu().numpy(), w)
+        bits_equal(one.cpu().numpy(), w)
