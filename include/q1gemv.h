@@ -234,7 +234,9 @@ int q1_device_status(int clear);
  * checked the same way).  Runs synchronously on
  * the current device with its own allocations, against a host-side reference
  * compiled into the library.
- *   flags  : 0 = default shape set; bit 0 (1) = quick set (three small shapes);
+ *   flags  : 0 = default shape set (small products for the panel kernel, two
+ *            with too many rows for it that take the streaming kernel, and
+ *            the batched product); bit 0 (1) = quick set (three small shapes);
  *            bit 1 (2) = negative control: in every one-vector case the
  *            packed scales of one row (nonzero reference output, about the
  *            middle row) are doubled after packing, so the check must report
