@@ -285,7 +285,10 @@ int launch_panel_w(const q1_product* prods, int count, cudaStream_t s, const cha
 // (16, 8, 4; starting from the longest row's quads rounded up) whose grid of
 // one CTA per panel of every product is one wave; then half-quad units, and
 // twice the warps where that still fits, when they lower the work of the
-// busiest warp.
+// busiest warp.  A list that no shape runs in one wave takes the panel kernel
+// in two waves when it has more than one product (gate and up together), at
+// the W with the least work per SM; a single product, or more panels than two
+// waves, goes to the streaming kernel.
 template <class F>
 PanelConfig panel_config_for(const q1_product* prods, int count, int sms) {
   if (count < 1 || count > kPanelMaxProducts) return {};
@@ -299,18 +302,28 @@ PanelConfig panel_config_for(const q1_product* prods, int count, int sms) {
   if (nbp > kPanelMaxNbp) return {};
   const int nq = nbp / 4;
   const int by_smem = kPanelSmemPerSm / (panel_smem_bytes(nbp) + kPanelSmemPerCta);
-  auto fits = [&](int W) {
+  auto per_sm = [&](int W) {
     const int by_threads = 2048 / (32 * W);
-    int per_sm = panel_ctas_by_regs<F>(W);
-    per_sm = per_sm < by_threads ? per_sm : by_threads;
-    per_sm = per_sm < by_smem ? per_sm : by_smem;
-    return panels <= int64_t(per_sm) * sms;
+    int c = panel_ctas_by_regs<F>(W);
+    c = c < by_threads ? c : by_threads;
+    return c < by_smem ? c : by_smem;
   };
+  auto fits = [&](int W) { return panels <= int64_t(per_sm(W)) * sms; };
   auto busiest = [&](int W, int UB) { return (nbp / UB + W - 1) / W * (UB / 2); };  // half quads
+  const int W0 = nq > 8 ? 16 : nq > 4 ? 8 : 4;
   int W = 0;
-  for (int Wc = nq > 8 ? 16 : nq > 4 ? 8 : 4; Wc >= 4 && !W; Wc >>= 1)
+  for (int Wc = W0; Wc >= 4 && !W; Wc >>= 1)
     if (fits(Wc)) W = Wc;
-  if (!W) return {};
+  if (!W) {
+    if (count < 2) return {};
+    int64_t best = 0;
+    for (int Wc = W0; Wc >= 4; Wc >>= 1) {
+      if (panels > 2 * int64_t(per_sm(Wc)) * sms) continue;
+      const int64_t work = (panels + sms - 1) / sms * busiest(Wc, 4) * Wc;  // warp half-quads per SM
+      if (!W || work < best) W = Wc, best = work;
+    }
+    return W ? PanelConfig{W, 4} : PanelConfig{};
+  }
   PanelConfig c{W, 4};
   if (busiest(W, 2) < busiest(W, 4)) c.unit = 2;
   if (2 * W <= 16 && fits(2 * W) && busiest(2 * W, 2) < busiest(c.warps, c.unit)) c = PanelConfig{2 * W, 2};

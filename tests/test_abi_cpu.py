@@ -274,18 +274,21 @@ def test_q2_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
     ([(4096, 4096), (1024, 4096), (1024, 4096)], 8, 4),     # q, k, v of one layer
     ([(2048, 4096), (1000, 14336), (33, 128)], 16, 4),      # unequal rows and n
     ([(300, 1024)] * 8, 4, 2),                               # eight products
-    ([(14336, 4096), (14336, 4096)], 0, 0),                  # gate and up: 896 panels, more than one wave
+    ([(14336, 4096), (14336, 4096)], 8, 4),                  # gate and up: 896 panels, two waves
+    ([(14336, 4096)] * 3, 0, 0),                             # more than two waves
     ([(32, 128)] * 9, 0, 0),                                 # more than eight products
     ([(64, 4096), (32, 20096)], 0, 0)])                      # a row longer than 156 blocks
 def test_multi_plan_panel_lists(lib, shapes, warps, unit):
-    """Lists of up to 8 products whose panels together fit one wave take the
-    panel kernel, sized by the longest row and the total panels."""
+    """Lists of up to 8 products whose panels together fit one wave, or two
+    waves when no shape fits one, take the panel kernel, sized by the longest
+    row and the total panels."""
     plan = binding.multi_plan(shapes, sms=152)
     assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
     if warps:
         panels = sum(-(-r // 256) * 8 for r, _ in shapes)
         nbp = max(-(-(n // 128) // 4) * 4 for _, n in shapes)
-        assert plan["grid"] == panels <= _panel_per_sm(warps, nbp, 80 if warps < 16 else 128) * 152
+        waves = 1 if panels <= _panel_per_sm(4, nbp, 80) * 152 else 2
+        assert plan["grid"] == panels <= waves * _panel_per_sm(warps, nbp, 80 if warps < 16 else 128) * 152
 
 
 def test_multi_plan_rejects_bad_arguments(lib):

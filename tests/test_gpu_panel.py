@@ -157,12 +157,14 @@ def test_panel_in_graph_with_dependent_launches():
 
 @pytest.mark.parametrize("shapes", [
     [(4096, 4096), (1024, 4096), (1024, 4096)],
+    [(14336, 4096), (14336, 4096)],  # gate and up: two waves
     [(2048, 4096), (1000, 14336), (33, 128)],
     [(300, 1024), (7, 384), (256, 1152), (1, 128), (100, 2048), (32, 640), (500, 1024), (64, 4096)]])
 def test_panel_product_lists(shapes):
-    """Several products in one panel launch (one CTA per panel of each), f32
-    and q8_0 activations mixed: every output against the oracle and against
-    the same products launched one at a time."""
+    """Several products in one panel launch (one CTA per panel of each, in
+    one wave or, for gate and up, two), f32 and q8_0 activations mixed: every
+    output against the oracle and against the same products launched one at
+    a time."""
     plan = binding.multi_plan(shapes)
     assert plan["panel_warps"] > 0
     items, want, alone = [], [], []
@@ -188,3 +190,24 @@ def test_panel_product_lists(shapes):
     for item, w, one in zip(items, want, alone):
         bits_equal(item[-1].cpu().numpy(), w)
         bits_equal(one.cpu().numpy(), w)
+
+
+def test_panel_q2_two_wave_list():
+    """Two Q2_0 products whose 752 panels need two waves of the Q2_0 panel
+    kernel (one wave of the Q1_0 one): every output against the oracle."""
+    shapes = [(12000, 2048), (12000, 2048)]
+    assert binding.multi_plan(shapes, sms=152, fmt="q2")["panel_warps"] > 0
+    assert binding.multi_plan(shapes, fmt="q2")["panel_warps"] > 0
+    items, want = [], []
+    for i, (rows, n) in enumerate(shapes):
+        rng = synth.rng_for(505, i)
+        tb = synth.ternary_blocks(rng, rows, n, "lognormal")
+        xh = synth.activations(rng, 1, n, outliers=0.01)
+        q, d = oracle.q8_quantize(xh)
+        out = torch.full((rows,), float("nan"), device="cuda")
+        items.append((binding.q2_pack(dev(tb), rows, n), rows, n, dev(xh[0]), None, None, out))
+        want.append(oracle.q2_gemv(tb, q[0], d[0]))
+    binding.q2_gemv_multi(items)
+    torch.cuda.synchronize()
+    for item, w in zip(items, want):
+        bits_equal(item[-1].cpu().numpy(), w)
