@@ -103,8 +103,10 @@ __device__ __forceinline__ void unit_ab(const uint4 (&wv)[4], const uint4 (&nv)[
   }
 }
 
-// Registers a thread may use (the prefetched words of PF units dominate), and
-// the CTAs of W warps an SM then holds by registers.
+// Register budget of a thread (the prefetched words of PF units dominate) and
+// the CTAs of W warps an SM holds at that budget (at least one).  The kernel's
+// launch bounds ask for that many CTAs an SM, which holds the compiler to the
+// budget; where that is one CTA (16 warps) it may use up to 128 registers.
 template <class F>
 __host__ __device__ constexpr int panel_regs() { return F::kTwoPlanes ? 128 : 80; }
 template <class F>
