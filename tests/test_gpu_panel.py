@@ -104,7 +104,8 @@ def test_panel_q1_equals_streaming_and_oracle(rows, n, warps, unit, act):
 
 
 @pytest.mark.parametrize("rows,n,warps,unit", [s for s in SHAPES if s[0] * s[1] <= 4096 * 14336])
-def test_panel_q2_equals_streaming_and_oracle(rows, n, warps, unit):
+@pytest.mark.parametrize("act", ["f32", "q8"])
+def test_panel_q2_equals_streaming_and_oracle(rows, n, warps, unit, act):
     """Q2_0 keeps up to 128 registers a thread, so its warp counts can be
     lower than Q1_0's; every shape here stays within its one-wave limit."""
     assert binding.multi_plan([(rows, n)], fmt="q2")["panel_warps"] > 0
@@ -114,9 +115,14 @@ def test_panel_q2_equals_streaming_and_oracle(rows, n, warps, unit):
     else:
         tb = synth.ternary_blocks(rng, rows, n, "lognormal")
     packed = binding.q2_pack(dev(tb), rows, n)
-    xh = synth.activations(rng, 1, n, outliers=0.01)
-    q, d = oracle.q8_quantize(xh)
-    alone, paired = _run("q2", packed, rows, n, dev(xh[0]), None, None)
+    if act == "f32":
+        xh = synth.activations(rng, 1, n, outliers=0.01)
+        q, d = oracle.q8_quantize(xh)
+        args = (dev(xh[0]), None, None)
+    else:
+        q, d = synth.raw_quants(rng, 1, n, scale="lognormal", m128_frac=0.03)
+        args = (None, dev(q[0]), dev(d[0].view(np.int16)))
+    alone, paired = _run("q2", packed, rows, n, *args)
     bits_equal(alone, paired)
     idx = _sample(rows, rng)
     want = (oracle.q2_gemv(tb, q[0], d[0]) if rows <= FULL_ORACLE_ROWS
