@@ -1,6 +1,8 @@
-// multi.cu -- the streaming matrix-vector kernel: q1_0_gemv / q2_0_gemv (one
-// product) and q1_0_gemv_multi / q2_0_gemv_multi (up to Q1_MAX_PRODUCTS
-// independent products in one launch).
+// multi.cu -- the streaming matrix-vector kernel behind q1_0_gemv_multi /
+// q2_0_gemv_multi (up to Q1_MAX_PRODUCTS independent products in one launch)
+// and q1_0_gemv / q2_0_gemv, for launches of many rows or many products; the
+// launcher here (launch_products) sends launches of a few thousand rows in
+// total to the panel kernel (panel.cu) instead.
 //
 // Definition (bankML "docs/modules/gpu.md", "kernels.rs -- the Q1_0 kernels",
 // first and second bullets): each output row is one dot product of 128-weight
