@@ -291,6 +291,41 @@ def test_multi_plan_panel_lists(lib, shapes, warps, unit):
         assert plan["grid"] == panels <= waves * _panel_per_sm(warps, nbp, 80 if warps < 16 else 128) * 152
 
 
+@pytest.mark.parametrize("fmt,regs", [("q1", 80), ("q2", 128)])
+@pytest.mark.parametrize("seed", range(4))
+def test_multi_plan_panel_rules_random_lists(lib, fmt, regs, seed):
+    """Random lists of 1-10 products: the launcher's kernel choice follows its
+    stated rules.  The panel kernel only for at most 8 products with rows of at
+    most 156 blocks; one wave when any shape fits one (the busiest warp then
+    no more loaded than under any other one-wave shape); two waves only for
+    lists of two or more that fit no shape in one; the streaming kernel
+    otherwise."""
+    import random
+    rnd = random.Random(1000 + seed)
+    for _ in range(60):
+        count = rnd.randint(1, 10)
+        shapes = [(rnd.choice([1, 33, 256, 1024, 4096, 6000, 14336, 20000]),
+                   128 * rnd.choice([1, 3, 8, 16, 32, 112, 156, 157])) for _ in range(count)]
+        plan = binding.multi_plan(shapes, sms=152, fmt=fmt)
+        panels = sum(-(-r // 256) * 8 for r, _ in shapes)
+        nbp = max(-(-(n // 128) // 4) * 4 for _, n in shapes)
+        per_sm = lambda w: min(max(1, 65536 // (regs * 32 * w)), 2048 // (32 * w), 233472 // (nbp * 1472 + 1024))
+        one_wave = [w for w in (4, 8, 16) if panels <= per_sm(w) * 152]
+        two_wave = [w for w in (4, 8, 16) if panels <= 2 * per_sm(w) * 152]
+        eligible = count <= 8 and nbp <= 156
+        if not eligible or (not one_wave and (count < 2 or not two_wave)):
+            assert plan["panel_warps"] == 0, (shapes, plan)
+            continue
+        assert plan["panel_warps"] in (4, 8, 16) and plan["grid"] == panels, (shapes, plan)
+        w, u = plan["panel_warps"], plan["panel_unit_blocks"]
+        if one_wave:
+            assert panels <= per_sm(w) * 152
+            best = min(_busiest(nbp, w2, u2) for w2 in one_wave for u2 in (4, 2))
+            assert _busiest(nbp, w, u) == best, (shapes, plan)
+        else:
+            assert count >= 2 and u == 4 and panels <= 2 * per_sm(w) * 152, (shapes, plan)
+
+
 def test_multi_plan_rejects_bad_arguments(lib):
     with pytest.raises(binding.Q1Error):
         binding.multi_plan([(0, 128)], sms=4)
