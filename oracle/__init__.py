@@ -85,6 +85,10 @@ def _load():
         lib.q1o_rows_sampled.restype = None
         lib.q1o_gemv_threaded.argtypes = [P, I64, I64, P, P, P, ctypes.c_int]
         lib.q1o_gemv_threaded.restype = ctypes.c_longlong
+        lib.q1o_gemm_threaded.argtypes = [P, I64, I64, I64, P, P, P, ctypes.c_int]
+        lib.q1o_gemm_threaded.restype = ctypes.c_longlong
+        lib.q2o_gemv_threaded.argtypes = [P, I64, I64, P, P, P, ctypes.c_int]
+        lib.q2o_gemv_threaded.restype = ctypes.c_longlong
         lib.q2o_weight.argtypes = [P, I64, I64, I64]
         lib.q2o_weight.restype = ctypes.c_float
         lib.q2o_dot_row.argtypes = [P, I64, P, P]
@@ -264,6 +268,31 @@ def gemv_threaded(blocks: np.ndarray, q: np.ndarray, d: np.ndarray, threads: int
     return out, int(done)
 
 
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def gemm_threaded(blocks: np.ndarray, q: np.ndarray, d: np.ndarray, threads: int | None = None) -> np.ndarray:
+    """Batched product on `threads` threads (16-row claims, every vector of a
+    claimed row by the single-thread row function): float32 [B, rows],
+    bit-identical to ``gemm``."""
+    rows, n = _check_blocks(blocks)
+    blocks = _c(blocks, np.uint8)
+    q = _c(q, np.int8)
+    d = _c(d, np.uint16)
+    if q.ndim == 1:
+        q, d = q[None, :], d[None, :]
+    nvec = q.shape[0]
+    if q.shape != (nvec, n) or d.shape != (nvec, n // 32):
+        raise ValueError("activation shape mismatch")
+    out = np.empty((nvec, rows), dtype=np.float32)
+    done = _load().q1o_gemm_threaded(_ptr(blocks), rows, n, nvec, _ptr(q), _ptr(d), _ptr(out),
+                                     int(threads or default_threads()))
+    if done != rows:
+        raise RuntimeError("threaded oracle did not write every row")
+    return out
+
+
 # ------------------------------------------------------- Q2_0 (ternary) --
 def _check_tblocks(tblocks: np.ndarray):
     if tblocks.ndim != 3 or tblocks.shape[2] != 34:
@@ -307,6 +336,22 @@ def q2_gemv(tblocks: np.ndarray, q: np.ndarray, d: np.ndarray) -> np.ndarray:
         raise ValueError("activation shape mismatch")
     out = np.empty(rows, dtype=np.float32)
     _load().q2o_gemv(_ptr(tblocks), rows, n, _ptr(q), _ptr(d), _ptr(out))
+    return out
+
+
+def q2_gemv_threaded(tblocks: np.ndarray, q: np.ndarray, d: np.ndarray, threads: int | None = None) -> np.ndarray:
+    """Q2_0 matrix-vector product on `threads` threads, bit-identical to ``q2_gemv``."""
+    rows, n = _check_tblocks(tblocks)
+    tblocks = _c(tblocks, np.uint8)
+    q = _c(q, np.int8).ravel()
+    d = _c(d, np.uint16).ravel()
+    if q.size != n or d.size != n // 32:
+        raise ValueError("activation shape mismatch")
+    out = np.empty(rows, dtype=np.float32)
+    done = _load().q2o_gemv_threaded(_ptr(tblocks), rows, n, _ptr(q), _ptr(d), _ptr(out),
+                                     int(threads or default_threads()))
+    if done != rows:
+        raise RuntimeError("threaded oracle did not write every row")
     return out
 
 

@@ -453,16 +453,21 @@ void q2o_rows_sampled(const uint8_t *blocks, int64_t n, int64_t count, const int
 /* function, so the bits do not depend on the thread count).                 */
 /* ------------------------------------------------------------------------ */
 
+typedef float (*q1o_row_fn)(const uint8_t *, int64_t, const int8_t *, const uint16_t *);
+
 typedef struct {
+    q1o_row_fn row;          /* q1o_dot_row or q2o_dot_row                  */
     const uint8_t *blocks;
-    int64_t rows, nb;
-    const int8_t *q;
-    const uint16_t *d;
-    float *out;
+    int64_t rows, n, nb, nvec, block_bytes;
+    const int8_t *q;         /* nvec * n quants                             */
+    const uint16_t *d;       /* nvec * n/32 scales                          */
+    float *out;              /* nvec * rows: out[v*rows + r]                */
     atomic_llong next;
     atomic_llong rows_done;
 } q1o_job;
 
+/* A claim is 16 consecutive rows; the claimant computes them for every
+ * vector, each output by the single-thread row function. */
 static void *q1o_worker(void *arg)
 {
     q1o_job *job = (q1o_job *)arg;
@@ -473,31 +478,25 @@ static void *q1o_worker(void *arg)
         long long r1 = r0 + Q1O_CHUNK_ROWS;
         if (r1 > job->rows)
             r1 = job->rows;
-        for (long long r = r0; r < r1; ++r)
-            job->out[r] = q1o_dot_row(job->blocks + r * job->nb * Q1O_BLOCK_BYTES, job->nb,
-                                      job->q, job->d);
+        for (int64_t v = 0; v < job->nvec; ++v)
+            for (long long r = r0; r < r1; ++r)
+                job->out[v * job->rows + r] =
+                    job->row(job->blocks + r * job->nb * job->block_bytes, job->nb,
+                             job->q + v * job->n, job->d + v * (job->n / Q1O_QBLOCK));
         atomic_fetch_add(&job->rows_done, r1 - r0);
     }
     return NULL;
 }
 
-/* Returns the number of rows written (== rows on success), or -1 if a thread
- * could not be started.  The calling thread is worker 0. */
-long long q1o_gemv_threaded(const uint8_t *blocks, int64_t rows, int64_t n,
-                            const int8_t *q, const uint16_t *d, float *out, int threads)
+/* Runs `job` on `threads` threads (the calling thread is worker 0).  Returns
+ * the number of rows written (== rows on success), or -1 if a thread could
+ * not be started. */
+static long long q1o_run_threaded(q1o_job *job, int threads)
 {
     if (threads < 1)
         threads = 1;
-    q1o_job job;
-    job.blocks = blocks;
-    job.rows = rows;
-    job.nb = n / Q1O_BLOCK;
-    job.q = q;
-    job.d = d;
-    job.out = out;
-    atomic_init(&job.next, 0);
-    atomic_init(&job.rows_done, 0);
-
+    atomic_init(&job->next, 0);
+    atomic_init(&job->rows_done, 0);
     pthread_t *tid = NULL;
     int started = 0;
     if (threads > 1) {
@@ -505,16 +504,55 @@ long long q1o_gemv_threaded(const uint8_t *blocks, int64_t rows, int64_t n,
         if (!tid)
             return -1;
         for (int t = 0; t < threads - 1; ++t) {
-            if (pthread_create(&tid[t], NULL, q1o_worker, &job) != 0)
+            if (pthread_create(&tid[t], NULL, q1o_worker, job) != 0)
                 break;
             ++started;
         }
     }
-    q1o_worker(&job);
+    q1o_worker(job);
     for (int t = 0; t < started; ++t)
         pthread_join(tid[t], NULL);
     free(tid);
     if (threads > 1 && started != threads - 1)
         return -1;
-    return (long long)atomic_load(&job.rows_done);
+    return (long long)atomic_load(&job->rows_done);
+}
+
+static long long q1o_threaded(q1o_row_fn row, int64_t block_bytes, const uint8_t *blocks, int64_t rows,
+                              int64_t n, int64_t nvec, const int8_t *q, const uint16_t *d, float *out,
+                              int threads)
+{
+    q1o_job job;
+    job.row = row;
+    job.blocks = blocks;
+    job.rows = rows;
+    job.n = n;
+    job.nb = n / Q1O_BLOCK;
+    job.nvec = nvec;
+    job.block_bytes = block_bytes;
+    job.q = q;
+    job.d = d;
+    job.out = out;
+    return q1o_run_threaded(&job, threads);
+}
+
+/* Matrix-vector product on `threads` threads: out[r] = q1o_dot_row(row r). */
+long long q1o_gemv_threaded(const uint8_t *blocks, int64_t rows, int64_t n,
+                            const int8_t *q, const uint16_t *d, float *out, int threads)
+{
+    return q1o_threaded(q1o_dot_row, Q1O_BLOCK_BYTES, blocks, rows, n, 1, q, d, out, threads);
+}
+
+/* Batched product on `threads` threads: out[v*rows + r] as q1o_gemm. */
+long long q1o_gemm_threaded(const uint8_t *blocks, int64_t rows, int64_t n, int64_t nvec,
+                            const int8_t *q, const uint16_t *d, float *out, int threads)
+{
+    return q1o_threaded(q1o_dot_row, Q1O_BLOCK_BYTES, blocks, rows, n, nvec, q, d, out, threads);
+}
+
+/* Q2_0 matrix-vector product on `threads` threads: out[r] = q2o_dot_row(row r). */
+long long q2o_gemv_threaded(const uint8_t *blocks, int64_t rows, int64_t n,
+                            const int8_t *q, const uint16_t *d, float *out, int threads)
+{
+    return q1o_threaded(q2o_dot_row, Q2O_BLOCK_BYTES, blocks, rows, n, 1, q, d, out, threads);
 }

@@ -344,6 +344,22 @@ def test_thread_count_invariance(oracle_mod, threads):
         assert np.all(np.isnan(out[rows:]))
 
 
+@pytest.mark.parametrize("threads", [1, 2, 3, 5])
+def test_threaded_gemm_thread_count_invariance(oracle_mod, threads):
+    """The threaded batched product (several vectors per claimed row) equals the
+    single-thread product per vector at 1, 2, 3 and 5 threads, with ragged
+    row counts and -128 quants (par.md, "How it is verified")."""
+    rng = synth.rng_for(31)
+    blocks_all = synth.weight_blocks(rng, 203, 384, "lognormal")
+    q, d = synth.raw_quants(rng, 3, 384, m128_frac=0.02)
+    for rows in (1, 16, 17, 203):
+        got = oracle_mod.gemm_threaded(blocks_all[:rows], q, d, threads)
+        assert got.shape == (3, rows)
+        for v in range(3):
+            want = oracle_mod.gemv(blocks_all[:rows], q[v], d[v])
+            assert np.array_equal(got[v].view(np.uint32), want.view(np.uint32))
+
+
 def test_threaded_reused_many_times(oracle_mod):
     rng = synth.rng_for(29)
     blocks = synth.weight_blocks(rng, 37, 128)

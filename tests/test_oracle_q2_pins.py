@@ -156,3 +156,16 @@ def test_rows_sampled_matches_gemv(oracle_mod):
     idx = np.array([0, 7, 49, 13, 13])
     assert np.array_equal(oracle_mod.q2_rows_sampled(tb, idx, q[0], d[0]).view(np.uint32),
                           full[idx].view(np.uint32))
+
+
+@pytest.mark.parametrize("threads", [1, 2, 3, 5])
+def test_q2_threaded_thread_count_invariance(oracle_mod, threads):
+    """The threaded Q2_0 product equals the single-thread one at 1, 2, 3 and 5
+    threads (par.md, "How it is verified")."""
+    rng = synth.rng_for(61)
+    tb = synth.ternary_blocks(rng, 181, 256, p_zero=1 / 3, scale="lognormal")
+    q, d = synth.raw_quants(rng, 1, 256, m128_frac=0.02)
+    for rows in (1, 16, 17, 181):
+        got = oracle_mod.q2_gemv_threaded(tb[:rows], q[0], d[0], threads)
+        want = oracle_mod.q2_gemv(tb[:rows], q[0], d[0])
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
