@@ -20,7 +20,8 @@ Printed (rank 0, one JSON line):
               launch / launch time vs the measured HBM peak
   e2e         same metric with the activations copied in from pinned host memory
               and the outputs copied back inside every timed step
-  cpu_baseline  the CPU oracle timed on a bounded sample (rank 0, N = 1 only)
+  cpu_baseline  the threaded CPU oracle timed over the whole set once (rank 0, N = 1 only)
+  parity      that oracle pass's outputs against every output of the timed step
 Multi-GPU: independent replicas (the product shards by rows, but this workload
 is one GPU's; N GPUs run N copies), scaling "weak".
 
@@ -146,32 +147,41 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------- CPU baseline --
-def cpu_oracle_sample(layers: int, budget_s: float, threads: int, seed: int = 3):
-    """Time the threaded CPU oracle (q8_0 quantization + product) on the first
-    `layers` layers of the decode set, repeated until about `budget_s` seconds
-    of work; returns (weight GB/s, description, threads)."""
+def cpu_oracle_set(ds, gpu_out, threads: int):
+    """The CPU baseline and the parity check of the timed step, in one pass:
+    the threaded oracle (q8_0 quantization + product) over every product of
+    the decode set `ds`, on the same seeded inputs, timed; and every one of
+    its outputs compared bit for bit with `gpu_out`, the device's output
+    buffer after one replay of the timed step.  Returns (weight GB/s,
+    description, threads, parity record)."""
+    import numpy as np
+
     import oracle
-    from decode_q1_gemv_gb300 import synth
 
     oracle.build()
-    shapes = synth.decode_set_shapes()[:7 * layers]
-    inputs = [(synth.weight_blocks(synth.rng_for(seed, i, 0), rows, n), synth.activations(synth.rng_for(seed, i, 1), 1, n))
-              for i, (_, rows, n) in enumerate(shapes)]
-    pass_bytes = sum(rows * n * 18 // 128 for _, rows, n in shapes)
-    done_bytes, elapsed, passes = 0, 0.0, 0
-    while elapsed < budget_s:
-        for blocks, x in inputs:
-            t0 = time.perf_counter()
-            q, d = oracle.q8_quantize(x)
-            oracle.gemv_threaded(blocks, q[0], d[0], threads)
-            elapsed += time.perf_counter() - t0
-        done_bytes += pass_bytes
-        passes += 1
-    gbs = done_bytes / elapsed / 1e9
-    desc = (f"first {layers} layers of the decode set ({len(shapes)} products, {pass_bytes / 1e6:.1f} MB of "
-            f"weights) x {passes} passes: q8_0 quantization + threaded oracle product, {threads} threads, "
-            f"{elapsed:.1f} s")
-    return gbs, desc, threads
+    elapsed, checked, mismatches, first = 0.0, 0, 0, None
+    for i, (name, rows, n) in enumerate(ds.shapes):
+        blocks, x = ds.host_blocks(i), ds.host_x(i)
+        t0 = time.perf_counter()
+        q, d = oracle.q8_quantize(x[None, :])
+        want, done = oracle.gemv_threaded(blocks, q[0], d[0], threads)
+        elapsed += time.perf_counter() - t0
+        got = gpu_out[ds.out_off[i]:ds.out_off[i] + rows]
+        bad = np.nonzero(got.view(np.uint32) != want.view(np.uint32))[0]
+        checked += rows
+        mismatches += int(bad.size) + (rows - int(done))
+        if first is None and (bad.size or done != rows):
+            first = f"{name} row {int(bad[0]) if bad.size else int(done)}"
+        del blocks
+    gbs = ds.weight_bytes / elapsed / 1e9
+    desc = (f"the whole decode set once ({len(ds.shapes)} products, {ds.weight_bytes / 1e6:.1f} MB of weights): "
+            f"q8_0 quantization + threaded oracle product, {threads} threads, {elapsed:.1f} s")
+    parity = {"checked": checked, "mismatches": mismatches, "oracle_s": round(elapsed, 2),
+              "compared": "every output of the timed step (one more replay of its graph) against the threaded "
+                          "oracle on the same seeded inputs, f32 bits equal"}
+    if first:
+        parity["first_mismatch"] = first
+    return gbs, desc, threads, parity
 
 
 def cpu_context(seed: int = 3):
@@ -529,9 +539,13 @@ def run_ours(args):
     traffic = recorded_traffic()
     clocks = sampler.summary()
 
-    cpu = ctx = None
+    cpu = ctx = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, desc, cores = cpu_oracle_sample(layers=4, budget_s=args.cpu_budget, threads=os.cpu_count() or 1)
+        ds.out_all.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        gpu_out = ds.out_all.cpu().numpy()
+        gbs, desc, cores, parity = cpu_oracle_set(ds, gpu_out, threads=os.cpu_count() or 1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
         ctx = cpu_context()
 
@@ -568,6 +582,7 @@ def run_ours(args):
             "gpu_launches": ds.launches("set") * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "parity": parity,
             "cpu_context": ctx,
         }
         print(json.dumps(line), flush=True)
@@ -582,7 +597,6 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU-oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip timing the single-product and batched configurations")

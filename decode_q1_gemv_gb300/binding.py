@@ -144,6 +144,19 @@ def _dev(t: torch.Tensor, name: str, dtypes, host_ok: bool = False) -> int:
     return t.data_ptr()
 
 
+def _packed_ptr(packed: torch.Tensor, rows: int, n: int, fmt: str) -> int:
+    """Pointer of a packed weight buffer after checking that it holds the
+    format's packed size for a rows x n matrix: the library reads that many
+    bytes from the pointer, which it cannot check itself."""
+    need = packed_bytes(rows, n) if fmt == "q1" else q2_packed_bytes(rows, n)
+    if not isinstance(packed, torch.Tensor):
+        raise TypeError("packed must be a torch.Tensor")
+    if packed.numel() * packed.element_size() < need:
+        raise ValueError(f"packed holds {packed.numel() * packed.element_size()} bytes; a {fmt.upper()}_0 "
+                         f"{rows} x {n} matrix needs {need}")
+    return _dev(packed, "packed", (torch.uint8,))
+
+
 _SCALE_DTYPES = (torch.int16, torch.float16) + ((torch.uint16,) if hasattr(torch, "uint16") else ())
 
 
@@ -174,7 +187,7 @@ def unpack(packed: torch.Tensor, rows: int, n: int, blocks: torch.Tensor | None 
         blocks = torch.empty((rows, n // 128, 18), dtype=torch.uint8, device=packed.device)
     if blocks.numel() != rows * (n // 128) * 18:
         raise ValueError("blocks must hold rows*(n/128) 18-byte blocks")
-    _check(load().q1_0_unpack(_dev(packed, "packed", (torch.uint8,)), rows, n,
+    _check(load().q1_0_unpack(_packed_ptr(packed, rows, n, "q1"), rows, n,
                               _dev(blocks, "blocks", (torch.uint8,)), _stream_ptr(stream)), "q1_0_unpack")
     return blocks
 
@@ -202,16 +215,20 @@ def gemv(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tens
         out = torch.empty(rows, dtype=torch.float32, device=q.device)
     if out.numel() != rows:
         raise ValueError("out must hold rows values")
-    _check(load().q1_0_gemv(_dev(packed, "packed", (torch.uint8,)), rows, n, _dev(q, "q", (torch.int8,)),
+    _check(load().q1_0_gemv(_packed_ptr(packed, rows, n, "q1"), rows, n, _dev(q, "q", (torch.int8,)),
                             _dev(d, "d", _SCALE_DTYPES), _dev(out, "out", (torch.float32,)),
                             _stream_ptr(stream)), "q1_0_gemv")
     return out
 
 
-def product_array(items):
+def product_array(items, fmt: str = "q1"):
     """Build a ctypes q1_product array from tuples
     (packed, rows, n, x_or_None, q_or_None, d_or_None, out) of CUDA tensors;
-    x, q, d and out may also be pinned host tensors."""
+    x, q, d and out may also be pinned host tensors.  fmt ("q1" or "q2") is
+    the weight format the array is for: each packed buffer is checked against
+    that format's packed size."""
+    if fmt not in ("q1", "q2"):
+        raise ValueError("fmt must be 'q1' or 'q2'")
     arr = (Product * len(items))()
     for i, (packed, rows, n, x, q, d, out) in enumerate(items):
         if x is None and (q is None or d is None):
@@ -222,7 +239,7 @@ def product_array(items):
             raise ValueError("q must hold n quants and d n/32 scales")
         if out.numel() != rows:
             raise ValueError("out must hold rows values")
-        arr[i] = Product(_dev(packed, "packed", (torch.uint8,)), int(rows), int(n),
+        arr[i] = Product(_packed_ptr(packed, int(rows), int(n), fmt), int(rows), int(n),
                          _dev(x, "x", (torch.float32,), True) if x is not None else None,
                          _dev(q, "q", (torch.int8,), True) if q is not None else None,
                          _dev(d, "d", _SCALE_DTYPES, True) if d is not None else None,
@@ -287,7 +304,7 @@ def q2_unpack(packed: torch.Tensor, rows: int, n: int, blocks: torch.Tensor | No
         blocks = torch.empty((rows, n // 128, 34), dtype=torch.uint8, device=packed.device)
     if blocks.numel() != rows * (n // 128) * 34:
         raise ValueError("blocks must hold rows*(n/128) 34-byte blocks")
-    _check(load().q2_0_unpack(_dev(packed, "packed", (torch.uint8,)), rows, n,
+    _check(load().q2_0_unpack(_packed_ptr(packed, rows, n, "q2"), rows, n,
                               _dev(blocks, "blocks", (torch.uint8,)), _stream_ptr(stream)), "q2_0_unpack")
     return blocks
 
@@ -300,7 +317,7 @@ def q2_gemv(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.T
         out = torch.empty(rows, dtype=torch.float32, device=q.device)
     if out.numel() != rows:
         raise ValueError("out must hold rows values")
-    _check(load().q2_0_gemv(_dev(packed, "packed", (torch.uint8,)), rows, n, _dev(q, "q", (torch.int8,)),
+    _check(load().q2_0_gemv(_packed_ptr(packed, rows, n, "q2"), rows, n, _dev(q, "q", (torch.int8,)),
                             _dev(d, "d", _SCALE_DTYPES), _dev(out, "out", (torch.float32,)),
                             _stream_ptr(stream)), "q2_0_gemv")
     return out
@@ -309,7 +326,7 @@ def q2_gemv(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.T
 def q2_gemv_multi(items=None, stream=None, array=None):
     """One launch for several independent Q2_0 products (items as product_array
     takes them, with packed buffers from q2_pack)."""
-    arr = array if array is not None else product_array(items)
+    arr = array if array is not None else product_array(items, fmt="q2")
     _check(load().q2_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q2_0_gemv_multi")
 
 
@@ -322,7 +339,7 @@ def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torc
         out = torch.empty((nvec, rows), dtype=torch.float32, device=q.device)
     if out.numel() != nvec * rows:
         raise ValueError("out must hold nvec*rows values")
-    _check(load().q1_0_gemm_small(_dev(packed, "packed", (torch.uint8,)), rows, n, nvec,
+    _check(load().q1_0_gemm_small(_packed_ptr(packed, rows, n, "q1"), rows, n, nvec,
                                   _dev(q, "q", (torch.int8,)), _dev(d, "d", _SCALE_DTYPES),
                                   _dev(out, "out", (torch.float32,)), _stream_ptr(stream)), "q1_0_gemm_small")
     return out

@@ -12,9 +12,21 @@ __device__ __forceinline__ int elem_of(int w, int pl, int i) {
   return 32 * (pl >> 1) + 4 * (w + 4 * (pl & 1)) + i;
 }
 
+// Per-call record of rejected input, in device memory the call allocates on
+// its stream: the smallest (row * nb + block) index of a block whose fp16
+// scale is Inf or NaN, and of a Q2_0 block holding the code 3 (all ones when
+// there is none).
+struct PackReject {
+  unsigned long long scale;
+  unsigned long long code;
+};
+
+__device__ __forceinline__ bool f16_nonfinite(uint16_t h) { return (h & 0x7c00u) == 0x7c00u; }
+
 // One thread per (padded row, padded block).
 __global__ void k_pack(const uint8_t* __restrict__ blocks, int64_t rows, int64_t nb, int64_t nbp,
-                       int64_t rows_pad, uint32_t* __restrict__ bits, uint16_t* __restrict__ scales) {
+                       int64_t rows_pad, uint32_t* __restrict__ bits, uint16_t* __restrict__ scales,
+                       PackReject* __restrict__ reject) {
   int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= rows_pad * nbp) return;
   int64_t r = idx / nbp, b = idx % nbp;
@@ -25,6 +37,7 @@ __global__ void k_pack(const uint8_t* __restrict__ blocks, int64_t rows, int64_t
   if (r < rows && b < nb) {
     const uint8_t* blk = blocks + (r * nb + b) * kBlockBytes;
     sc = uint16_t(blk[0] | (blk[1] << 8));
+    if (f16_nonfinite(sc)) atomicMin(&reject->scale, (unsigned long long)(r * nb + b));
     uint8_t qs[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) qs[j] = blk[2 + j];
@@ -76,11 +89,10 @@ __global__ void k_unpack(const uint32_t* __restrict__ bits, const uint16_t* __re
 
 // Q2_0: one thread per (padded row, padded block); codes 0/1/2 become the N
 // (weight -1) and P (+1) sign planes, each in the Q1_0 bit order.  A code 3
-// (not a weight) sets g_q2_bad_code and is packed as 0.
-static __device__ unsigned g_q2_bad_code = 0u;
-
+// (not a weight) is recorded in `reject` and packed as 0.
 __global__ void k_pack_q2(const uint8_t* __restrict__ blocks, int64_t rows, int64_t nb, int64_t nbp,
-                          int64_t rows_pad, uint32_t* __restrict__ bits, uint16_t* __restrict__ scales) {
+                          int64_t rows_pad, uint32_t* __restrict__ bits, uint16_t* __restrict__ scales,
+                          PackReject* __restrict__ reject) {
   int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= rows_pad * nbp) return;
   int64_t r = idx / nbp, b = idx % nbp;
@@ -91,6 +103,7 @@ __global__ void k_pack_q2(const uint8_t* __restrict__ blocks, int64_t rows, int6
   if (r < rows && b < nb) {
     const uint8_t* blk = blocks + (r * nb + b) * 34;
     sc = uint16_t(blk[0] | (blk[1] << 8));
+    if (f16_nonfinite(sc)) atomicMin(&reject->scale, (unsigned long long)(r * nb + b));
     uint8_t qs[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) qs[j] = blk[2 + j];
@@ -107,7 +120,7 @@ __global__ void k_pack_q2(const uint8_t* __restrict__ blocks, int64_t rows, int6
           nw[w] |= uint32_t(c == 0u) << (8 * i + pl);
           bad |= c == 3u;
         }
-    if (bad) atomicOr(&g_q2_bad_code, 1u);
+    if (bad) atomicMin(&reject->code, (unsigned long long)(r * nb + b));
   }
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
@@ -158,6 +171,38 @@ static int check_pack_args(const char* who, const void* blocks, int64_t rows, in
   return Q1_OK;
 }
 
+// Runs one pack kernel with a fresh reject record on `s`, waits for it, and
+// turns a recorded block into a Q1_ERR_ARG naming its row and block.  The
+// record is this call's own (stream-ordered allocation), so calls on other
+// threads or streams never see each other's findings.
+template <class Launch>
+static int pack_checked(const char* who, int64_t nb, cudaStream_t s, Launch&& launch) {
+  PackReject* rec = nullptr;
+  if (int e = cuda_status(cudaMallocAsync(reinterpret_cast<void**>(&rec), sizeof(PackReject), s), who)) return e;
+  int rc = cuda_status(cudaMemsetAsync(rec, 0xff, sizeof(PackReject), s), who);
+  if (rc == Q1_OK) {
+    launch(rec);
+    rc = cuda_status(cudaGetLastError(), who);
+  }
+  PackReject host = {~0ull, ~0ull};
+  if (rc == Q1_OK) rc = cuda_status(cudaMemcpyAsync(&host, rec, sizeof host, cudaMemcpyDeviceToHost, s), who);
+  const int rf = cuda_status(cudaFreeAsync(rec, s), who);
+  // The products may read packed weights before the kernel that precedes them
+  // on a stream has finished, so packing completes before the call returns;
+  // the reject record needs the wait too.
+  const int rs = cuda_status(cudaStreamSynchronize(s), who);
+  if (rc != Q1_OK) return rc;
+  if (rf != Q1_OK) return rf;
+  if (rs != Q1_OK) return rs;
+  if (host.scale != ~0ull)
+    return fail(Q1_ERR_ARG, "%s: row %lld block %lld: the fp16 weight scale is not finite", who,
+                (long long)(host.scale / nb), (long long)(host.scale % nb));
+  if (host.code != ~0ull)
+    return fail(Q1_ERR_ARG, "%s: row %lld block %lld holds the code 3, which is not a ternary weight", who,
+                (long long)(host.code / nb), (long long)(host.code % nb));
+  return Q1_OK;
+}
+
 }  // namespace q1
 
 using namespace q1;
@@ -170,12 +215,10 @@ extern "C" int q1_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* p
   int64_t total = L.rows_pad * L.nbp;
   int threads = 256;
   int64_t grid = (total + threads - 1) / threads;
-  k_pack<<<dim3(unsigned(grid)), threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales);
-  if (int e = cuda_status(cudaGetLastError(), "q1_0_pack launch")) return e;
-  // The products may read packed weights before the kernel that precedes them
-  // on a stream has finished, so packing completes before this call returns.
-  return cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "q1_0_pack");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return pack_checked("q1_0_pack", L.nb, s, [&](PackReject* rec) {
+    k_pack<<<dim3(unsigned(grid)), threads, 0, s>>>(blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales, rec);
+  });
 }
 
 extern "C" int q1_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t* blocks, void* stream) {
@@ -194,8 +237,6 @@ extern "C" int q1_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t*
 
 extern "C" int q2_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* packed, void* stream) {
   if (int e = check_pack_args("q2_0_pack", blocks, rows, n, packed)) return e;
-  const unsigned zero = 0;
-  if (int e = cuda_status(cudaMemcpyToSymbol(g_q2_bad_code, &zero, sizeof zero), "q2_0_pack")) return e;
   Layout L = layout_q2(rows, n);
   uint32_t* bits = static_cast<uint32_t*>(packed);
   uint16_t* scales = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(packed) + L.bits_bytes);
@@ -203,14 +244,9 @@ extern "C" int q2_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* p
   int threads = 256;
   int64_t grid = (total + threads - 1) / threads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  k_pack_q2<<<dim3(unsigned(grid)), threads, 0, s>>>(blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales);
-  if (int e = cuda_status(cudaGetLastError(), "q2_0_pack launch")) return e;
-  // Synchronous for the same reason as q1_0_pack; the code check needs it too.
-  if (int e = cuda_status(cudaStreamSynchronize(s), "q2_0_pack")) return e;
-  unsigned bad = 0;
-  if (int e = cuda_status(cudaMemcpyFromSymbol(&bad, g_q2_bad_code, sizeof bad), "q2_0_pack")) return e;
-  if (bad) return fail(Q1_ERR_ARG, "q2_0_pack: a block holds the code 3, which is not a ternary weight");
-  return Q1_OK;
+  return pack_checked("q2_0_pack", L.nb, s, [&](PackReject* rec) {
+    k_pack_q2<<<dim3(unsigned(grid)), threads, 0, s>>>(blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales, rec);
+  });
 }
 
 extern "C" int q2_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t* blocks, void* stream) {

@@ -142,7 +142,8 @@ class DecodeSet:
     def _arrays(self, schedule):
         key = "_arr_" + schedule
         if not hasattr(self, key):
-            setattr(self, key, [binding.product_array([self._item(i) for i in g]) for g in self.groups(schedule)])
+            setattr(self, key, [binding.product_array([self._item(i) for i in g], fmt=self.fmt)
+                                for g in self.groups(schedule)])
         return getattr(self, key)
 
     def launches(self, schedule: str) -> int:

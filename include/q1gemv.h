@@ -34,8 +34,9 @@
  *     rejected argument or a CUDA error (nothing is enqueued after a rejected
  *     argument); q1_last_error() then names the call and the reason.
  *   - Activation scales must be finite.  With a non-finite activation scale
- *     the affected outputs are unspecified (never a fault).  Weight scales may
- *     be any fp16 value: non-finite ones propagate exactly as in the definition.
+ *     the affected outputs are unspecified (never a fault).  Weight scales
+ *     must be finite too: q1_0_pack and q2_0_pack reject a block whose fp16
+ *     scale is Inf or NaN (Q1_ERR_ARG naming its row and block).
  */
 #ifndef Q1GEMV_H
 #define Q1GEMV_H
@@ -72,7 +73,12 @@ int64_t q1_0_packed_bytes(int64_t rows, int64_t n);
  *            Only 2-byte alignment is required for this pointer.
  *   packed : device, q1_0_packed_bytes(rows, n) bytes, written entirely.
  * Synchronous: returns after `stream` has finished the packing (see q1_0_gemv).
- * Errors: Q1_ERR_ARG for a bad shape or pointer; Q1_ERR_CUDA on launch failure. */
+ * Errors: Q1_ERR_ARG for a bad shape or pointer, or when some block's fp16
+ * scale is Inf or NaN (the message names the first such row and block; the
+ * packed buffer must then not be used); Q1_ERR_CUDA on a failed launch or
+ * copy.  The check uses a few bytes of device memory allocated on `stream`
+ * for this call alone, so concurrent calls on other streams or threads do not
+ * interfere. */
 int q1_0_pack(const uint8_t *blocks, int64_t rows, int64_t n, void *packed, void *stream);
 
 /* Inverse of q1_0_pack: writes rows*(n/128) 18-byte blocks identical to the
@@ -165,7 +171,10 @@ typedef struct q1_multi_plan {
 int q1_0_gemv_multi_plan(const q1_product *products, int count, int sms, q1_multi_plan *plan, int64_t *cuts,
                          int max_cuts);
 
-/* Small-batch product: the matrix-vector product for each of nvec activation
+/* Small-batch product ("kernels.rs -- the Q1_0 kernels", second bullet: each
+ * lane's chain over the blocks is independent of every other chain, so one
+ * stream of the weights serves several activation vectors, each vector's
+ * chains kept apart): the matrix-vector product for each of nvec activation
  * vectors sharing one pass over the weights (1 <= nvec <= 64).
  *   q : device int8 [nvec][n]; d : device fp16 bits [nvec][n/32];
  *   out : device f32 [nvec][rows] (row-major per vector).
@@ -198,8 +207,10 @@ int64_t q2_0_packed_bytes(int64_t rows, int64_t n);
  *   blocks : device, rows*(n/128) consecutive 34-byte blocks, row-major, as
  *            above; only 2-byte alignment is required.
  *   packed : device, q2_0_packed_bytes(rows, n) bytes, written entirely.
- * Synchronous.  Returns Q1_ERR_ARG if any element holds the code 3 (the buffer
- * is then written with those elements as 0), or for a bad shape or pointer. */
+ * Synchronous.  Returns Q1_ERR_ARG if any element holds the code 3 or any
+ * block's fp16 scale is Inf or NaN (the message names the first such row and
+ * block; the packed buffer must then not be used), or for a bad shape or
+ * pointer.  Like q1_0_pack, the check uses device memory of this call alone. */
 int q2_0_pack(const uint8_t *blocks, int64_t rows, int64_t n, void *packed, void *stream);
 
 /* Inverse of q2_0_pack: writes rows*(n/128) 34-byte blocks identical to the

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from decode_q1_gemv_gb300 import binding, build
 
@@ -356,3 +357,51 @@ def test_q2_null_pointers_rejected_on_host(lib):
     assert lib.q2_0_pack(None, 32, 128, None, None) == binding.Q1_ERR_ARG
     assert lib.q2_0_gemv(None, 32, 128, None, None, None, None) == binding.Q1_ERR_ARG
     assert lib.q2_0_gemv_multi(None, 1, None) == binding.Q1_ERR_ARG
+
+
+# ------------------------------------- binding: packed sizes checked first --
+def _short(nbytes):
+    return torch.empty(nbytes - 1, dtype=torch.uint8)
+
+
+@pytest.mark.parametrize("call", ["gemv", "q2_gemv", "gemm_small", "unpack", "q2_unpack", "multi_q1", "multi_q2"])
+def test_binding_rejects_short_packed_buffers_before_launch(lib, call):
+    """Every binding call that takes a packed weight buffer checks its size
+    against the format's packed size for (rows, n) before anything reaches the
+    library: the kernels would read past a short buffer."""
+
+    rows, n = 300, 1024
+    q = torch.zeros(n, dtype=torch.int8)
+    d = torch.zeros(n // 32, dtype=torch.int16)
+    out = torch.zeros(rows)
+    p1 = _short(binding.packed_bytes(rows, n))
+    p2 = _short(binding.q2_packed_bytes(rows, n))
+    with pytest.raises(ValueError, match="needs"):
+        if call == "gemv":
+            binding.gemv(p1, rows, n, q, d, out)
+        elif call == "q2_gemv":
+            binding.q2_gemv(p2, rows, n, q, d, out)
+        elif call == "gemm_small":
+            binding.gemm_small(p1, rows, n, q[None, :], d[None, :], out[None, :])
+        elif call == "unpack":
+            binding.unpack(p1, rows, n, torch.zeros((rows, n // 128, 18), dtype=torch.uint8))
+        elif call == "q2_unpack":
+            binding.q2_unpack(p2, rows, n, torch.zeros((rows, n // 128, 34), dtype=torch.uint8))
+        elif call == "multi_q1":
+            binding.product_array([(p1, rows, n, None, q, d, out)])
+        else:
+            binding.product_array([(p2, rows, n, None, q, d, out)], fmt="q2")
+
+
+def test_binding_rejects_q1_buffer_for_q2_products(lib):
+    """A Q1_0-packed buffer is about half the Q2_0 size: a Q2_0 product list
+    naming it is refused on the host."""
+
+    rows, n = 4096, 4096
+    p1 = torch.empty(binding.packed_bytes(rows, n), dtype=torch.uint8)
+    q = torch.zeros(n, dtype=torch.int8)
+    d = torch.zeros(n // 32, dtype=torch.int16)
+    with pytest.raises(ValueError, match="Q2_0"):
+        binding.product_array([(p1, rows, n, None, q, d, torch.zeros(rows))], fmt="q2")
+    with pytest.raises(ValueError, match="fmt"):
+        binding.product_array([(p1, rows, n, None, q, d, torch.zeros(rows))], fmt="q3")

@@ -102,6 +102,38 @@ def test_pack_unpack_round_trip(rows, n):
     assert np.array_equal(back, blocks)
 
 
+@pytest.mark.parametrize("bad", [0x7C00, 0xFC00, 0x7E00, 0x7C01])
+def test_pack_rejects_non_finite_scale(bad):
+    """A block whose fp16 scale is +Inf, -Inf or NaN is rejected with an
+    error naming the first such row and block (in row-major block order)."""
+    rows, n = 300, 1024
+    blocks = synth.weight_blocks(synth.rng_for(103), rows, n)
+    for r, b in ((211, 5), (17, 6), (17, 2)):
+        blocks[r, b, 0], blocks[r, b, 1] = bad & 0xFF, bad >> 8
+    with pytest.raises(binding.Q1Error, match="row 17 block 2: the fp16 weight scale is not finite"):
+        binding.pack(dev(blocks), rows, n)
+    # the rejection belongs to that call only
+    ok = synth.weight_blocks(synth.rng_for(104), rows, n)
+    binding.pack(dev(ok), rows, n)
+
+
+def test_pack_rejections_stay_per_call_across_streams():
+    """Packs of a bad and a good matrix issued from two streams at once: the
+    bad one is rejected and the good one is not."""
+    rows, n = 4096, 4096
+    bad = synth.weight_blocks(synth.rng_for(105), rows, n)
+    bad[4000, 31, 1] = 0x7C
+    bad[4000, 31, 0] = 0x00
+    good = synth.weight_blocks(synth.rng_for(106), rows, n)
+    bd, gd = dev(bad), dev(good)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        with pytest.raises(binding.Q1Error, match="row 4000 block 31"):
+            binding.pack(bd, rows, n, stream=s1)
+        packed = binding.pack(gd, rows, n, stream=s2)
+        assert np.array_equal(binding.unpack(packed, rows, n).cpu().numpy(), good)
+
+
 # ---------------------------------------------------------- quantization --
 @pytest.mark.parametrize("case", ["normal", "outliers", "tiny", "large", "zeros", "ties"])
 def test_quantize_parity(case):
@@ -236,24 +268,16 @@ def test_gemm_small_columns_equal_gemv():
         assert np.array_equal(outb[v].view(np.uint32), outv.view(np.uint32))
 
 
-def _sampled(blocks, q, d, count, rng):
-    nvec, rows = q.shape[0], blocks.shape[0]
-    idx = rng.integers(0, rows, size=count)
-    idx[:4] = [0, rows - 1, rows // 2, 31 % rows]
-    vec = rng.integers(0, nvec, size=count)
-    vec[:2] = [0, nvec - 1]
-    return idx, vec, oracle.rows_sampled(blocks, idx, q, d, vec)
-
-
 @pytest.mark.parametrize("rows,n,nvec,scale", [
     (14336, 4096, 16, "halfnormal"),
     (4096, 14336, 16, "halfnormal"),
     (128256, 4096, 64, "lognormal"),
     (4096, 14336, 64, "lognormal"),
 ])
-def test_batched_full_size_sampled(rows, n, nvec, scale):
+def test_batched_full_size(rows, n, nvec, scale):
     """Multi-sequence (16 vectors) and prefill-chunk (64 vectors, log-normal
-    block scales) products at full size: 3000 sampled outputs vs the oracle."""
+    block scales) products at full size: every output against the threaded
+    oracle (gpu.md, "How it is verified": every row of every shape)."""
     rng = synth.rng_for(4 if nvec == 16 else 5, rows, n)
     blocks = synth.weight_blocks(rng, rows, n, scale)
     x = synth.activations(rng, nvec, n)
@@ -263,8 +287,7 @@ def test_batched_full_size_sampled(rows, n, nvec, scale):
     qh, dh = q.cpu().numpy(), d.cpu().numpy().view(np.uint16)
     want_q, want_d = oracle.q8_quantize(x)
     assert np.array_equal(qh, want_q) and np.array_equal(dh, want_d)
-    idx, vec, want = _sampled(blocks, want_q, want_d, 3000, rng)
-    bits_equal(out[vec, idx], want)
+    bits_equal(out, oracle.gemm_threaded(blocks, want_q, want_d))
 
 
 # ----------------------------------------------------- multi-product call --
@@ -375,36 +398,40 @@ def decode_set():
     return DecodeSet(seed=3)
 
 
+@pytest.fixture(scope="module")
+def decode_set_expected(decode_set):
+    """Every output of the decode set from the threaded oracle, with the q8_0
+    quants and scales of every activation: per product (out, q, d)."""
+    ds = decode_set
+    exp = []
+    for i in range(len(ds.shapes)):
+        want_q, want_d = oracle.q8_quantize(ds.host_x(i)[None, :])
+        want = oracle.gemm_threaded(ds.host_blocks(i), want_q, want_d)[0]
+        exp.append((want, want_q[0], want_d[0]))
+    return exp
+
+
 @pytest.mark.parametrize("schedule", ["set", "grouped", "decode", "separate"])
-def test_decode_set_graph_sampled(decode_set, schedule):
+def test_decode_set_graph_full(decode_set, decode_set_expected, schedule):
     """The full 225-product Llama-3-8B-shaped decode set, run exactly as the
     benchmark runs it (one CUDA graph per schedule, programmatic dependent
-    launch), with 24 sampled rows of products of every shape compared against
-    the oracle."""
+    launch): every output of every product against the oracle, bit for bit
+    (gpu.md, "How it is verified": every row of every shape)."""
     ds = decode_set
     g = ds.capture(schedule)
     ds.out_all.fill_(float("nan"))
     g.replay()
     g.replay()
     torch.cuda.synchronize()
-    for i in range(len(ds.shapes)):  # every row of every product written
-        assert not torch.isnan(ds.out[i]).any().item(), ds.shapes[i][0]
-    rng = np.random.default_rng(len(schedule))
-    picks = [0, 1, 2, 3, 4, 5, 6, 7 * 17 + 1, 7 * 31 + 4, 7 * 31 + 6, len(ds.shapes) - 1]
-    for i in picks:
-        name, rows, n = ds.shapes[i]
-        blocks = ds.host_blocks(i)
-        x = ds.host_x(i)
-        want_q, want_d = oracle.q8_quantize(x[None, :])
-        idx = rng.integers(0, rows, size=24)
-        idx[:2] = [0, rows - 1]
-        want = oracle.rows_sampled(blocks, idx, want_q[0], want_d[0])
-        got = ds.out[i].cpu().numpy()
+    got_all = ds.out_all.cpu().numpy()
+    for i, (name, rows, n) in enumerate(ds.shapes):
+        want, want_q, want_d = decode_set_expected[i]
+        got = got_all[ds.out_off[i]:ds.out_off[i] + rows]
         assert not np.any(np.isnan(got)), name
-        bits_equal(got[idx], want)
+        bits_equal(got, want)
         if schedule == "separate":
-            assert np.array_equal(ds.q[i].cpu().numpy(), want_q[0]), name
-            assert np.array_equal(ds.d[i].cpu().numpy().view(np.uint16), want_d[0]), name
+            assert np.array_equal(ds.q[i].cpu().numpy(), want_q), name
+            assert np.array_equal(ds.d[i].cpu().numpy().view(np.uint16), want_d), name
 
 
 # ---------------------------------------------------- edge and error cases --

@@ -4,7 +4,7 @@ The format and its row product are this library's reading of the pages'
 Q2_0 (bankML "docs/modules/gpu.md", "Advantages and efficiency" and
 "Limitations" name it without defining it): 34-byte blocks of an fp16 scale
 and 2-bit codes 0/1/2 = -1/0/+1, and the Q1_0 chain over ternary lane sums.
-Outputs are compared bit for bit with oracle.q2_gemv / q2_rows_sampled.
+Every output is compared bit for bit with oracle.q2_gemv / q2_gemv_threaded.
 """
 import numpy as np
 import pytest
@@ -50,10 +50,19 @@ def test_pack_rejects_code_three():
     rows, n = 40, 256
     tb = synth.ternary_blocks(synth.rng_for(402), rows, n)
     tb[7, 1, 5] |= 0x30  # element 4*3+2 = 14 of block 1 of row 7 gets code 3
-    with pytest.raises(binding.Q1Error, match="code 3"):
+    tb[30, 0, 9] |= 0x0C
+    with pytest.raises(binding.Q1Error, match="row 7 block 1 holds the code 3"):
         binding.q2_pack(dev(tb), rows, n)
     ok = synth.ternary_blocks(synth.rng_for(403), rows, n)
-    binding.q2_pack(dev(ok), rows, n)  # the flag does not stick to the next call
+    binding.q2_pack(dev(ok), rows, n)  # the rejection does not stick to the next call
+
+
+def test_pack_rejects_non_finite_scale():
+    rows, n = 40, 256
+    tb = synth.ternary_blocks(synth.rng_for(404), rows, n)
+    tb[12, 1, 0], tb[12, 1, 1] = 0x00, 0xFE   # NaN
+    with pytest.raises(binding.Q1Error, match="row 12 block 1: the fp16 weight scale is not finite"):
+        binding.q2_pack(dev(tb), rows, n)
 
 
 @pytest.mark.parametrize("rows,n", [(1, 128), (7, 256), (33, 384), (300, 1024), (1000, 4096), (513, 14336),
@@ -131,9 +140,9 @@ def test_gemv_multi_products(size):
 
 
 @pytest.mark.parametrize("rows,n", [(14336, 4096), (4096, 14336), (128256, 4096)])
-def test_full_size_sampled(rows, n):
-    """Llama-3-8B shapes in Q2_0 as the set benchmark draws them: 2000 sampled
-    rows (first and last included) against the oracle."""
+def test_full_size(rows, n):
+    """Llama-3-8B shapes in Q2_0 as the set benchmark draws them: every row
+    against the threaded oracle."""
     rng = synth.rng_for(430, rows, n)
     tb = synth.ternary_blocks_fast(rng, rows, n)
     x = synth.activations(rng, 1, n)
@@ -141,9 +150,26 @@ def test_full_size_sampled(rows, n):
     packed = binding.q2_pack(dev(tb), rows, n)
     out = torch.empty(rows, device="cuda")
     binding.q2_gemv_multi([(packed, rows, n, dev(x[0]), None, None, out)])
-    idx = rng.integers(0, rows, size=2000)
-    idx[:2] = [0, rows - 1]
-    bits_equal(out.cpu().numpy()[idx], oracle.q2_rows_sampled(tb, idx, q[0], d[0]))
+    bits_equal(out.cpu().numpy(), oracle.q2_gemv_threaded(tb, q[0], d[0]))
+
+
+def test_q2_decode_set_full():
+    """The 225-product decode set with Q2_0 weights in one launch, as the
+    benchmark times it (CUDA graph): every output of every product against the
+    threaded oracle."""
+    from decode_q1_gemv_gb300.decode_set import DecodeSet
+    ds = DecodeSet(seed=3, fmt="q2")
+    g = ds.capture("set")
+    ds.out_all.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    got_all = ds.out_all.cpu().numpy()
+    for i, (name, rows, n) in enumerate(ds.shapes):
+        q, d = oracle.q8_quantize(ds.host_x(i)[None, :])
+        want = oracle.q2_gemv_threaded(ds.host_blocks(i), q[0], d[0])
+        bits_equal(got_all[ds.out_off[i]:ds.out_off[i] + rows], want)
+    del ds, g
+    torch.cuda.empty_cache()
 
 
 def test_device_status_clean():
