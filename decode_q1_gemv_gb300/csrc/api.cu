@@ -47,8 +47,9 @@ extern "C" int64_t q2_0_packed_bytes(int64_t rows, int64_t n) {
 }
 
 extern "C" int q1_device_status(int clear) {
-  unsigned v = 0, u = 0;
+  unsigned v = 0, u = 0, t = 0;
   if (int e = q1::status_word_dp4a(&v, clear)) return e;
   if (int e = q1::status_word_prod(&u, clear)) return e;
-  return int(v | u);
+  if (int e = q1::status_word_tc(&t, clear)) return e;
+  return int(v | u | t);
 }

@@ -110,6 +110,13 @@ int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, con
 // Device status word of the product kernels (read and optionally cleared).
 int status_word_dp4a(unsigned* v, int clear);
 int status_word_prod(unsigned* v, int clear);
+int status_word_tc(unsigned* v, int clear);
+// The batched product on the tensor core (tcprod.cu): scratch bytes it needs
+// for n and nvec, and the launch (a prologue kernel and the product kernel)
+// with that scratch in device memory owned by the caller of launch_tc.
+int64_t tc_scratch_bytes(int64_t n, int64_t nvec);
+int launch_tc(const void* packed, int64_t rows, int64_t n, int64_t nvec, const int8_t* q, const uint16_t* d,
+              float* out, uint8_t* scratch, cudaStream_t s, const char* who);
 
 }  // namespace q1
 

@@ -228,11 +228,31 @@ static ProdArgs make_args(const void* packed, int64_t rows, int64_t n, int64_t n
 
 using namespace q1;
 
+// Vector counts from which the tensor-core kernel (tcprod.cu) takes the
+// product, and the largest scratch it may ask for (records of 8 KB per block
+// and group of 16 vectors: up to 64 MB at n = 2^20 and 64 vectors).
+constexpr int64_t kTcMinVectors = 8;
+constexpr int64_t kTcMaxScratch = int64_t(64) << 20;
+
 extern "C" int q1_0_gemm_small(const void* packed, int64_t rows, int64_t n, int64_t nvec, const int8_t* q,
                                const uint16_t* d, float* out, void* stream) {
   if (int e = check_prod_args("q1_0_gemm_small", packed, rows, n, nvec, q, d, out)) return e;
-  ProdArgs a = make_args(packed, rows, n, nvec, q, d, out);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t scratch_bytes = tc_scratch_bytes(n, nvec);
+  if (nvec >= kTcMinVectors && scratch_bytes <= kTcMaxScratch) {
+    // The scratch lives for this call only (stream-ordered allocation), so
+    // calls on different streams never share it.
+    uint8_t* scratch = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), size_t(scratch_bytes), s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return fail(Q1_ERR_NOMEM, "q1_0_gemm_small: could not allocate %lld bytes of scratch on the stream",
+                  (long long)scratch_bytes);
+    }
+    const int rc = launch_tc(packed, rows, n, nvec, q, d, out, scratch, s, "q1_0_gemm_small launch");
+    const int rf = cuda_status(cudaFreeAsync(scratch, s), "q1_0_gemm_small");
+    return rc != Q1_OK ? rc : rf;
+  }
+  ProdArgs a = make_args(packed, rows, n, nvec, q, d, out);
   const int64_t panels = a.panels;
   // Four rows per thread amortize each activation-table load over four rows
   // (one row per thread leaves the loop bound by shared-memory loads).  Four
