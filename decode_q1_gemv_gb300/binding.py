@@ -33,7 +33,7 @@ Q1_MISMATCH = 2
 EXPORTS = ("q1_last_error", "q1_0_packed_bytes", "q1_0_pack", "q1_0_unpack", "q8_quantize_act",
            "q1_0_gemv", "q1_0_gemv_multi", "q1_0_gemv_multi_plan", "q1_0_gemm_small", "q1_0_verify",
            "q1_device_status", "q2_0_packed_bytes", "q2_0_pack", "q2_0_unpack", "q2_0_gemv", "q2_0_gemv_multi",
-           "q2_0_gemv_multi_plan")
+           "q2_0_gemv_multi_plan", "q1_gemm_small_kernel")
 
 MAX_PRODUCTS = 256
 
@@ -108,6 +108,8 @@ def load():
         lib.q2_0_gemv_multi.restype = I
         lib.q1_0_gemm_small.argtypes = [P, I64, I64, I64, P, P, P, P]
         lib.q1_0_gemm_small.restype = I
+        lib.q1_gemm_small_kernel.argtypes = [I]
+        lib.q1_gemm_small_kernel.restype = I
         lib.q1_device_status.argtypes = [I]
         lib.q1_device_status.restype = I
         lib.q1_0_verify.argtypes = [I, ctypes.c_char_p, ctypes.c_size_t]
@@ -343,6 +345,20 @@ def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torc
                                   _dev(q, "q", (torch.int8,)), _dev(d, "d", _SCALE_DTYPES),
                                   _dev(out, "out", (torch.float32,)), _stream_ptr(stream)), "q1_0_gemm_small")
     return out
+
+
+GEMM_KERNELS = {"auto": 0, "dp4a": 1, "tensor": 2}
+
+
+def gemm_small_kernel(choice: str) -> str:
+    """Select the kernel of gemm_small for the calls that follow in this
+    process ("auto", "dp4a" or "tensor"); returns the previous choice."""
+    if choice not in GEMM_KERNELS:
+        raise ValueError(f"choice must be one of {sorted(GEMM_KERNELS)}")
+    prev = load().q1_gemm_small_kernel(GEMM_KERNELS[choice])
+    if prev < 0:
+        raise Q1Error(prev, last_error())
+    return {v: k for k, v in GEMM_KERNELS.items()}[prev]
 
 
 def device_status(clear: bool = True) -> int:

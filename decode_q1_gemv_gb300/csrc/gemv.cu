@@ -11,6 +11,8 @@
 // kProdStages shared-memory stages that one thread keeps filled, so the
 // weight loads' latency is hidden without holding the next quad in registers.
 #include <algorithm>
+#include <atomic>
+#include <cmath>
 
 #include "table.cuh"
 
@@ -228,22 +230,81 @@ static ProdArgs make_args(const void* packed, int64_t rows, int64_t n, int64_t n
 
 using namespace q1;
 
+// The stream-ordered pool the batched product takes its per-call scratch
+// from, one per device.  Freed scratch stays in the pool for the next call
+// (release threshold: unlimited) instead of going back to the driver at every
+// synchronization, which made each call pay a fresh allocation; the pool
+// holds at most the largest scratch of concurrently running calls.
+static int scratch_pool(cudaMemPool_t* out) {
+  static cudaMemPool_t pools[64] = {};
+  int dev = 0;
+  if (int e = cuda_status(cudaGetDevice(&dev), "q1_0_gemm_small")) return e;
+  if (dev < 0 || dev >= 64) return fail(Q1_ERR_ARG, "q1_0_gemm_small: device %d outside 0..63", dev);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t p = nullptr;
+    if (int e = cuda_status(cudaMemPoolCreate(&p, &props), "q1_0_gemm_small: cudaMemPoolCreate")) return e;
+    uint64_t keep = ~uint64_t(0);
+    if (int e = cuda_status(cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep),
+                            "q1_0_gemm_small: cudaMemPoolSetAttribute"))
+      return e;
+    pools[dev] = p;
+  }
+  *out = pools[dev];
+  return Q1_OK;
+}
+
+// Which kernel is faster for a product, from a cost model of both measured on
+// a GB300 (cold L2, one launch between events; 14336x4096 to 128256x4096,
+// 8 to 64 vectors): the tensor-core kernel keeps one 128-row x 16-vector
+// unit per SM in flight at about 0.94 us per block of 128 weights, plus
+// about 12 us of prologue and ramp; the dp4a kernel streams about 2.2e13
+// weight-vector products per second plus about 5 us.
+static bool tc_faster(int64_t rows, int64_t n, int64_t nvec) {
+  const double sms = double(num_sms());
+  const double units = double((rows + 127) / 128) * double((nvec + 15) / 16);
+  const double waves = std::ceil(units / sms);
+  const double t_tc = waves * double(n / kBlock) * 0.94 + 12.0;
+  const double t_dp4a = double(rows) * double(n) * double(nvec) / 2.2e7 + 5.0;
+  return t_tc < t_dp4a;
+}
+
 // Vector counts from which the tensor-core kernel (tcprod.cu) takes the
 // product, and the largest scratch it may ask for (records of 8 KB per block
 // and group of 16 vectors: up to 64 MB at n = 2^20 and 64 vectors).
 constexpr int64_t kTcMinVectors = 8;
 constexpr int64_t kTcMaxScratch = int64_t(64) << 20;
 
+// Kernel choice of q1_0_gemm_small (q1_gemm_small_kernel): 0 automatic, 1 dp4a,
+// 2 tensor core.
+static std::atomic<int> g_kernel_choice{0};
+
+extern "C" int q1_gemm_small_kernel(int choice) {
+  if (choice < 0 || choice > 2) return fail(Q1_ERR_ARG, "q1_gemm_small_kernel: choice %d outside 0..2", choice);
+  return g_kernel_choice.exchange(choice);
+}
+
 extern "C" int q1_0_gemm_small(const void* packed, int64_t rows, int64_t n, int64_t nvec, const int8_t* q,
                                const uint16_t* d, float* out, void* stream) {
   if (int e = check_prod_args("q1_0_gemm_small", packed, rows, n, nvec, q, d, out)) return e;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t scratch_bytes = tc_scratch_bytes(n, nvec);
-  if (nvec >= kTcMinVectors && scratch_bytes <= kTcMaxScratch) {
-    // The scratch lives for this call only (stream-ordered allocation), so
-    // calls on different streams never share it.
+  const int choice = g_kernel_choice.load();
+  if (choice == 2 && scratch_bytes > kTcMaxScratch)
+    return fail(Q1_ERR_ARG, "q1_0_gemm_small: the tensor-core kernel would need %lld bytes of scratch (limit %lld)",
+                (long long)scratch_bytes, (long long)kTcMaxScratch);
+  const bool tc = choice == 2 || (choice == 0 && nvec >= kTcMinVectors && scratch_bytes <= kTcMaxScratch &&
+                                  tc_faster(rows, n, nvec));
+  if (tc) {
+    // The scratch lives for this call only (stream-ordered allocation from
+    // the library's pool), so calls on different streams never share it.
     uint8_t* scratch = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), size_t(scratch_bytes), s) != cudaSuccess) {
+    cudaMemPool_t pool = nullptr;
+    if (int e = scratch_pool(&pool)) return e;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), size_t(scratch_bytes), pool, s) != cudaSuccess) {
       (void)cudaGetLastError();
       return fail(Q1_ERR_NOMEM, "q1_0_gemm_small: could not allocate %lld bytes of scratch on the stream",
                   (long long)scratch_bytes);

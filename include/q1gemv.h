@@ -182,6 +182,21 @@ int q1_0_gemv_multi_plan(const q1_product *products, int count, int sms, q1_mult
 int q1_0_gemm_small(const void *packed, int64_t rows, int64_t n, int64_t nvec, const int8_t *q,
                     const uint16_t *d, float *out, void *stream);
 
+/* Which kernel q1_0_gemm_small runs, for every call that follows in this
+ * process (no counterpart in the pages: a tuning and testing knob).  Both
+ * kernels give identical bits.
+ *   choice : 0 = automatic (the default): from 8 vectors up, a cost model
+ *            measured on a GB300 picks the faster of the two for the shape;
+ *            1 = the dp4a kernel (CUDA cores) always;
+ *            2 = the tensor-core kernel always (an f16 MMA gives each lane's
+ *            sub-block chain in one exact f32 accumulator where an activation
+ *            bound allows it, the dp4a chain elsewhere; it takes a per-call
+ *            scratch of about 8 KB per 128 weights of n per 16 vectors from
+ *            a pool the library keeps per device, and rejects shapes needing
+ *            more than 64 MB).
+ * Returns the previous choice, or Q1_ERR_ARG for another value. */
+int q1_gemm_small_kernel(int choice);
+
 /* ---------------------------------------------------------------------------
  * Q2_0 (ternary) weights: the sibling format the pages name as the next GPU
  * kernel ("Advantages and efficiency", where optimization goes next;
