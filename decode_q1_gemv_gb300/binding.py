@@ -33,7 +33,7 @@ Q1_MISMATCH = 2
 EXPORTS = ("q1_last_error", "q1_0_packed_bytes", "q1_0_pack", "q1_0_unpack", "q8_quantize_act",
            "q1_0_gemv", "q1_0_gemv_multi", "q1_0_gemv_multi_plan", "q1_0_gemm_small", "q1_0_verify",
            "q1_device_status", "q2_0_packed_bytes", "q2_0_pack", "q2_0_unpack", "q2_0_gemv", "q2_0_gemv_multi",
-           "q2_0_gemv_multi_plan", "q1_gemm_small_kernel")
+           "q2_0_gemv_multi_plan", "q1_gemm_small_kernel", "q1_0_gemm_small_noalloc")
 
 MAX_PRODUCTS = 256
 
@@ -108,6 +108,8 @@ def load():
         lib.q2_0_gemv_multi.restype = I
         lib.q1_0_gemm_small.argtypes = [P, I64, I64, I64, P, P, P, P]
         lib.q1_0_gemm_small.restype = I
+        lib.q1_0_gemm_small_noalloc.argtypes = [P, I64, I64, I64, P, P, P, P]
+        lib.q1_0_gemm_small_noalloc.restype = I
         lib.q1_gemm_small_kernel.argtypes = [I]
         lib.q1_gemm_small_kernel.restype = I
         lib.q1_device_status.argtypes = [I]
@@ -344,6 +346,24 @@ def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torc
     _check(load().q1_0_gemm_small(_packed_ptr(packed, rows, n, "q1"), rows, n, nvec,
                                   _dev(q, "q", (torch.int8,)), _dev(d, "d", _SCALE_DTYPES),
                                   _dev(out, "out", (torch.float32,)), _stream_ptr(stream)), "q1_0_gemm_small")
+    return out
+
+
+def gemm_small_noalloc(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tensor,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gemm_small through q1_0_gemm_small_noalloc: the tensor-core kernel with
+    the library's fixed scratch array, no allocation (see include/q1gemv.h)."""
+    nvec = q.numel() // n
+    if q.numel() != nvec * n or d.numel() != nvec * (n // 32):
+        raise ValueError("q must be [nvec, n] and d [nvec, n/32]")
+    if out is None:
+        out = torch.empty((nvec, rows), dtype=torch.float32, device=q.device)
+    if out.numel() != nvec * rows:
+        raise ValueError("out must hold nvec*rows values")
+    _check(load().q1_0_gemm_small_noalloc(_packed_ptr(packed, rows, n, "q1"), rows, n, nvec,
+                                          _dev(q, "q", (torch.int8,)), _dev(d, "d", _SCALE_DTYPES),
+                                          _dev(out, "out", (torch.float32,)), _stream_ptr(stream)),
+           "q1_0_gemm_small_noalloc")
     return out
 
 

@@ -59,6 +59,7 @@
 // before it).  Every wait is bounded; a wait that gives up raises a CTA-wide
 // abort flag and the device status word, and every role winds down.
 #include <algorithm>
+#include <mutex>
 #include <cuda_fp16.h>
 
 #include "table.cuh"
@@ -599,3 +600,60 @@ int launch_tc(const void* packed, int64_t rows, int64_t n, int64_t nvec, const i
 }
 
 }  // namespace q1
+
+// ------------------------------------------- allocation-free batched call --
+// q1_0_gemm_small_noalloc: the tensor-core batched product with its scratch
+// (the prologue's flags and B records) in one array that lives in this
+// library's own device memory from load to exit, for callers that cannot
+// allocate device memory while they run (see q1gemv.h).
+namespace q1 {
+
+constexpr int64_t kNoAllocScratchBytes = int64_t(8) << 20;  // 8 MiB on every device that loads the library
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array on the current device.  The host-side name of a
+// __device__ array is only a handle: the address a kernel may use comes from
+// cudaGetSymbolAddress with that device current, looked up once per device.
+static int noalloc_scratch(uint8_t** out) {
+  static std::mutex lock;
+  static uint8_t* addr[64] = {};
+  int dev = 0;
+  if (int e = cuda_status(cudaGetDevice(&dev), "q1_0_gemm_small_noalloc")) return e;
+  if (dev < 0 || dev >= 64) return fail(Q1_ERR_ARG, "q1_0_gemm_small_noalloc: device %d outside 0..63", dev);
+  std::lock_guard<std::mutex> g(lock);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (int e = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_scratch),
+                            "q1_0_gemm_small_noalloc: cudaGetSymbolAddress"))
+      return e;
+    addr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = addr[dev];
+  return Q1_OK;
+}
+
+}  // namespace q1
+
+extern "C" int q1_0_gemm_small_noalloc(const void* packed, int64_t rows, int64_t n, int64_t nvec, const int8_t* q,
+                                       const uint16_t* d, float* out, void* stream) {
+  using namespace q1;
+  const char* who = "q1_0_gemm_small_noalloc";
+  if (rows < 1 || rows > (int64_t(1) << 26) || n < 128 || n > (int64_t(1) << 24) || n % 128)
+    return fail(Q1_ERR_ARG, "%s: bad shape rows=%lld n=%lld", who, (long long)rows, (long long)n);
+  if (nvec < 1 || nvec > 64) return fail(Q1_ERR_ARG, "%s: nvec=%lld outside 1..64", who, (long long)nvec);
+  if (!packed || !q || !d || !out) return fail(Q1_ERR_ARG, "%s: null pointer", who);
+  if (reinterpret_cast<uintptr_t>(packed) % 16 || reinterpret_cast<uintptr_t>(q) % 16 ||
+      reinterpret_cast<uintptr_t>(d) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(Q1_ERR_ARG, "%s: buffers must be 16-byte aligned", who);
+  const int64_t need = tc_scratch_bytes(n, nvec);
+  if (need > kNoAllocScratchBytes)
+    return fail(Q1_ERR_ARG,
+                "%s: n=%lld with %lld vectors needs %lld bytes of scratch; the fixed scratch holds %lld "
+                "(8 KB per 128 weights of n per group of 16 vectors)",
+                who, (long long)n, (long long)nvec, (long long)need, (long long)kNoAllocScratchBytes);
+  uint8_t* scratch = nullptr;
+  if (int e = noalloc_scratch(&scratch)) return e;
+  // Nothing in the scratch needs to start at zero: the prologue writes every
+  // flag and every record byte the product kernel reads before it reads them.
+  return launch_tc(packed, rows, n, nvec, q, d, out, scratch, static_cast<cudaStream_t>(stream), who);
+}

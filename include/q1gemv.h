@@ -197,6 +197,37 @@ int q1_0_gemm_small(const void *packed, int64_t rows, int64_t n, int64_t nvec, c
  * Returns the previous choice, or Q1_ERR_ARG for another value. */
 int q1_gemm_small_kernel(int choice);
 
+/* Small-batch product that allocates no device memory.  The pages have no
+ * counterpart: this is a service for callers, not part of the method.
+ *
+ * q1_0_gemm_small takes its tensor-core scratch from a memory pool at call
+ * time.  Some callers cannot allow that: a serving loop that reserves all
+ * device memory up front and forbids allocation on its decode path (an
+ * allocation can stall behind other device work, and fails when a
+ * framework's allocator already holds the memory), or a host whose memory
+ * accounting must see every byte the process uses.  This call runs the
+ * tensor-core kernel of q1_0_gemm_small with its scratch in one fixed array
+ * of 8 MiB that the library holds in every device's memory from load to
+ * process exit.  It calls no allocator.
+ *   Arguments, layout and outputs: as q1_0_gemm_small (1 <= nvec <= 64);
+ *   out[v][r] is bit-identical to q1_0_gemm_small's.
+ *   Limit: the scratch needs 8 KB per 128 weights of n for each group of 16
+ *   vectors, plus a few bytes; a larger n is rejected with Q1_ERR_ARG before
+ *   anything is enqueued (for example n <= 32640 with 33..64 vectors,
+ *   n <= 130944 with 1..16).
+ *   First call on a device: it looks up the device address of the array on
+ *   the current device (once per device); make that first call before any
+ *   stream capture.
+ *   Sharing: every call on a device uses the same array, and the array keeps
+ *   the last call's contents (nothing in it needs to start at zero: each call
+ *   writes what it reads).  Calls whose work overlaps on the GPU (on different
+ *   streams, or from different host threads without ordering) race on it;
+ *   order them, e.g. issue them on one stream.
+ * Errors: Q1_ERR_ARG for a bad shape, pointer or a size beyond the limit;
+ * Q1_ERR_CUDA for a failed lookup or launch. */
+int q1_0_gemm_small_noalloc(const void *packed, int64_t rows, int64_t n, int64_t nvec, const int8_t *q,
+                            const uint16_t *d, float *out, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Q2_0 (ternary) weights: the sibling format the pages name as the next GPU
  * kernel ("Advantages and efficiency", where optimization goes next;
