@@ -345,6 +345,43 @@ def test_gemv_multi_many_products_balanced(size):
         bits_equal(item[-1].cpu().numpy(), w)
 
 
+@pytest.mark.parametrize("act", ["f32", "q8"])
+@pytest.mark.parametrize("shapes", [
+    [(2600, 20480)],
+    [(300, 1024), (2600, 20480), (64, 24576), (1000, 4096), (5000, 16512), (7, 17408), (256, 384),
+     (4096, 4096), (1, 128), (999, 20608)],
+    [(128256, 16512)],
+])
+def test_streaming_kernel_long_rows_table_chunks(shapes, act):
+    """Rows longer than the streaming kernel's one-chunk activation table
+    (more than 128 blocks): the table is rebuilt chunk by chunk inside every
+    tile, from f32 input (quantized on the way) or from q8_0 input, for one
+    product and for a list of more than eight; every output against the
+    oracle.  The lm_head-sized row count takes eight rows per thread."""
+    plan = binding.multi_plan(shapes)
+    assert plan["panel_warps"] == 0
+    if shapes[0][0] == 128256:
+        assert plan["rows_per_thread"] == 8
+    items, want = [], []
+    for i, (rows, n) in enumerate(shapes):
+        rng = synth.rng_for(140, i, len(shapes), len(act))
+        blocks = synth.weight_blocks(rng, rows, n, "lognormal" if i % 2 else "halfnormal")
+        out = torch.full((rows,), float("nan"), device="cuda")
+        packed = binding.pack(dev(blocks), rows, n)
+        if act == "f32":
+            x = synth.activations(rng, 1, n, outliers=0.01)
+            q, d = oracle.q8_quantize(x)
+            items.append((packed, rows, n, dev(x[0]), None, None, out))
+        else:
+            q, d = synth.raw_quants(rng, 1, n, scale="lognormal", m128_frac=0.03)
+            items.append((packed, rows, n, None, dev(q[0]), dev(d[0].view(np.int16)), out))
+        want.append(oracle.gemm_threaded(blocks, q, d)[0])
+    binding.gemv_multi(items)
+    torch.cuda.synchronize()
+    for item, w in zip(items, want):
+        bits_equal(item[-1].cpu().numpy(), w)
+
+
 def test_gemv_multi_fused_equals_quantize_then_gemv():
     rows, n = 4096, 14336
     rng = synth.rng_for(111)
