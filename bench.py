@@ -317,12 +317,29 @@ OTHER_CONFIGS = (
 )
 
 
+# Roof of the batched product: the definition's chain needs at least 5 f32
+# operations per lane, block and vector (d1*s, three fma with d1, the outer fma
+# with d0) when the integer lane sums come for free: 5/16 per weight and vector
+# on the CUDA cores' f32 pipes (128 lanes per SM per clock).  The tensor-core
+# kernel takes most of the chain into its MMAs, so it is measured against the
+# same roof (it could exceed it).
+CHAIN_OPS_PER_WEIGHT_VECTOR = 5.0 / 16.0
+
+
+def fp32_roof_ops_per_s(sm_mhz=None):
+    import torch
+    props = torch.cuda.get_device_properties(0)
+    mhz = sm_mhz or 2070.0
+    return props.multi_processor_count * 128 * mhz * 1e6
+
+
 def time_other_configs(dev, reps: int = 15):
     import torch
     from decode_q1_gemv_gb300 import binding, synth
 
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
     stream = torch.cuda.current_stream(dev)
+    roof = fp32_roof_ops_per_s()
     res = {}
     for ci, (name, rows, n, nvec, scale, outl) in enumerate(OTHER_CONFIGS):
         blocks = synth.weight_blocks(synth.rng_for(11, ci, 0), rows, n, scale)
@@ -337,25 +354,42 @@ def time_other_configs(dev, reps: int = 15):
             else:
                 binding.gemm_small(packed, rows, n, q, d, out)
 
-        for _ in range(3):
-            launch()
-        ts = []
-        for _ in range(reps):
-            flush.add_(1.0)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            launch()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3)
-        ts.sort()
-        us = ts[len(ts) // 2]
+        def cold_median():
+            for _ in range(3):
+                launch()
+            ts = []
+            for _ in range(reps):
+                flush.add_(1.0)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                launch()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            ts.sort()
+            return ts[len(ts) // 2], ts[0]
+
+        us, us_min = cold_median()
         wbytes = rows * n * 18 // 128
-        entry = {"rows": rows, "n": n, "vectors": nvec, "us": round(us, 2), "us_min": round(ts[0], 2),
+        entry = {"rows": rows, "n": n, "vectors": nvec, "us": round(us, 2), "us_min": round(us_min, 2),
                  "weight_gbs": round(wbytes / (us * 1e-6) / 1e9, 1)}
         if nvec > 1:
-            # lane-chain work of the exact contract: 0.5 fp32 ops per weight per vector
-            entry["weight_vector_products_per_s"] = round(rows * n * nvec / (us * 1e-6), 0)
+            wv = rows * n * nvec
+            entry["weight_vector_products_per_s"] = round(wv / (us * 1e-6), 0)
+            entry["roofline"] = {"bound": "alu", "unit": "f32 ops/s",
+                                 "achieved": round(wv * CHAIN_OPS_PER_WEIGHT_VECTOR / (us * 1e-6), 0),
+                                 "peak": roof,
+                                 "frac": round(wv * CHAIN_OPS_PER_WEIGHT_VECTOR / (us * 1e-6) / roof, 4),
+                                 "roof": "definition's f32 chain, 5 ops per 16 weight-vector products, on all "
+                                         "SMs' f32 lanes at 2070 MHz"}
+            by_kernel = {}
+            for k in ("dp4a", "tensor"):
+                prev = binding.gemm_small_kernel(k)
+                try:
+                    by_kernel[k] = round(cold_median()[0], 2)
+                finally:
+                    binding.gemm_small_kernel(prev)
+            entry["us_by_kernel"] = by_kernel
         res[name] = entry
         del packed, q, d, out
     del flush
