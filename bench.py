@@ -515,6 +515,17 @@ def run_ours(args):
             g.replay()
         torch.cuda.synchronize()
         sched_us[sch] = round(reduce_max(_time_graph(g, max(args.steps // 4, 10), stream)) * 1e3, 2)
+    # the dependent schedules without the next launch's L2 prefetch, for comparison
+    sched_us_nopf = {}
+    ds.prefetch_next = False
+    for sch in [s for s in schedules[1:] if s in ("grouped", "decode")]:
+        g = ds._capture(lambda sch=sch: ds.step(schedule=sch))
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        sched_us_nopf[sch] = round(reduce_max(_time_graph(g, max(args.steps // 4, 10), stream)) * 1e3, 2)
+        del g
+    ds.prefetch_next = True
 
     # ---- end to end through the public API with host buffers.  First with the
     # activations and outputs in pinned host memory that the kernel reads and
@@ -598,6 +609,7 @@ def run_ours(args):
             "q2_0_decode_set": q2,
             "hbm_frac_of_measured": round(value / world / peak, 4),
             "us_per_set_by_schedule": sched_us,
+            "us_per_set_without_prefetch": sched_us_nopf,
             "launches_by_schedule": {sch: ds.launches(sch) for sch in schedules},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,

@@ -33,7 +33,8 @@ Q1_MISMATCH = 2
 EXPORTS = ("q1_last_error", "q1_0_packed_bytes", "q1_0_pack", "q1_0_unpack", "q8_quantize_act",
            "q1_0_gemv", "q1_0_gemv_multi", "q1_0_gemv_multi_plan", "q1_0_gemm_small", "q1_0_verify",
            "q1_device_status", "q2_0_packed_bytes", "q2_0_pack", "q2_0_unpack", "q2_0_gemv", "q2_0_gemv_multi",
-           "q2_0_gemv_multi_plan", "q1_gemm_small_kernel", "q1_0_gemm_small_noalloc")
+           "q2_0_gemv_multi_plan", "q1_gemm_small_kernel", "q1_0_gemm_small_noalloc",
+           "q1_0_gemv_multi_prefetch", "q2_0_gemv_multi_prefetch")
 
 MAX_PRODUCTS = 256
 
@@ -43,6 +44,14 @@ class Product(ctypes.Structure):
     _fields_ = [("packed", ctypes.c_void_p), ("rows", ctypes.c_int64), ("n", ctypes.c_int64),
                 ("x", ctypes.c_void_p), ("q", ctypes.c_void_p), ("d", ctypes.c_void_p),
                 ("out", ctypes.c_void_p)]
+
+
+class Range(ctypes.Structure):
+    """Mirror of q1_range (include/q1gemv.h)."""
+    _fields_ = [("ptr", ctypes.c_void_p), ("bytes", ctypes.c_int64)]
+
+
+MAX_PREFETCH_RANGES = 4
 
 
 class MultiPlan(ctypes.Structure):
@@ -106,6 +115,9 @@ def load():
         lib.q2_0_gemv.restype = I
         lib.q2_0_gemv_multi.argtypes = [ctypes.POINTER(Product), I, P]
         lib.q2_0_gemv_multi.restype = I
+        for fn in (lib.q1_0_gemv_multi_prefetch, lib.q2_0_gemv_multi_prefetch):
+            fn.argtypes = [ctypes.POINTER(Product), I, ctypes.POINTER(Range), I, P]
+            fn.restype = I
         lib.q1_0_gemm_small.argtypes = [P, I64, I64, I64, P, P, P, P]
         lib.q1_0_gemm_small.restype = I
         lib.q1_0_gemm_small_noalloc.argtypes = [P, I64, I64, I64, P, P, P, P]
@@ -251,11 +263,42 @@ def product_array(items, fmt: str = "q1"):
     return arr
 
 
-def gemv_multi(items=None, stream=None, array=None):
+def _one_range(r):
+    if isinstance(r, torch.Tensor):
+        if not r.is_cuda or not r.is_contiguous():
+            raise ValueError("a prefetch range must be a contiguous CUDA tensor")
+        return Range(r.data_ptr(), r.numel() * r.element_size())
+    ptr, nbytes = r
+    return Range(int(ptr) or None, int(nbytes))
+
+
+def prefetch_ranges(prefetch):
+    """A ctypes q1_range array from a prefetch argument: a CUDA tensor (its
+    bytes), a (pointer, bytes) pair, or a list of those."""
+    items = [prefetch] if isinstance(prefetch, (torch.Tensor, tuple)) else list(prefetch)
+    arr = (Range * max(len(items), 1))()
+    for i, r in enumerate(items):
+        arr[i] = _one_range(r)
+    return arr, len(items)
+
+
+def gemv_multi(items=None, stream=None, array=None, prefetch=None):
     """One launch for several independent products.  `items` as product_array
-    takes them, or a prebuilt `array` (to avoid rebuilding it per call)."""
+    takes them, or a prebuilt `array` (to avoid rebuilding it per call).
+    `prefetch` (a CUDA tensor, a (pointer, bytes) pair, or a list of up to
+    four of those; or a prebuilt (q1_range array, count) from prefetch_ranges)
+    is pulled into L2 while the launch runs, through q1_0_gemv_multi_prefetch."""
     arr = array if array is not None else product_array(items)
-    _check(load().q1_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q1_0_gemv_multi")
+    if prefetch is None:
+        _check(load().q1_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q1_0_gemv_multi")
+        return
+    ranges, nr = prefetch if _is_range_array(prefetch) else prefetch_ranges(prefetch)
+    _check(load().q1_0_gemv_multi_prefetch(arr, len(arr), ranges, nr, _stream_ptr(stream)),
+           "q1_0_gemv_multi_prefetch")
+
+
+def _is_range_array(p) -> bool:
+    return isinstance(p, tuple) and len(p) == 2 and isinstance(p[0], ctypes.Array)
 
 
 def multi_plan(shapes, sms: int = 0, fmt: str = "q1") -> dict:
@@ -327,11 +370,16 @@ def q2_gemv(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.T
     return out
 
 
-def q2_gemv_multi(items=None, stream=None, array=None):
+def q2_gemv_multi(items=None, stream=None, array=None, prefetch=None):
     """One launch for several independent Q2_0 products (items as product_array
-    takes them, with packed buffers from q2_pack)."""
+    takes them, with packed buffers from q2_pack); `prefetch` as gemv_multi."""
     arr = array if array is not None else product_array(items, fmt="q2")
-    _check(load().q2_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q2_0_gemv_multi")
+    if prefetch is None:
+        _check(load().q2_0_gemv_multi(arr, len(arr), _stream_ptr(stream)), "q2_0_gemv_multi")
+        return
+    ranges, nr = prefetch if _is_range_array(prefetch) else prefetch_ranges(prefetch)
+    _check(load().q2_0_gemv_multi_prefetch(arr, len(arr), ranges, nr, _stream_ptr(stream)),
+           "q2_0_gemv_multi_prefetch")
 
 
 def gemm_small(packed: torch.Tensor, rows: int, n: int, q: torch.Tensor, d: torch.Tensor,

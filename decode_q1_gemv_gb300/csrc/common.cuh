@@ -105,8 +105,20 @@ int cuda_status(cudaError_t e, const char* what);
 int num_sms();
 // Argument checks of one q1_product (shape, pointers, 16-byte alignment).
 int check_product(const char* who, int idx, const q1_product& pr);
+// Device byte ranges a product launch pulls into L2 while it runs (the packed
+// weights and the activation of the launch that follows): each p 16-byte
+// aligned, bytes a multiple of 16; count 0 for none.
+struct L2Range {
+  const uint8_t* p;
+  int64_t bytes;
+};
+struct L2Ranges {
+  L2Range r[Q1_MAX_PREFETCH_RANGES];
+  int count;
+};
 // The streaming matrix-vector kernel behind q1_0_gemv / q1_0_gemv_multi.
-int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, const char* who);
+int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, const char* who,
+                         const L2Ranges& pf = L2Ranges{});
 // Device status word of the product kernels (read and optionally cleared).
 int status_word_dp4a(unsigned* v, int clear);
 int status_word_prod(unsigned* v, int clear);
@@ -171,6 +183,23 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
   if (mbar_try(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, limit_ns);
+}
+
+// This CTA's share of an L2 prefetch of r, issued by the calling thread: the
+// range is cut into `ctas` pieces on 16-byte boundaries and piece `cta` goes
+// out as one bulk prefetch (one per 16 MB).  A hint: nothing waits for it.
+__device__ __forceinline__ void l2_prefetch_share(const L2Range& r, int cta, int ctas) {
+  if (r.p == nullptr || r.bytes < 16) return;
+  const int64_t units = r.bytes >> 4;
+  const int64_t u0 = units * cta / ctas, u1 = units * (cta + 1) / ctas;
+  for (int64_t u = u0; u < u1; u += int64_t(1) << 20) {  // at most 16 MB an instruction
+    const int64_t m = u1 - u < (int64_t(1) << 20) ? u1 - u : int64_t(1) << 20;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(r.p + (u << 4)), "r"(uint32_t(m << 4))
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void l2_prefetch_share(const L2Ranges& rs, int cta, int ctas) {
+  for (int i = 0; i < rs.count && i < Q1_MAX_PREFETCH_RANGES; ++i) l2_prefetch_share(rs.r[i], cta, ctas);
 }
 
 // 1-D bulk copy global -> shared, completing on `bar` (both addresses 16-byte

@@ -40,6 +40,7 @@ struct PanelConfig {
 template <class F>
 PanelConfig panel_config(const q1_product* prods, int count, int sms);
 template <class F>
-int launch_panel(const q1_product* prods, int count, PanelConfig c, cudaStream_t s, const char* who);
+int launch_panel(const q1_product* prods, int count, PanelConfig c, cudaStream_t s, const char* who,
+                 const L2Ranges& pf);
 
 }  // namespace q1

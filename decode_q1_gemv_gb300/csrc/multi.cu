@@ -74,6 +74,7 @@ struct MArgs {
   int count;
   int kc;                // table chunk in blocks (multiple of 4)
   int ncut;              // 0: equal split of the cost axis; else CTA b owns [cut[b], cut[b+1])
+  L2Ranges pf;           // pulled into L2 while this launch runs (the next launch's inputs)
   int64_t cut[PMAX > 8 ? kMaxCuts + 1 : 1];
 };
 
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
   constexpr int kConsumers = consumers<R>();
   constexpr int TB = kSlots * R * F::kQuadBits;  // bits part of a stage
   constexpr int kTableBatch = R >= 8 ? 8 : 4;  // load rounds in flight while a table is built
+  constexpr int kTableBatchX = R >= 8 ? 4 : R >= 2 ? 2 : 1;  // the same from f32 (two words a round)
   unsigned char* table = smem + S * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(table + table_bytes(a.kc));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,6 +153,7 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
     if (lane == 0) {
+      l2_prefetch_share(a.pf, int(blockIdx.x), int(gridDim.x));  // the next launch's inputs, if given
       bool ok = true;
       int it = 0;
       for (int j = first_product(a, lo); j < a.count && a.p[j].cost_begin < hi && ok; ++j) {
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
     const bool one_chunk = pnbp <= kc;
     if (one_chunk) {
       named_barrier(kConsumerBarrier, kConsumers);  // previous product's table no longer read
-      if (px) build_table_x<kTableBatch, typename F::Consts>(px, pnb, 0, pnbp, table, tid, kConsumers, kc);
+      if (px) build_table_x<kTableBatchX, typename F::Consts>(px, pnb, 0, pnbp, table, tid, kConsumers, kc);
       else build_table_q<kTableBatch, typename F::Consts>(pq, pd, pnb, 0, pnbp, table, tid, kConsumers, kc);
       named_barrier(kConsumerBarrier, kConsumers);
     }
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(multi_threads<R>(), 2) k_q1_multi(const __grid
         if (!one_chunk && b0 % kc == 0) {
           named_barrier(kConsumerBarrier, kConsumers);
           const int kcb = min(kc, pnbp - b0);
-          if (px) build_table_x<kTableBatch, typename F::Consts>(px, pnb, b0, kcb, table, tid, kConsumers, kc);
+          if (px) build_table_x<kTableBatchX, typename F::Consts>(px, pnb, b0, kcb, table, tid, kConsumers, kc);
           else build_table_q<kTableBatch, typename F::Consts>(pq, pd, pnb, b0, kcb, table, tid, kConsumers, kc);
           named_barrier(kConsumerBarrier, kConsumers);
         }
@@ -425,11 +428,12 @@ static void plan_multi(const q1_product* prods, int count, int sms, MArgs<PMAX>&
 }
 
 template <int R, int PMAX, class F>
-static int launch_multi(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+static int launch_multi(const q1_product* prods, int count, cudaStream_t s, const char* who, const L2Ranges& pf) {
   if (int e = set_smem_attr<R, PMAX, F>()) return e;
   MArgs<PMAX> a;
   int grid = 0;
   plan_multi<R, PMAX, F>(prods, count, num_sms(), a, grid);
+  a.pf = pf;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(multi_threads<R>());
@@ -488,11 +492,11 @@ static int rows_per_thread(const q1_product* prods, int count, int sms) {
 }
 
 template <int PMAX, class F>
-static int dispatch(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+static int dispatch(const q1_product* prods, int count, cudaStream_t s, const char* who, const L2Ranges& pf) {
   switch (rows_per_thread<F>(prods, count, num_sms())) {
-    case F::kBigRows: return launch_multi<F::kBigRows, PMAX, F>(prods, count, s, who);
-    case 2: return launch_multi<2, PMAX, F>(prods, count, s, who);
-    default: return launch_multi<1, PMAX, F>(prods, count, s, who);
+    case F::kBigRows: return launch_multi<F::kBigRows, PMAX, F>(prods, count, s, who, pf);
+    case 2: return launch_multi<2, PMAX, F>(prods, count, s, who, pf);
+    default: return launch_multi<1, PMAX, F>(prods, count, s, who, pf);
   }
 }
 
@@ -530,16 +534,17 @@ int check_product(const char* who, int idx, const q1_product& pr) {
 }
 
 template <class F>
-static int launch_products(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+static int launch_products(const q1_product* prods, int count, cudaStream_t s, const char* who,
+                           const L2Ranges& pf = L2Ranges{}) {
   const PanelConfig c = panel_config<F>(prods, count, num_sms());
-  if (c.warps) return launch_panel<F>(prods, count, c, s, who);
-  if (count == 1) return dispatch<1, F>(prods, count, s, who);
-  if (count <= 8) return dispatch<8, F>(prods, count, s, who);
-  return dispatch<Q1_MAX_PRODUCTS, F>(prods, count, s, who);
+  if (c.warps) return launch_panel<F>(prods, count, c, s, who, pf);
+  if (count == 1) return dispatch<1, F>(prods, count, s, who, pf);
+  if (count <= 8) return dispatch<8, F>(prods, count, s, who, pf);
+  return dispatch<Q1_MAX_PRODUCTS, F>(prods, count, s, who, pf);
 }
 
-int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, const char* who) {
-  return launch_products<FmtQ1>(prods, count, s, who);
+int launch_products_dp4a(const q1_product* prods, int count, cudaStream_t s, const char* who, const L2Ranges& pf) {
+  return launch_products<FmtQ1>(prods, count, s, who, pf);
 }
 
 int status_word_dp4a(unsigned* v, int clear) {
@@ -610,6 +615,39 @@ extern "C" int q1_0_gemv_multi(const q1_product* products, int count, void* stre
   for (int j = 0; j < count; ++j)
     if (int e = check_product("q1_0_gemv_multi", j, products[j])) return e;
   return launch_products_dp4a(products, count, static_cast<cudaStream_t>(stream), "q1_0_gemv_multi launch");
+}
+
+// q1_0_gemv_multi / q2_0_gemv_multi with L2 prefetches of the given ranges,
+// issued by the launch's CTAs before they wait for the preceding kernel.
+template <class F>
+static int multi_prefetch(const char* who, const q1_product* products, int count, const q1_range* prefetch,
+                          int nranges, void* stream) {
+  if (!products || count < 1 || count > Q1_MAX_PRODUCTS)
+    return fail(Q1_ERR_ARG, "%s: count=%d outside 1..%d (or null list)", who, count, Q1_MAX_PRODUCTS);
+  for (int j = 0; j < count; ++j)
+    if (int e = check_product(who, j, products[j])) return e;
+  if (nranges < 0 || nranges > Q1_MAX_PREFETCH_RANGES || (nranges > 0 && !prefetch))
+    return fail(Q1_ERR_ARG, "%s: %d prefetch ranges (0..%d)", who, nranges, Q1_MAX_PREFETCH_RANGES);
+  L2Ranges pf{};
+  for (int i = 0; i < nranges; ++i) {
+    const q1_range& r = prefetch[i];
+    if (r.bytes < 0 || r.bytes > (int64_t(1) << 40) || (r.bytes > 0 && !r.ptr))
+      return fail(Q1_ERR_ARG, "%s: prefetch range %d: %lld bytes at %p", who, i, (long long)r.bytes, r.ptr);
+    if (reinterpret_cast<uintptr_t>(r.ptr) % 16 != 0)
+      return fail(Q1_ERR_ARG, "%s: prefetch range %d must start 16-byte aligned", who, i);
+    if (r.bytes >= 16) pf.r[pf.count++] = L2Range{static_cast<const uint8_t*>(r.ptr), r.bytes / 16 * 16};
+  }
+  return launch_products<F>(products, count, static_cast<cudaStream_t>(stream), who, pf);
+}
+
+extern "C" int q1_0_gemv_multi_prefetch(const q1_product* products, int count, const q1_range* prefetch,
+                                        int nranges, void* stream) {
+  return multi_prefetch<FmtQ1>("q1_0_gemv_multi_prefetch", products, count, prefetch, nranges, stream);
+}
+
+extern "C" int q2_0_gemv_multi_prefetch(const q1_product* products, int count, const q1_range* prefetch,
+                                        int nranges, void* stream) {
+  return multi_prefetch<FmtQ2>("q2_0_gemv_multi_prefetch", products, count, prefetch, nranges, stream);
 }
 
 extern "C" int q2_0_gemv(const void* packed, int64_t rows, int64_t n, const int8_t* q, const uint16_t* d,

@@ -51,6 +51,7 @@ struct PanelProd {
 struct PanelArgs {
   PanelProd p[kPanelMaxProducts];
   int count;
+  L2Ranges pf;  // pulled into L2 while this launch runs (the next launch's inputs)
 };
 
 __host__ __device__ constexpr int panel_smem_bytes(int nbp) { return nbp * kPanelBytesPerBlock; }
@@ -167,11 +168,14 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
     }
   };
   load(0);
+  // The next launch's inputs (q1_0_gemv_multi_prefetch), one bulk prefetch a
+  // range from one thread: spread over a warp's lanes they held that warp back.
+  if (tid == 32 * W - 32) l2_prefetch_share(a.pf, int(blockIdx.x), int(gridDim.x));
 
   pdl_wait();  // the activation may be written by the preceding kernel
   if (mine > 0) {  // this warp's own table entries: blocks UB u0 .. UB (u0 + mine) - 1
     // Inlined, so that the sign-word loads above stay in flight meanwhile.
-    if (pr.x) table_x_body<4, typename F::Consts>(pr.x, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
+    if (pr.x) table_x_body<2, typename F::Consts>(pr.x, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
     else table_q_body<4, typename F::Consts>(pr.q, pr.d, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
   }
   __syncwarp();
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
 }
 
 template <class F, int W, int UB>
-int launch_panel_w(const q1_product* prods, int count, cudaStream_t s, const char* who) {
+int launch_panel_w(const q1_product* prods, int count, cudaStream_t s, const char* who, const L2Ranges& pf) {
   constexpr int PF = 2;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -252,6 +256,7 @@ int launch_panel_w(const q1_product* prods, int count, cudaStream_t s, const cha
   }
   PanelArgs a = {};
   a.count = count;
+  a.pf = pf;
   int panels = 0, nbp_max = 0;
   for (int j = 0; j < count; ++j) {
     const q1_product& pr = prods[j];
@@ -342,19 +347,20 @@ template PanelConfig panel_config<FmtQ1>(const q1_product*, int, int);
 template PanelConfig panel_config<FmtQ2>(const q1_product*, int, int);
 
 template <class F>
-int launch_panel(const q1_product* prods, int count, PanelConfig c, cudaStream_t s, const char* who) {
+int launch_panel(const q1_product* prods, int count, PanelConfig c, cudaStream_t s, const char* who,
+                 const L2Ranges& pf) {
   if (count < 1 || count > kPanelMaxProducts) return fail(Q1_ERR_ARG, "%s: %d products for the panel kernel", who, count);
   switch (c.warps * 10 + c.unit) {
-    case 164: return launch_panel_w<F, 16, 4>(prods, count, s, who);
-    case 162: return launch_panel_w<F, 16, 2>(prods, count, s, who);
-    case 84: return launch_panel_w<F, 8, 4>(prods, count, s, who);
-    case 82: return launch_panel_w<F, 8, 2>(prods, count, s, who);
-    case 44: return launch_panel_w<F, 4, 4>(prods, count, s, who);
-    case 42: return launch_panel_w<F, 4, 2>(prods, count, s, who);
+    case 164: return launch_panel_w<F, 16, 4>(prods, count, s, who, pf);
+    case 162: return launch_panel_w<F, 16, 2>(prods, count, s, who, pf);
+    case 84: return launch_panel_w<F, 8, 4>(prods, count, s, who, pf);
+    case 82: return launch_panel_w<F, 8, 2>(prods, count, s, who, pf);
+    case 44: return launch_panel_w<F, 4, 4>(prods, count, s, who, pf);
+    case 42: return launch_panel_w<F, 4, 2>(prods, count, s, who, pf);
     default: return fail(Q1_ERR_ARG, "%s: %d warps x %d-block units per panel", who, c.warps, c.unit);
   }
 }
-template int launch_panel<FmtQ1>(const q1_product*, int, PanelConfig, cudaStream_t, const char*);
-template int launch_panel<FmtQ2>(const q1_product*, int, PanelConfig, cudaStream_t, const char*);
+template int launch_panel<FmtQ1>(const q1_product*, int, PanelConfig, cudaStream_t, const char*, const L2Ranges&);
+template int launch_panel<FmtQ2>(const q1_product*, int, PanelConfig, cudaStream_t, const char*, const L2Ranges&);
 
 }  // namespace q1

@@ -54,6 +54,9 @@ struct ConstsQ2 {
     qp = word;
     nq = __vsub4(0u, word);  // per-byte 0 - q modulo 256: -(-128) stays -128
   }
+  static __device__ __forceinline__ void lane_no_m128(uint32_t word, int k, int par, uint32_t& qp, uint32_t& nq) {
+    lane(word, k, par, qp, nq);
+  }
   static __device__ __forceinline__ void scale(float d1, int k, int par, float& dprime, float& K) {
     dprime = __fmul_rn(d1, pow2i(-(2 * k + par)));
     K = -__fmul_rn(dprime, kMagic);

@@ -44,6 +44,15 @@ __device__ __forceinline__ void lane_consts(uint32_t word, int k, int par, uint3
   ci = uint32_t(int(kMagicBits) - A * (1 << (pe_of(k, par) - 1)));
 }
 
+// The same for a word known to hold no -128 byte (the quantizer's own output:
+// |x * id| stays below 127.5, so every code is in -127..127): q' = word and
+// A = sum(q').
+__device__ __forceinline__ void lane_consts_no_m128(uint32_t word, int k, int par, uint32_t& qp, uint32_t& ci) {
+  qp = word;
+  const int A = __dp4a(int(word), 0x01010101, 0);
+  ci = uint32_t(int(kMagicBits) - A * (1 << (pe_of(k, par) - 1)));
+}
+
 __device__ __forceinline__ void scale_consts(float d1, int k, int par, float& dprime, float& K) {
   dprime = __fmul_rn(d1, pow2i(1 - pe_of(k, par)));
   K = -__fmul_rn(dprime, kMagic);
@@ -54,6 +63,9 @@ __device__ __forceinline__ void scale_consts(float d1, int k, int par, float& dp
 struct ConstsQ1 {
   static __device__ __forceinline__ void lane(uint32_t word, int k, int par, uint32_t& qp, uint32_t& ci) {
     lane_consts(word, k, par, qp, ci);
+  }
+  static __device__ __forceinline__ void lane_no_m128(uint32_t word, int k, int par, uint32_t& qp, uint32_t& ci) {
+    lane_consts_no_m128(word, k, par, qp, ci);
   }
   static __device__ __forceinline__ void scale(float d1, int k, int par, float& dprime, float& K) {
     scale_consts(d1, k, par, dprime, K);
@@ -129,58 +141,86 @@ static __device__ __noinline__ void build_table_q(const int8_t* __restrict__ q, 
   table_q_body<kTableBatch, C>(q, d1, nb, blk0, kcb, table, tid, nthreads, kc, 0);
 }
 
+// roundf(t) (halves away from zero) as an 8-bit two's-complement code, for
+// |t| < 2^22, with floating-point adds on the FMA pipe instead of conversion
+// instructions.  With s = |t| + 1/2 exact, k = floor(s) = roundf(|t|) is an
+// integer with k <= s; rounding toward zero is monotone and keeps k, so
+// a = RZ(s) lies in [k, s] and floor(a) = k.  Between 2^23 and 2^24 floats are
+// the integers, so RZ(a + 2^23) = 2^23 + k exactly and its low bits are k.
+// The sign of t is then applied in two's complement.  (t = +-0 gives 0.)
+__device__ __forceinline__ uint32_t round_code(float t) {
+  const float a = __fadd_rz(fabsf(t), 0.5f);
+  const uint32_t k = __float_as_uint(__fadd_rz(a, 8388608.0f));  // 0x4B000000 + k
+  const uint32_t neg = 0u - (__float_as_uint(t) >> 31);          // all ones when t < 0
+  return ((k ^ neg) - neg) & 0xffu;
+}
+
+// The four q8_0 codes of v (x * id per element, rounded as above) in one word,
+// element 0 in the low byte.
+__device__ __forceinline__ uint32_t quant_word(const float4& v, float id) {
+  const uint32_t c0 = round_code(__fmul_rn(v.x, id)), c1 = round_code(__fmul_rn(v.y, id));
+  const uint32_t c2 = round_code(__fmul_rn(v.z, id)), c3 = round_code(__fmul_rn(v.w, id));
+  return c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+}
+
 // Table for blocks [blk0, blk0 + kcb) (at table positions from tpos0, as
-// above) from an f32 activation x [n], quantizing
-// it on the way exactly as q8_quantize_act does (per 32 values: amax, d =
-// amax/127, id = d ? 1/d : 0, q = roundf(x*id), scale fp16(d)).  One thread per
-// (sub-block, lane); the 8 threads of a sub-block are consecutive in a warp.
-// nthreads must be a multiple of 32 and every thread of the group must call.
-// table_x_body inlined, build_table_x out of line, as for the quantized form.
+// above) from an f32 activation x [n], quantizing it on the way exactly as
+// q8_quantize_act does (per 32 values: amax, d = amax/127, id = d ? 1/d : 0,
+// q = roundf(x*id), scale fp16(d)).  One thread per (sub-block, word w): the
+// lanes w and w + 4, i.e. elements 4w..4w+3 and 16+4w..16+4w+3, which fill one
+// QC entry; the 4 threads of a sub-block are consecutive in a warp and share
+// amax by two shuffles; thread w = 0 writes the sub-block's DK entry.  A round
+// of a warp whose first thread is past the end is skipped (the whole warp
+// agrees); nthreads must be a multiple of 32 and every thread of the group
+// must call.  table_x_body inlined, build_table_x out of line, as for the
+// quantized form.
 template <int kTableBatch, class C>
 __device__ __forceinline__ void table_x_body(const float* __restrict__ x, int nb, int blk0, int kcb,
                                              unsigned char* table, int tid, int nthreads, int kc, int tpos0) {
-  uint32_t* QCw = reinterpret_cast<uint32_t*>(table) + tpos0 * 64;
-  float* DKf = reinterpret_cast<float*>(table + table_dk_offset(kc)) + tpos0 * 16;
+  uint4* QC = reinterpret_cast<uint4*>(table) + tpos0 * 16;
+  float4* DK = reinterpret_cast<float4*>(table + table_dk_offset(kc)) + tpos0 * 4;
   const int nsub = nb * 4;
-  const int total = kcb * 4 * 8;
+  const int total = kcb * 16;
+  const int warp0 = tid & ~31;
   for (int base = 0; base < total; base += kTableBatch * nthreads) {  // same trip count for every thread
-    float4 vb[kTableBatch];
+    float4 lo[kTableBatch], hi[kTableBatch];
 #pragma unroll
     for (int u = 0; u < kTableBatch; ++u) {
       const int t = base + u * nthreads + tid;
-      const int G = blk0 * 4 + (t >> 3);
-      vb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < total && G < nsub) vb[u] = *reinterpret_cast<const float4*>(x + int64_t(G) * kSub + 4 * (t & 7));
+      const int G = blk0 * 4 + (t >> 2), w = t & 3;
+      lo[u] = hi[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < total && G < nsub) {
+        const float* xs = x + int64_t(G) * kSub + 4 * w;
+        lo[u] = *reinterpret_cast<const float4*>(xs);
+        hi[u] = *reinterpret_cast<const float4*>(xs + 16);
+      }
     }
 #pragma unroll
     for (int u = 0; u < kTableBatch; ++u) {
+      if (base + u * nthreads + warp0 >= total) break;  // uniform in the warp
       const int t = base + u * nthreads + tid;
-      const int g = t >> 3, l = t & 7;
+      const int g = t >> 2, w = t & 3;
       const int G = blk0 * 4 + g;
-      const float4 v = vb[u];
-      float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+      const float4 a = lo[u], b = hi[u];
+      float amax = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                         fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
       const float dd = __fdiv_rn(amax, 127.0f);
       const float id = (dd != 0.0f) ? __fdiv_rn(1.0f, dd) : 0.0f;
-      const uint32_t q0 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.x, id)))) & 0xffu;
-      const uint32_t q1 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.y, id)))) & 0xffu;
-      const uint32_t q2 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.z, id)))) & 0xffu;
-      const uint32_t q3 = uint32_t(static_cast<int>(roundf(__fmul_rn(v.w, id)))) & 0xffu;
-      const uint32_t word = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
-      const float d1 = __half2float(__float2half_rn(dd));
+      const uint32_t wlo = quant_word(a, id), whi = quant_word(b, id);
       if (t < total) {
-        const int k = g & 3, par = l >> 2, w = l & 3;
-        uint32_t qp, ci;
-        C::lane(word, k, par, qp, ci);
-        QCw[(g * 4 + w) * 4 + par] = qp;
-        QCw[(g * 4 + w) * 4 + 2 + par] = ci;
-        if ((l & 3) == 0) {
-          float dprime, K;
-          C::scale(G < nsub ? d1 : 0.0f, k, par, dprime, K);
-          DKf[g * 4 + par] = dprime;
-          DKf[g * 4 + 2 + par] = K;
+        const int k = g & 3;
+        uint32_t qp0, ci0, qp1, ci1;
+        C::lane_no_m128(wlo, k, 0, qp0, ci0);
+        C::lane_no_m128(whi, k, 1, qp1, ci1);
+        QC[g * 4 + w] = make_uint4(qp0, qp1, ci0, ci1);
+        if (w == 0) {
+          const float d1 = G < nsub ? __half2float(__float2half_rn(dd)) : 0.0f;
+          float de, dodd, ke, ko;
+          C::scale(d1, k, 0, de, ke);
+          C::scale(d1, k, 1, dodd, ko);
+          DK[g] = make_float4(de, dodd, ke, ko);
         }
       }
     }

@@ -16,7 +16,13 @@ per product.  Schedules of the same work:
 
 Every schedule can be captured once as a CUDA graph and replayed; the kernels
 use programmatic dependent launch, so each launch's weight streaming begins
-while the previous kernel drains.
+while the previous kernel drains.  In "grouped" and "decode" each launch also
+pulls the packed weights and the activations of the launch after it into L2
+(q1_0_gemv_multi_prefetch; prefetch_next=False turns that off).  Weights do
+not depend on the chain; in a real decode step the activation is the output
+of the kernel just before, already in L2, while here every product reads its
+own stored vector, so prefetching it gives a launch the inputs a real step's
+launch finds in L2.
 
 fmt="q2" builds the same set with Q2_0 (ternary) weights (q2_0_* calls,
 34 bytes per 128 weights, synth.ternary_blocks_fast).
@@ -37,7 +43,7 @@ def _round_up(x: int, a: int) -> int:
 
 class DecodeSet:
     def __init__(self, seed: int = 3, device: str = "cuda", shapes=None, scale: str = "halfnormal",
-                 outliers: float = 0.0, fmt: str = "q1"):
+                 outliers: float = 0.0, fmt: str = "q1", prefetch_next: bool = True):
         if fmt not in ("q1", "q2"):
             raise ValueError(f"unknown weight format {fmt!r}")
         self.fmt = fmt
@@ -47,6 +53,7 @@ class DecodeSet:
         self._gemv = binding.gemv if fmt == "q1" else binding.q2_gemv
         self._gemv_multi = binding.gemv_multi if fmt == "q1" else binding.q2_gemv_multi
         self.seed = seed
+        self.prefetch_next = prefetch_next
         self.device = torch.device(device)
         self.shapes = list(shapes) if shapes is not None else synth.decode_set_shapes()
         self.scale = scale
@@ -146,6 +153,30 @@ class DecodeSet:
                                 for g in self.groups(schedule)])
         return getattr(self, key)
 
+    def weights_view(self, first: int, last: int) -> torch.Tensor:
+        """The packed weights of products first..last (contiguous in the
+        resident buffer, in product order)."""
+        _, rows, n = self.shapes[last]
+        return self.packed[self.offsets[first]:self.offsets[last] + self._packed_bytes(rows, n)]
+
+    def activations_view(self, first: int, last: int) -> torch.Tensor:
+        """The f32 activations of products first..last (contiguous)."""
+        _, rows, n = self.shapes[last]
+        return self.x_all[self.x_off[first]:self.x_off[last] + n]
+
+    def _prefetches(self, schedule):
+        """Per launch of the schedule: the next launch's packed weights and
+        activations as a prebuilt range array, or None."""
+        gs = self.groups(schedule)
+        if not self.prefetch_next or schedule == "set":
+            return [None] * len(gs)
+        key = "_pf_" + schedule
+        if not hasattr(self, key):
+            setattr(self, key, [binding.prefetch_ranges([self.weights_view(gs[k + 1][0], gs[k + 1][-1]),
+                                                         self.activations_view(gs[k + 1][0], gs[k + 1][-1])])
+                                if k + 1 < len(gs) else None for k in range(len(gs))])
+        return getattr(self, key)
+
     def launches(self, schedule: str) -> int:
         return 2 * len(self.shapes) if schedule == "separate" else len(self.groups(schedule))
 
@@ -156,8 +187,8 @@ class DecodeSet:
                 binding.quantize(self.x[i], self.q[i], self.d[i], stream=stream)
                 self._gemv(self.packed_view(i), rows, n, self.q[i], self.d[i], self.out[i], stream=stream)
             return
-        for arr in self._arrays(schedule):
-            self._gemv_multi(array=arr, stream=stream)
+        for arr, pf in zip(self._arrays(schedule), self._prefetches(schedule)):
+            self._gemv_multi(array=arr, stream=stream, prefetch=pf)
 
     def products(self, stream=None):
         """Enqueue the products alone (activations already quantized)."""

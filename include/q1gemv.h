@@ -136,6 +136,36 @@ typedef struct q1_product {
  * preceding kernel on `stream` has finished). */
 int q1_0_gemv_multi(const q1_product *products, int count, void *stream);
 
+/* A device byte range (for q1_0_gemv_multi_prefetch). */
+typedef struct q1_range {
+  const void *ptr;        /* device pointer, 16-byte aligned; NULL with 0 bytes   */
+  int64_t bytes;          /* 0 <= bytes <= 2^40, rounded down to a multiple of 16 */
+} q1_range;
+
+#define Q1_MAX_PREFETCH_RANGES 4
+
+/* q1_0_gemv_multi, and while the launch runs its CTAs also pull the given
+ * device byte ranges into the L2 cache (one bulk prefetch a CTA and range,
+ * issued before the kernel waits for the preceding one; nothing waits for
+ * them and nothing of them is read into the SMs).  For a chain of dependent
+ * launches (a decode step, where each product's activation is produced by the
+ * kernels before it), the ranges are the packed weights of the launch that
+ * follows (they do not depend on the chain) and its activation (in a decode
+ * step the output of the kernel just before, already in L2; a chain that
+ * reads stored activations gets the same effect by prefetching them).  That
+ * launch then finds its inputs in L2 instead of HBM.  A prefetch never
+ * changes what a kernel reads: L2 is where every write lands first.  No
+ * counterpart in the pages; it serves their point that each matrix call pays
+ * its own submit and wait ("Limitations").
+ *   prefetch : HOST array of `nranges` ranges (0 <= nranges <=
+ *              Q1_MAX_PREFETCH_RANGES; NULL with 0), read during the call
+ *              only.  Each range must be memory the device may read; its
+ *              contents do not matter and no byte outside it is touched.
+ * Outputs are those of q1_0_gemv_multi, bit for bit.  Q1_ERR_ARG for a bad
+ * range, as for the products. */
+int q1_0_gemv_multi_prefetch(const q1_product *products, int count, const q1_range *prefetch, int nranges,
+                             void *stream);
+
 /* The work split of a q1_0_gemv_multi launch, as the call would make it.
  * Planning only: nothing is launched and no pointer in `products` is read
  * (only rows and n; the shapes are checked as q1_0_gemv_multi checks them).
@@ -270,6 +300,10 @@ int q2_0_gemv(const void *packed, int64_t rows, int64_t n, const int8_t *q, cons
 /* Several independent Q2_0 products in one launch: as q1_0_gemv_multi, each
  * descriptor's `packed` from q2_0_pack(rows, n). */
 int q2_0_gemv_multi(const q1_product *products, int count, void *stream);
+
+/* q2_0_gemv_multi with the L2 prefetch of q1_0_gemv_multi_prefetch. */
+int q2_0_gemv_multi_prefetch(const q1_product *products, int count, const q1_range *prefetch, int nranges,
+                             void *stream);
 
 /* The work split of a q2_0_gemv_multi launch: as q1_0_gemv_multi_plan.  The
  * kernel choice for a single product can differ from Q1_0's (the Q2_0 panel

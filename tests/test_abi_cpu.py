@@ -95,6 +95,27 @@ def test_misaligned_pointers_rejected_on_host(lib):
     assert lib.q1_0_pack(ctypes.c_void_p(0x10001), 4, 128, ok, None) == binding.Q1_ERR_ARG
 
 
+@pytest.mark.parametrize("fn", ["q1_0_gemv_multi_prefetch", "q2_0_gemv_multi_prefetch"])
+def test_prefetch_ranges_rejected_on_host(lib, fn):
+    """Bad prefetch ranges are refused before anything is launched."""
+    ok = 0x10000
+    prods = (binding.Product * 1)(binding.Product(ok, 4, 128, ok, None, None, ok))
+    call = getattr(lib, fn)
+
+    def ranges(*rs):
+        arr = (binding.Range * max(len(rs), 1))()
+        for i, (p, b) in enumerate(rs):
+            arr[i] = binding.Range(p, b)
+        return arr, len(rs)
+
+    for rs in ([(ok + 8, 64)], [(ok, -16)], [(None, 64)], [(ok, 1 << 41)], [(ok, 16)] * 5):
+        arr, nr = ranges(*rs)
+        assert call(prods, 1, arr, nr, None) == binding.Q1_ERR_ARG
+        assert "prefetch" in binding.last_error()
+    assert call(prods, 1, None, 2, None) == binding.Q1_ERR_ARG
+    assert call(prods, 1, None, -1, None) == binding.Q1_ERR_ARG
+
+
 def test_oracle_and_library_share_no_code():
     """The library sources never include or name the oracle, and vice versa."""
     csrc = os.path.join(ROOT, "decode_q1_gemv_gb300", "csrc")

@@ -135,10 +135,11 @@ def test_pack_rejections_stay_per_call_across_streams():
 
 
 # ---------------------------------------------------------- quantization --
-@pytest.mark.parametrize("case", ["normal", "outliers", "tiny", "large", "zeros", "ties"])
-def test_quantize_parity(case):
-    rng = synth.rng_for(102, len(case))
-    nvec, n = 3, 4096
+QUANT_CASES = ["normal", "outliers", "tiny", "large", "zeros", "ties"]
+
+
+def quant_case_activations(rng, case, nvec, n):
+    """f32 activations of the named quantizer regime."""
     if case == "normal":
         x = synth.activations(rng, nvec, n)
     elif case == "outliers":
@@ -150,11 +151,20 @@ def test_quantize_parity(case):
     elif case == "zeros":
         x = synth.activations(rng, nvec, n)
         x[:, 64:128] = 0.0
-        x[1, :] = 0.0
+        if nvec > 1:
+            x[1, :] = 0.0
     else:  # values whose scaled magnitude is exactly k + 0.5 when amax = 127
         x = np.zeros((nvec, n), dtype=np.float32)
         x[:, ::32] = 127.0
         x[:, 1::32] = (rng.integers(-126, 126, size=(nvec, n // 32)) + 0.5).astype(np.float32)
+    return x
+
+
+@pytest.mark.parametrize("case", QUANT_CASES)
+def test_quantize_parity(case):
+    rng = synth.rng_for(102, len(case))
+    nvec, n = 3, 4096
+    x = quant_case_activations(rng, case, nvec, n)
     q, d = binding.quantize(dev(x))
     want_q, want_d = oracle.q8_quantize(x)
     assert np.array_equal(q.cpu().numpy(), want_q)
@@ -393,6 +403,81 @@ def test_gemv_multi_fused_equals_quantize_then_gemv():
     b = torch.empty(rows, device="cuda")
     binding.gemv_multi([(packed, rows, n, x, None, None, b)])
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("fmt,rows", [("q1", 1000), ("q1", 40000), ("q2", 1000), ("q2", 40000)])
+@pytest.mark.parametrize("case", QUANT_CASES + ["fixture"])
+def test_fused_quantization_every_regime(fmt, rows, case):
+    """The product kernels quantize an f32 activation themselves while they
+    build their tables (two words of a sub-block per thread, rounding with
+    adds instead of conversions).  Every regime of the quantizer test, and the
+    hand-derived q8 block, gives the oracle's quantize-then-product bits, in
+    the panel kernel (1000 rows) and in the streaming kernel (40000 rows)."""
+    import json
+    import os
+    n = 4096
+    rng = synth.rng_for(112, rows, len(case), len(fmt))
+    if case == "fixture":
+        spec = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "q8_hand_derived.json")))
+        blocks32 = []
+        for c in spec["cases"]:
+            xb = np.full(32, int(c["x_fill_hex"], 16), dtype=np.uint32)
+            for k, v in c["x_hex"].items():
+                xb[int(k)] = int(v, 16)
+            blocks32.append(xb.view(np.float32))
+        x = np.resize(np.concatenate(blocks32), n)[None, :].astype(np.float32)
+    else:
+        x = quant_case_activations(rng, case, 1, n)
+    plan = binding.multi_plan([(rows, n)], fmt=fmt)
+    assert (plan["panel_warps"] > 0) == (rows == 1000)
+    wq, wd = oracle.q8_quantize(x)
+    out = torch.empty(rows, device="cuda")
+    if fmt == "q1":
+        blocks = synth.weight_blocks(rng, rows, n, "lognormal")
+        binding.gemv_multi([(binding.pack(dev(blocks), rows, n), rows, n, dev(x[0]), None, None, out)])
+        want = oracle.gemm_threaded(blocks, wq, wd)[0]
+    else:
+        tb = synth.ternary_blocks_fast(rng, rows, n)
+        binding.q2_gemv_multi([(binding.q2_pack(dev(tb), rows, n), rows, n, dev(x[0]), None, None, out)])
+        want = oracle.q2_gemv_threaded(tb, wq[0], wd[0])
+    bits_equal(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("fmt,rows", [("q1", 1000), ("q1", 40000), ("q2", 1000), ("q2", 40000)])
+def test_gemv_multi_prefetch_same_bits(fmt, rows):
+    """q1_0_gemv_multi_prefetch / q2_0_gemv_multi_prefetch give the bits of the
+    plain call, with the prefetched ranges another product's packed weights, a
+    ragged byte count (rounded down inside the range), empty ranges, or
+    several ranges (weights and the activation itself)."""
+    n = 2048
+    rng = synth.rng_for(113, rows, len(fmt))
+    x = dev(synth.activations(rng, 1, n)[0])
+    if fmt == "q1":
+        blocks = synth.weight_blocks(rng, rows, n)
+        packed, other = binding.pack(dev(blocks), rows, n), binding.pack(dev(blocks[:777]), 777, n)
+        run = binding.gemv_multi
+    else:
+        tb = synth.ternary_blocks_fast(rng, rows, n)
+        packed, other = binding.q2_pack(dev(tb), rows, n), binding.q2_pack(dev(tb[:777]), 777, n)
+        run = binding.q2_gemv_multi
+    base = torch.empty(rows, device="cuda")
+    run([(packed, rows, n, x, None, None, base)])
+    for pf in (other, (other.data_ptr(), other.numel() - 5), (other.data_ptr(), 0), (0, 0), [other, x],
+               [(0, 0)] * 4, []):
+        out = torch.full((rows,), float("nan"), device="cuda")
+        run([(packed, rows, n, x, None, None, out)], prefetch=pf)
+        assert torch.equal(out.view(torch.int32), base.view(torch.int32))
+
+
+def test_gemv_multi_prefetch_rejects_bad_ranges():
+    rows, n = 256, 1024
+    packed = binding.pack(dev(synth.weight_blocks(synth.rng_for(114), rows, n)), rows, n)
+    x = torch.zeros(n, device="cuda")
+    out = torch.empty(rows, device="cuda")
+    for pf in ((packed.data_ptr() + 8, 64), (packed.data_ptr(), -16), (0, 64), [packed] * 5,
+               [x, (packed.data_ptr() + 4, 16)]):
+        with pytest.raises(binding.Q1Error, match="prefetch"):
+            binding.gemv_multi([(packed, rows, n, x, None, None, out)], prefetch=pf)
 
 
 def test_gemv_multi_host_activations_and_outputs():
