@@ -602,7 +602,7 @@ def run_ours(args):
             "config": {"workload": WORKLOAD if args.layers >= 32 else f"first {args.layers} layers of the set",
                        "products": len(ds.shapes), "batch": 1, "weight_bytes": wb,
                        "schedule": "set: one q1_0_gemv_multi launch, q8_0 quantization fused",
-                       "l2": "inputs larger than L2: each step streams 1.055 GB of weights",
+                       "l2": f"inputs larger than L2: each step streams {wb / 1e9:.3f} GB of weights",
                        "parallelism": f"replicas x{world}"},
             "us_per_set": round(step_ms * 1e3, 2),
             "other_configs_cold_l2": other,
