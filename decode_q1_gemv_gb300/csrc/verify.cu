@@ -301,6 +301,50 @@ int run_wait_probe(Report& rep) {
   return Q1_OK;
 }
 
+// The product kernels round x * id with adds on the FMA pipe (round_code in
+// table.cuh) instead of roundf and a conversion.  Every float t with
+// |t| < 2^22 (the kernels' values stay below 127.5) is compared with the
+// device's roundf converted to int, low byte.
+__global__ void k_round_check(unsigned long long* res, unsigned* first) {
+  unsigned long long tested = 0, bad = 0;
+  const unsigned long long step = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
+  for (unsigned long long i = blockIdx.x * static_cast<unsigned long long>(blockDim.x) + threadIdx.x;
+       i < (1ull << 32); i += step) {
+    const float t = __uint_as_float(static_cast<uint32_t>(i));
+    if (!(fabsf(t) < 4194304.0f)) continue;
+    ++tested;
+    const uint32_t want = static_cast<uint32_t>(static_cast<int>(roundf(t))) & 0xffu;
+    if (round_code(t) != want) {
+      ++bad;
+      atomicMin(first, static_cast<uint32_t>(i));
+    }
+  }
+  atomicAdd(&res[0], tested);
+  atomicAdd(&res[1], bad);
+}
+
+int run_round_check(Report& rep) {
+  Dev dev;
+  auto* d_res = static_cast<unsigned long long*>(dev.get(16));
+  auto* d_first = static_cast<unsigned*>(dev.get(4));
+  if (!d_res || !d_first) return fail(Q1_ERR_NOMEM, "q1_0_verify: device allocation failed");
+  if (int e = cuda_status(cudaMemset(d_res, 0, 16), "q1_0_verify rounding check")) return e;
+  if (int e = cuda_status(cudaMemset(d_first, 0xff, 4), "q1_0_verify rounding check")) return e;
+  k_round_check<<<num_sms() * 8, 256>>>(d_res, d_first);
+  if (int e = cuda_status(cudaGetLastError(), "q1_0_verify rounding check")) return e;
+  unsigned long long res[2] = {0, 0};
+  unsigned first = 0;
+  if (int e = cuda_status(cudaMemcpy(res, d_res, 16, cudaMemcpyDeviceToHost), "q1_0_verify rounding check")) return e;
+  if (int e = cuda_status(cudaMemcpy(&first, d_first, 4, cudaMemcpyDeviceToHost), "q1_0_verify rounding check"))
+    return e;
+  if (res[1] != 0) {
+    rep.add("q8 rounding by adds: %llu of %llu values differ from roundf, first bits 0x%08x\n", res[1], res[0], first);
+    return Q1_MISMATCH;
+  }
+  rep.add("q8 rounding by adds: all %llu floats with |t| < 2^22 equal roundf\n", res[0]);
+  return Q1_OK;
+}
+
 }  // namespace
 }  // namespace q1
 
@@ -332,6 +376,11 @@ extern "C" int q1_0_verify(int flags, char* report, size_t report_len) {
   const Case* cs = (flags & 1) ? quick : full;
   const size_t nc = (flags & 1) ? sizeof quick / sizeof quick[0] : sizeof full / sizeof full[0];
   int status = Q1_OK;
+  if (!(flags & 1)) {
+    const int e = run_round_check(rep);
+    if (e < 0) return e;
+    if (e == Q1_MISMATCH) status = Q1_MISMATCH;
+  }
   for (size_t i = 0; i < nc; ++i) {
     int e = run_case(cs[i], 0x51ED5EEDull + 7919ull * i, (flags & 2) != 0, rep);
     if (e < 0) {

@@ -60,6 +60,9 @@ def test_library_self_check():
     rc, report = binding.verify(quick=False)
     assert rc == binding.Q1_OK, report
     lines = report.strip().splitlines()
+    # first the exhaustive check of the kernels' quantizer rounding (all floats |t| < 2^22)
+    assert lines[0] == "q8 rounding by adds: all 2499805184 floats with |t| < 2^22 equal roundf", report
+    lines = lines[1:]
     assert len(lines) == 15 and all(line.endswith("bit-exact") for line in lines), report
     # both matrix-vector kernels: the last two shapes have too many rows for the panel kernel
     assert binding.multi_plan([(40000, 256)])["panel_warps"] == 0
