@@ -21,6 +21,9 @@ int fail(int code, const char* fmt, ...) {
 
 int cuda_status(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return Q1_OK;
+  // The runtime also keeps the error in the thread's last-error slot; read it
+  // here, so that a later launch check does not report it as its own.
+  (void)cudaGetLastError();
   return fail(Q1_ERR_CUDA, "%s: CUDA error %d (%s)", what, (int)e, cudaGetErrorString(e));
 }
 

@@ -101,6 +101,17 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 int fail(int code, const char* fmt, ...);
 // Checks a CUDA runtime status after a launch; records and maps errors.
 int cuda_status(cudaError_t e, const char* what);
+// A plain launch (no attributes) whose status is that of this launch alone:
+// unlike a <<<>>> launch checked with cudaGetLastError, an error an earlier
+// call left behind is not taken for this launch's.
+template <typename... KArgs, typename... Args>
+int launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, const char* who, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, args...), who);
+}
 // SM count of the current device (cached per device).
 int num_sms();
 // Argument checks of one q1_product (shape, pointers, 16-byte alignment).

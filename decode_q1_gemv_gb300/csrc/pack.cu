@@ -180,10 +180,7 @@ static int pack_checked(const char* who, int64_t nb, cudaStream_t s, Launch&& la
   PackReject* rec = nullptr;
   if (int e = cuda_status(cudaMallocAsync(reinterpret_cast<void**>(&rec), sizeof(PackReject), s), who)) return e;
   int rc = cuda_status(cudaMemsetAsync(rec, 0xff, sizeof(PackReject), s), who);
-  if (rc == Q1_OK) {
-    launch(rec);
-    rc = cuda_status(cudaGetLastError(), who);
-  }
+  if (rc == Q1_OK) rc = launch(rec);
   PackReject host = {~0ull, ~0ull};
   if (rc == Q1_OK) rc = cuda_status(cudaMemcpyAsync(&host, rec, sizeof host, cudaMemcpyDeviceToHost, s), who);
   const int rf = cuda_status(cudaFreeAsync(rec, s), who);
@@ -217,7 +214,8 @@ extern "C" int q1_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* p
   int64_t grid = (total + threads - 1) / threads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return pack_checked("q1_0_pack", L.nb, s, [&](PackReject* rec) {
-    k_pack<<<dim3(unsigned(grid)), threads, 0, s>>>(blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales, rec);
+    return launch_plain(k_pack, dim3(unsigned(grid)), dim3(threads), s, "q1_0_pack launch", blocks, rows, L.nb, L.nbp,
+                        L.rows_pad, bits, scales, rec);
   });
 }
 
@@ -230,9 +228,8 @@ extern "C" int q1_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t*
   int64_t total = rows * L.nb;
   int threads = 256;
   int64_t grid = (total + threads - 1) / threads;
-  k_unpack<<<dim3(unsigned(grid)), threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      bits, scales, rows, L.nb, L.nbp, blocks);
-  return cuda_status(cudaGetLastError(), "q1_0_unpack launch");
+  return launch_plain(k_unpack, dim3(unsigned(grid)), dim3(threads), static_cast<cudaStream_t>(stream),
+                      "q1_0_unpack launch", bits, scales, rows, L.nb, L.nbp, blocks);
 }
 
 extern "C" int q2_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* packed, void* stream) {
@@ -245,7 +242,8 @@ extern "C" int q2_0_pack(const uint8_t* blocks, int64_t rows, int64_t n, void* p
   int64_t grid = (total + threads - 1) / threads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return pack_checked("q2_0_pack", L.nb, s, [&](PackReject* rec) {
-    k_pack_q2<<<dim3(unsigned(grid)), threads, 0, s>>>(blocks, rows, L.nb, L.nbp, L.rows_pad, bits, scales, rec);
+    return launch_plain(k_pack_q2, dim3(unsigned(grid)), dim3(threads), s, "q2_0_pack launch", blocks, rows, L.nb,
+                        L.nbp, L.rows_pad, bits, scales, rec);
   });
 }
 
@@ -258,7 +256,6 @@ extern "C" int q2_0_unpack(const void* packed, int64_t rows, int64_t n, uint8_t*
   int64_t total = rows * L.nb;
   int threads = 256;
   int64_t grid = (total + threads - 1) / threads;
-  k_unpack_q2<<<dim3(unsigned(grid)), threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      bits, scales, rows, L.nb, L.nbp, blocks);
-  return cuda_status(cudaGetLastError(), "q2_0_unpack launch");
+  return launch_plain(k_unpack_q2, dim3(unsigned(grid)), dim3(threads), static_cast<cudaStream_t>(stream),
+                      "q2_0_unpack launch", bits, scales, rows, L.nb, L.nbp, blocks);
 }

@@ -288,8 +288,7 @@ int run_wait_probe(Report& rep) {
   auto* d_res = static_cast<unsigned long long*>(dev.get(16));
   if (!d_res) return fail(Q1_ERR_NOMEM, "q1_0_verify: device allocation failed");
   const unsigned long long limit = 20000000ull;  // 20 ms
-  k_wait_probe<<<1, 32>>>(limit, d_res);
-  if (int e = cuda_status(cudaGetLastError(), "q1_0_verify wait probe")) return e;
+  if (int e = launch_plain(k_wait_probe, dim3(1), dim3(32), nullptr, "q1_0_verify wait probe", limit, d_res)) return e;
   unsigned long long res[2] = {0, 0};
   if (int e = cuda_status(cudaMemcpy(res, d_res, 16, cudaMemcpyDeviceToHost), "q1_0_verify wait probe")) return e;
   if (res[0] != 0 || res[1] < limit) {
@@ -330,8 +329,9 @@ int run_round_check(Report& rep) {
   if (!d_res || !d_first) return fail(Q1_ERR_NOMEM, "q1_0_verify: device allocation failed");
   if (int e = cuda_status(cudaMemset(d_res, 0, 16), "q1_0_verify rounding check")) return e;
   if (int e = cuda_status(cudaMemset(d_first, 0xff, 4), "q1_0_verify rounding check")) return e;
-  k_round_check<<<num_sms() * 8, 256>>>(d_res, d_first);
-  if (int e = cuda_status(cudaGetLastError(), "q1_0_verify rounding check")) return e;
+  if (int e = launch_plain(k_round_check, dim3(unsigned(num_sms() * 8)), dim3(256), nullptr,
+                           "q1_0_verify rounding check", d_res, d_first))
+    return e;
   unsigned long long res[2] = {0, 0};
   unsigned first = 0;
   if (int e = cuda_status(cudaMemcpy(res, d_res, 16, cudaMemcpyDeviceToHost), "q1_0_verify rounding check")) return e;
