@@ -217,11 +217,21 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile 
   if (mbar_try(bar, parity)) return true;
   return tc_wait_slow(bar, parity, abort_flag);
 }
-// Lane 0 waits; the outcome is the warp's.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane) {
-  int ok = 1;
-  if (lane == 0) ok = tc_wait(bar, parity, abort_flag) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+// Every lane of the warp waits (each then holds the barrier's acquire); the
+// warp goes on when all have seen the phase complete, and gives up with them.
+// In the common case the phase is already complete: one poll and one vote.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  bool done = mbar_try(bar, parity);
+  if (!done) done = tc_wait_slow(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, done);
+}
+// Slot index and phase bit of a ring of N, advanced one position.
+template <int N>
+__device__ __forceinline__ void ring_next(int& slot, uint32_t& phase) {
+  if (++slot == N) {
+    slot = 0;
+    phase ^= 1u;
+  }
 }
 
 // Integer multiply-add on the FMA pipe (the ALU pipe carries the masks).
@@ -271,22 +281,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(bar(kBarWFull + s), 1);
-      mbar_init(bar(kBarWEmpty + s), kEpiWarps + kBuildWarps);
+      mbar_init(bar(kBarWEmpty + s), 32 * (kEpiWarps + kBuildWarps));
     }
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(bar(kBarBFull + s), 1);
-      mbar_init(bar(kBarBEmpty + s), kEpiWarps);
+      mbar_init(bar(kBarBEmpty + s), 32 * kEpiWarps);
     }
     for (int s = 0; s < kASlots; ++s) {
-      mbar_init(bar(kBarAFull + s), kBuildWarps);
+      mbar_init(bar(kBarAFull + s), 32 * kBuildWarps);
       mbar_init(bar(kBarAFree + s), kIssuers);
     }
     for (int s = 0; s < kDSlots; ++s) {
       mbar_init(bar(kBarDFull + s), kIssuers);
-      mbar_init(bar(kBarDEmpty + s), kEpiWarps);
+      mbar_init(bar(kBarDEmpty + s), 32 * kEpiWarps);
     }
-    mbar_init(bar(kBarPartFull), kEpiWarps);
-    mbar_init(bar(kBarPartFree), kEpiWarps);
+    // Barriers the row workers release are arrived on by every lane of their
+    // warps (each lane after its own accesses), the others by one thread.
+    mbar_init(bar(kBarPartFull), 32 * kEpiWarps);
+    mbar_init(bar(kBarPartFree), 32 * kEpiWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -345,15 +357,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     // Warp kIssuerWarp0 + l, lane 0: lane l of every block.
     const int l = warp - kIssuerWarp0;
     const uint32_t idesc = idesc_f16(kTcRows, kTcV);
-    int it = 0, last = -1;
+    int it = 0, last = -1, last_dsl = 0;
+    uint32_t last_dph = 0;
     bool ok = true;
     if (lane == 0) {
+      int asl = 0, dsl = 0, s2 = 0;
+      uint32_t aph = 0, dph = 0, bph = 0;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         for (int b = 0; b < a.nb; ++b, ++it) {
-          const int asl = it % kASlots, dsl = it % kDSlots, s2 = it % kBStages;
-          if (!tc_wait(bar(kBarAFull + asl), uint32_t(it / kASlots) & 1u, abort_flag) ||
-              (it >= kDSlots && !tc_wait(bar(kBarDEmpty + dsl), uint32_t(it / kDSlots - 1) & 1u, abort_flag)) ||
-              !tc_wait(bar(kBarBFull + s2), uint32_t(it / kBStages) & 1u, abort_flag)) {
+          if (!tc_wait(bar(kBarAFull + asl), aph, abort_flag) ||
+              (it >= kDSlots && !tc_wait(bar(kBarDEmpty + dsl), dph ^ 1u, abort_flag)) ||
+              !tc_wait(bar(kBarBFull + s2), bph, abort_flag)) {
             ok = false;
             break;
           }
@@ -368,18 +382,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
           mma_commit(bar(kBarDFull + dsl));
           mma_commit(bar(kBarAFree + asl));
           last = it;
+          last_dsl = dsl;
+          last_dph = dph;
+          ring_next<kASlots>(asl, aph);
+          ring_next<kDSlots>(dsl, dph);
+          ring_next<kBStages>(s2, bph);
         }
       }
       // After an abort, this issuer's MMAs may still be running: let them
       // finish (bounded) before the tensor memory is released.
-      if (!ok && last >= 0) mbar_wait(bar(kBarDFull + last % kDSlots), uint32_t(last / kDSlots) & 1u, 100000000ull);
+      if (!ok && last >= 0) mbar_wait(bar(kBarDFull + last_dsl), last_dph, 100000000ull);
     }
     __syncwarp();
   } else if (warp >= kBuildWarp0) {
     // ------------------------------------------------------- A builders --
     const int quarter = warp & 3;
     const uint32_t lrow = tbase + (uint32_t(quarter * 32) << 16);
-    int it = 0, wq = 0;
+    int it = 0, ws = 0, asl = 0;
+    uint32_t wph = 0, aph = 0;
     bool ok = true;
     uint4 wq4[4];
 #pragma unroll
@@ -388,21 +408,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
       for (int b = 0; b < a.nb; ++b, ++it) {
         const int bq = b & 3;
         if (bq == 0) {
-          const int s = wq % kWStages;
-          if (!warp_wait(bar(kBarWFull + s), uint32_t(wq / kWStages) & 1u, abort_flag, lane)) {
+          if (!warp_wait(bar(kBarWFull + ws), wph, abort_flag)) {
             ok = false;
             break;
           }
-          const unsigned char* st = smem + kOffW + s * kWStageBytes + quarter * 2048 + lane * 64;
+          const unsigned char* st = smem + kOffW + ws * kWStageBytes + quarter * 2048 + lane * 64;
 #pragma unroll
           for (int j = 0; j < 4; ++j) wq4[j] = *reinterpret_cast<const uint4*>(st + j * 16);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarWEmpty + s));
-          ++wq;
+          mbar_arrive(bar(kBarWEmpty + ws));
+          ring_next<kWStages>(ws, wph);
         }
-        const int asl = it % kASlots;
         // The slot's previous block must be through its MMAs.
-        if (it >= kASlots && !warp_wait(bar(kBarAFree + asl), uint32_t(it / kASlots - 1) & 1u, abort_flag, lane)) {
+        if (it >= kASlots && !warp_wait(bar(kBarAFree + asl), aph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -415,8 +432,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
         }
         tmem_wait_st();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarAFull + asl));
+        mbar_arrive(bar(kBarAFull + asl));
+        ring_next<kASlots>(asl, aph);
       }
     }
   } else {
@@ -425,7 +442,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     const int rt = quarter * 32 + lane;               // row within the tile = tensor-memory lane
     const uint32_t lrow = tbase + (uint32_t(quarter * 32) << 16);
     float* part = reinterpret_cast<float*>(smem + kOffPart);  // [word][vector][row]
-    int it = 0, wq = 0, units_done = 0;
+    int ws = 0, dsl = 0, s2 = 0, units_done = 0;
+    uint32_t wph = 0, dph = 0, bph = 0;
     bool ok = true;
     uint4 wv = make_uint4(0u, 0u, 0u, 0u);
     uint2 sc = make_uint2(0u, 0u);
@@ -435,25 +453,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
       float accE[kTcV], accO[kTcV];
 #pragma unroll
       for (int v = 0; v < kTcV; ++v) accE[v] = accO[v] = 0.0f;
-      for (int b = 0; b < a.nb; ++b, ++it) {
+      for (int b = 0; b < a.nb; ++b) {
         const int bq = b & 3;
         if (bq == 0) {
-          const int s = wq % kWStages;
-          if (!warp_wait(bar(kBarWFull + s), uint32_t(wq / kWStages) & 1u, abort_flag, lane)) {
+          if (!warp_wait(bar(kBarWFull + ws), wph, abort_flag)) {
             ok = false;
             break;
           }
-          const unsigned char* st = smem + kOffW + s * kWStageBytes;
+          const unsigned char* st = smem + kOffW + ws * kWStageBytes;
           wv = *reinterpret_cast<const uint4*>(st + quarter * 2048 + (lane * 16 + w * 4) * 4);
           sc = *reinterpret_cast<const uint2*>(st + 4 * 2048 + quarter * 256 + lane * 8);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarWEmpty + s));
-          ++wq;
+          mbar_arrive(bar(kBarWEmpty + ws));
+          ring_next<kWStages>(ws, wph);
         }
         const uint32_t W = word_of(wv, bq), D0 = scale_of(sc, bq);
-        const int dsl = it % kDSlots, s2 = it % kBStages;
-        if (!warp_wait(bar(kBarDFull + dsl), uint32_t(it / kDSlots) & 1u, abort_flag, lane) ||
-            !warp_wait(bar(kBarBFull + s2), uint32_t(it / kBStages) & 1u, abort_flag, lane)) {
+        if (!warp_wait(bar(kBarDFull + dsl), dph, abort_flag) || !warp_wait(bar(kBarBFull + s2), bph, abort_flag)) {
           ok = false;
           break;
         }
@@ -469,14 +483,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
           tmem_ld16(lrow + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(w) + 16u, dv);
           tmem_wait_ld16(dv);
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarDEmpty + dsl));   // D slot free for the next block
+          mbar_arrive(bar(kBarDEmpty + dsl));   // D slot free for the next block
 #pragma unroll
           for (int v = 0; v < kTcV; ++v) accO[v] = __fmaf_rn(d0, __uint_as_float(dv[v]), accO[v]);
         } else {
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarDEmpty + dsl));
+          mbar_arrive(bar(kBarDEmpty + dsl));
           const unsigned char* tabs = smem + kOffB + s2 * kRecBytes;
           const uint4 wv1[1] = {make_uint4(W, 0u, 0u, 0u)};
           const uint2 sc1[1] = {make_uint2(D0, 0u)};
@@ -489,22 +501,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
             accO[v] = aO[0];
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarBEmpty + s2));
+        mbar_arrive(bar(kBarBEmpty + s2));
+        ring_next<kDSlots>(dsl, dph);
+        ring_next<kBStages>(s2, bph);
       }
       if (!ok) break;
       // Horizontal sum: word w holds (a_w, a_w+4); the four words meet in
       // shared memory: ((a0+a4) + (a2+a6)) + ((a1+a5) + (a3+a7)).
-      if (units_done > 0 &&
-          !warp_wait(bar(kBarPartFree), uint32_t(units_done - 1) & 1u, abort_flag, lane)) {
+      if (units_done > 0 && !warp_wait(bar(kBarPartFree), uint32_t(units_done - 1) & 1u, abort_flag)) {
         ok = false;
         break;
       }
 #pragma unroll
       for (int v = 0; v < kTcV; ++v) part[(w * kTcV + v) * kTcRows + rt] = __fadd_rn(accE[v], accO[v]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPartFull));
-      if (!warp_wait(bar(kBarPartFull), uint32_t(units_done) & 1u, abort_flag, lane)) {
+      mbar_arrive(bar(kBarPartFull));
+      if (!warp_wait(bar(kBarPartFull), uint32_t(units_done) & 1u, abort_flag)) {
         ok = false;
         break;
       }
@@ -516,8 +527,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
         const int vv = g * kTcV + v;
         if (row < a.rows && vv < a.nvec) a.out[int64_t(vv) * a.rows + row] = s;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPartFree));
+      mbar_arrive(bar(kBarPartFree));
     }
   }
 
