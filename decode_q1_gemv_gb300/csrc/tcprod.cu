@@ -195,17 +195,28 @@ __global__ void __launch_bounds__(128) k_tc_prep(const int8_t* __restrict__ q, c
 }
 
 // ---------------------------------------------------------- main kernel --
+// try_wait with a suspend-time hint: the thread sleeps in the barrier unit
+// until the phase completes or about `ns` nanoseconds pass, issuing nothing
+// meanwhile.
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return done != 0;
+}
+
 // Bounded wait with a CTA-wide abort flag: false when the flag is up or after
-// about two seconds (then it raises the flag).  Between polls the thread
-// sleeps for a growing interval (32 ns up to 256 ns): polling threads would
-// otherwise take most of the issue slots the row workers need.
+// about two seconds (then it raises the flag).  Each round parks the thread in
+// the barrier (up to 20 us): polling threads would otherwise take the issue
+// slots the other roles need, and a sleep between polls would overshoot the
+// phase's completion.
 static __device__ __noinline__ bool tc_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const uint64_t t0 = globaltimer();
-  uint32_t ns = 32;
   for (;;) {
-    __nanosleep(ns);
-    if (mbar_try(bar, parity)) return true;
-    ns = ns < 256 ? 2 * ns : 256;
+    if (mbar_try_suspend(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > uint64_t(kMaxWaitNs)) {
       *abort_flag = 1;
