@@ -338,7 +338,7 @@ def fp32_roof_ops_per_s(sm_mhz=None):
     return props.multi_processor_count * 128 * mhz * 1e6
 
 
-def time_other_configs(dev, reps: int = 15):
+def time_other_configs(dev, reps: int = 15, only=None):
     import torch
     from decode_q1_gemv_gb300 import binding, synth
 
@@ -347,6 +347,8 @@ def time_other_configs(dev, reps: int = 15):
     roof = fp32_roof_ops_per_s()
     res = {}
     for ci, (name, rows, n, nvec, scale, outl) in enumerate(OTHER_CONFIGS):
+        if only and name not in only:
+            continue
         blocks = synth.weight_blocks(synth.rng_for(11, ci, 0), rows, n, scale)
         x = synth.activations(synth.rng_for(11, ci, 1), nvec, n, outliers=outl)
         packed = binding.pack(torch.from_numpy(blocks).to(dev), rows, n)
@@ -449,7 +451,8 @@ def run_configs_only(args):
     from decode_q1_gemv_gb300 import binding
 
     binding.load()
-    res = time_other_configs(torch.device("cuda", 0), reps=max(args.steps, 1))
+    only = [c for c in args.config.split(",") if c] if args.config else None
+    res = time_other_configs(torch.device("cuda", 0), reps=max(args.steps, 1), only=only)
     print(json.dumps({"other_configs_cold_l2": res}), flush=True)
     return 0
 
@@ -511,6 +514,19 @@ def run_ours(args):
         torch.cuda.synchronize()
     sampler.stop()
     step_ms = reduce_max(step_ms)
+
+    # ---- median and minimum of single replays of the timed step (the value
+    # above is the mean over the K bracketed replays)
+    singles = []
+    for _ in range(max(args.steps // 4, 10)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        singles.append(e0.elapsed_time(e1) * 1e3)
+    singles.sort()
+    set_median_us, set_min_us = singles[len(singles) // 2], singles[0]
 
     # ---- the same work under the other schedules (decode-order dependencies)
     sched_us = {"set": round(step_ms * 1e3, 2)}
@@ -610,6 +626,8 @@ def run_ours(args):
                        "l2": f"inputs larger than L2: each step streams {wb / 1e9:.3f} GB of weights",
                        "parallelism": f"replicas x{world}"},
             "us_per_set": round(step_ms * 1e3, 2),
+            "us_per_set_single_replays": {"median": round(set_median_us, 2), "min": round(set_min_us, 2),
+                                          "replays": len(singles)},
             "other_configs_cold_l2": other,
             "q2_0_decode_set": q2,
             "hbm_frac_of_measured": round(value / world / peak, 4),
@@ -618,6 +636,7 @@ def run_ours(args):
             "launches_by_schedule": {sch: ds.launches(sch) for sch in schedules},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "frac_of_nominal_8000_gbs": round(achieved / 8000.0, 4),
                          "kernel": "k_q1_multi (q1_0_gemv_multi, 225 products)", "launches_per_step": 1,
                          "algorithmic_bytes_per_launch": launch_bytes, "peak_source": peak_kind},
             "e2e": {"value": round(world * wb / (zc_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
@@ -653,6 +672,9 @@ def main():
                     help="skip timing the single-product and batched configurations")
     ap.add_argument("--configs-only", action="store_true",
                     help="time only the single-product and batched configurations (for profiling)")
+    ap.add_argument("--config", default="",
+                    help="with --configs-only: comma list of configuration names to time (" +
+                         ", ".join(c[0] for c in OTHER_CONFIGS) + "); empty for all")
     ap.add_argument("--no-q2", dest="q2", action="store_false",
                     help="skip timing the decode set with Q2_0 (ternary) weights")
     ap.add_argument("--q2-only", action="store_true",
