@@ -58,7 +58,7 @@ class MultiPlan(ctypes.Structure):
     """Mirror of q1_multi_plan (include/q1gemv.h)."""
     _fields_ = [("rows_per_thread", ctypes.c_int), ("grid", ctypes.c_int), ("total_cost", ctypes.c_int64),
                 ("max_range_cost", ctypes.c_int64), ("panel_warps", ctypes.c_int),
-                ("panel_unit_blocks", ctypes.c_int)]
+                ("panel_unit_blocks", ctypes.c_int), ("panel_panels", ctypes.c_int)]
 
 
 class Q1Error(RuntimeError):
@@ -317,7 +317,7 @@ def multi_plan(shapes, sms: int = 0, fmt: str = "q1") -> dict:
     _check(fn(arr, len(arr), int(sms), ctypes.byref(plan), cuts, len(cuts)), f"{fmt}_0_gemv_multi_plan")
     return {"rows_per_thread": plan.rows_per_thread, "grid": plan.grid, "total_cost": plan.total_cost,
             "max_range_cost": plan.max_range_cost, "panel_warps": plan.panel_warps,
-            "panel_unit_blocks": plan.panel_unit_blocks,
+            "panel_unit_blocks": plan.panel_unit_blocks, "panel_panels": plan.panel_panels,
             "cuts": list(cuts[:plan.grid + 1]) if plan.panel_warps == 0 else []}
 
 

@@ -36,6 +36,7 @@ struct FmtQ2 {
 struct PanelConfig {
   int warps = 0;  // W: 16, 8 or 4
   int unit = 0;   // blocks per work unit: 4 (a quad) or 2 (half a quad)
+  int ppc = 1;    // consecutive panels of a product per CTA
 };
 template <class F>
 PanelConfig panel_config(const q1_product* prods, int count, int sms);

@@ -458,6 +458,7 @@ static int report_plan(const q1_product* prods, int count, int sms, q1_multi_pla
   out->rows_per_thread = R;
   out->panel_warps = 0;
   out->panel_unit_blocks = 0;
+  out->panel_panels = 0;
   out->grid = grid;
   out->total_cost = a->total_cost;
   out->max_range_cost = 0;
@@ -584,14 +585,15 @@ static int multi_plan(const char* who, const q1_product* products, int count, in
   const int n_sms = sms > 0 ? sms : num_sms();
   const PanelConfig c = panel_config<F>(products, count, n_sms);
   if (c.warps) {
-    int64_t panels = 0;
-    for (int j = 0; j < count; ++j) panels += F::layout(products[j].rows, products[j].n).panels;
+    int64_t ctas = 0;
+    for (int j = 0; j < count; ++j) ctas += (F::layout(products[j].rows, products[j].n).panels + c.ppc - 1) / c.ppc;
     plan->rows_per_thread = 4;
-    plan->grid = int(panels);
+    plan->grid = int(ctas);
     plan->total_cost = 0;
     plan->max_range_cost = 0;
     plan->panel_warps = c.warps;
     plan->panel_unit_blocks = c.unit;
+    plan->panel_panels = c.ppc;
     return Q1_OK;
   }
   if (count == 1) return dispatch_plan<1, F>(products, count, n_sms, plan, cuts, max_cuts);

@@ -37,6 +37,8 @@ constexpr int kPanelSmemPerSm = 233472;  // shared memory of an SM
 constexpr int kPanelSmemPerCta = 1024;   // reserved by the system per resident CTA
 
 constexpr int kPanelMaxProducts = 8;
+constexpr int kPanelMaxPpc = 8;          // panels a CTA takes at most
+constexpr int kPanelSmemMax = kPanelSmemPerSm - kPanelSmemPerCta;  // a CTA's dynamic shared memory at most
 
 struct PanelProd {
   const uint8_t* packed;
@@ -46,15 +48,20 @@ struct PanelProd {
   float* out;
   int64_t bits_bytes;
   int rows, nb, nbp;
+  int panels;            // panels of the product (rows padded to panel groups)
   int panel_begin;       // first CTA of this product
 };
 struct PanelArgs {
   PanelProd p[kPanelMaxProducts];
   int count;
+  int ppc;      // consecutive panels of a product per CTA (1: each warp builds its own table entries)
   L2Ranges pf;  // pulled into L2 while this launch runs (the next launch's inputs)
 };
 
-__host__ __device__ constexpr int panel_smem_bytes(int nbp) { return nbp * kPanelBytesPerBlock; }
+// Shared memory: one table for the row, and ab + d0 for each of the CTA's panels.
+__host__ __device__ constexpr int panel_smem_bytes(int nbp, int ppc = 1) {
+  return nbp * 4 * (4 * 16 + 16) + ppc * nbp * (128 * 8 + 32 * 4);
+}
 
 // fp16 scale w (0..3) of a quad held as 4 halves in a uint2.
 __device__ __forceinline__ float quad_scale_at(const uint2& v, int w) {
@@ -119,36 +126,42 @@ __host__ __device__ constexpr int panel_ctas_by_regs(int W) {
 // half quads, for rows of few quads, so that more warps get work).  Warp k
 // takes the contiguous units [k m, k m + m) (m = ceil(units / W)), four rows a
 // thread, keeps the words of PF units in flight, and builds the activation
-// table entries of its own blocks.
-template <class F, int W, int PF, int UB>
+// table entries of its own blocks.  A CTA may take a.ppc consecutive panels
+// of one product (the units of all of them, panel by panel): it then builds
+// the whole table once, with all its threads, before the quad steps.
+template <class F, int W, int PF, int UB, bool MP>
 __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(const __grid_constant__ PanelArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   int j = 0;  // this CTA's product: panels are numbered across the products in list order
   while (j + 1 < a.count && int(blockIdx.x) >= a.p[j + 1].panel_begin) ++j;
   const PanelProd& pr = a.p[j];
+  const int ppc = MP ? a.ppc : 1;  // the one-panel instance keeps the unit arithmetic compile-time
   const int nbp = pr.nbp, nu = nbp / UB;
   unsigned char* table = smem;
-  float2* ab = reinterpret_cast<float2*>(smem + table_bytes(nbp));  // [block][row][word]
-  float* d0s = reinterpret_cast<float*>(ab + nbp * 128);            // [block][row]
+  float2* ab = reinterpret_cast<float2*>(smem + table_bytes(nbp));  // [panel][block][row][word]
+  float* d0s = reinterpret_cast<float*>(ab + ppc * nbp * 128);      // [panel][block][row]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r0 = lane >> 2, w = lane & 3;  // rows r0 + 8j of the panel, word w
-  const int64_t p = int(blockIdx.x) - pr.panel_begin;  // panel within the product
+  const int64_t p0 = int64_t(int(blockIdx.x) - pr.panel_begin) * ppc;  // first panel of this CTA
+  const int np = !MP ? 1 : pr.panels - int(p0) < ppc ? pr.panels - int(p0) : ppc;  // its panels
+  const int nunits = np * nu;
   const uint8_t* bits = pr.packed;
   const uint8_t* scales = pr.packed + pr.bits_bytes;
-  const int m = (nu + W - 1) / W;
-  const int u0 = warp * m < nu ? warp * m : nu;
-  const int mine = u0 + m < nu ? m : nu - u0;  // units [u0, u0 + mine) of this warp
+  const int m = (nunits + W - 1) / W;
+  const int u0 = warp * m < nunits ? warp * m : nunits;
+  const int mine = u0 + m < nunits ? m : nunits - u0;  // units [u0, u0 + mine) of this warp
 
   // Sign words are loaded ahead; the block scales, needed only when a unit's
-  // products are stored, are loaded as its step starts.  Unit u is quad
-  // u UB / 4, blocks (u UB) % 4 .. + UB - 1 of it.
+  // products are stored, are loaded as its step starts.  Unit u is of panel
+  // u / nu; within it, quad uu UB / 4, blocks (uu UB) % 4 .. + UB - 1
+  // (uu = u % nu).
   uint4 wv[PF][4], nv[PF][4];
   auto load = [&](int i0) {
 #pragma unroll
     for (int v = 0; v < PF; ++v) {
       if (i0 + v < mine) {
-        const int u = u0 + i0 + v, qd = u * UB / 4, h = (u * UB) % 4 / 2;
-        const uint8_t* rec = bits + F::quad_bits_offset(p, qd, nbp);
+        const int u = u0 + i0 + v, pi = MP ? u / nu : 0, uu = u - pi * nu, qd = uu * UB / 4, h = (uu * UB) % 4 / 2;
+        const uint8_t* rec = bits + F::quad_bits_offset(p0 + pi, qd, nbp);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int word = (r0 + 8 * j) * 4 + w;
@@ -173,12 +186,18 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
   if (tid == 32 * W - 32) l2_prefetch_share(a.pf, int(blockIdx.x), int(gridDim.x));
 
   pdl_wait();  // the activation may be written by the preceding kernel
-  if (mine > 0) {  // this warp's own table entries: blocks UB u0 .. UB (u0 + mine) - 1
-    // Inlined, so that the sign-word loads above stay in flight meanwhile.
-    if (pr.x) table_x_body<2, typename F::Consts>(pr.x, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
-    else table_q_body<4, typename F::Consts>(pr.q, pr.d, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
+  if (!MP) {
+    if (mine > 0) {  // this warp's own table entries: blocks UB u0 .. UB (u0 + mine) - 1
+      // Inlined, so that the sign-word loads above stay in flight meanwhile.
+      if (pr.x) table_x_body<2, typename F::Consts>(pr.x, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
+      else table_q_body<4, typename F::Consts>(pr.q, pr.d, pr.nb, UB * u0, UB * mine, table, lane, 32, nbp, UB * u0);
+    }
+    __syncwarp();
+  } else {  // the whole table, once for the CTA's panels, by all its threads
+    if (pr.x) table_x_body<2, typename F::Consts>(pr.x, pr.nb, 0, nbp, table, tid, 32 * W, nbp, 0);
+    else table_q_body<4, typename F::Consts>(pr.q, pr.d, pr.nb, 0, nbp, table, tid, 32 * W, nbp, 0);
+    __syncthreads();
   }
-  __syncwarp();
 
   const uint4* QC = reinterpret_cast<const uint4*>(table);
   const float4* DK = reinterpret_cast<const float4*>(table + table_dk_offset(nbp));
@@ -187,26 +206,30 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
 #pragma unroll
     for (int v = 0; v < PF; ++v) {
       if (i0 + v < mine) {
-        const int u = u0 + i0 + v, qd = u * UB / 4, h = (u * UB) % 4 / 2, b0 = u * UB;
-        const uint2* srec = reinterpret_cast<const uint2*>(scales + quad_scales_offset(p, qd, nbp));
+        const int u = u0 + i0 + v, pi = MP ? u / nu : 0, uu = u - pi * nu, qd = uu * UB / 4, h = (uu * UB) % 4 / 2;
+        const int b0 = uu * UB;
+        const uint2* srec = reinterpret_cast<const uint2*>(scales + quad_scales_offset(p0 + pi, qd, nbp));
         uint2 sc[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if constexpr (UB == 4) sc[j] = __ldg(srec + r0 + 8 * j);
           else sc[j] = make_uint2(__ldg(reinterpret_cast<const uint32_t*>(srec + r0 + 8 * j) + h), 0u);
         }
-        unit_ab<F, UB>(wv[v], nv[v], sc, QC + b0 * 16, DK + b0 * 4, w, r0, ab + b0 * 128, d0s + b0 * 32);
+        unit_ab<F, UB>(wv[v], nv[v], sc, QC + b0 * 16, DK + b0 * 4, w, r0, ab + (pi * nbp + b0) * 128,
+                       d0s + (pi * nbp + b0) * 32);
       }
     }
   }
   pdl_launch_dependents();
   __syncthreads();
 
-  if (tid < 128) {  // outer chain over all blocks in order: row, lanes w and w + 4
-    const int row = tid >> 2;
+  // Outer chain over all blocks in order: (panel, row, word) per thread,
+  // lanes w and w + 4 (idx % 4 == lane % 4 == w: 32 W is a multiple of 4).
+  for (int idx = tid; idx < np * 128; idx += 32 * W) {
+    const int pi = idx >> 7, row = (idx & 127) >> 2;
     float accE = 0.0f, accO = 0.0f;
-    const float2* abr = ab + row * 4 + w;
-    const float* d0r = d0s + row;
+    const float2* abr = ab + pi * nbp * 128 + row * 4 + w;
+    const float* d0r = d0s + pi * nbp * 32 + row;
     // Four blocks at a time, the next four loaded while these are chained.
     float2 v[4];
     float dd[4];
@@ -236,28 +259,30 @@ __global__ void __launch_bounds__(32 * W, panel_ctas_by_regs<F>(W)) k_q1_panel(c
       }
     }
     const float sum = row_sum(accE, accO);
-    const int64_t r = p * kPanel + row;
+    const int64_t r = (p0 + pi) * kPanel + row;
     if (w == 0 && r < pr.rows) pr.out[r] = sum;
   }
 }
 
-template <class F, int W, int UB>
-int launch_panel_w(const q1_product* prods, int count, cudaStream_t s, const char* who, const L2Ranges& pf) {
+template <class F, int W, int UB, bool MP>
+int launch_panel_w(const q1_product* prods, int count, int ppc, cudaStream_t s, const char* who,
+                   const L2Ranges& pf) {
   constexpr int PF = 2;
   static bool attr_done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (!attr_done[dev]) {
-    if (int e = cuda_status(cudaFuncSetAttribute(k_q1_panel<F, W, PF, UB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 panel_smem_bytes(kPanelMaxNbp)),
+    if (int e = cuda_status(cudaFuncSetAttribute(k_q1_panel<F, W, PF, UB, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kPanelSmemMax),
                             "cudaFuncSetAttribute"))
       return e;
     attr_done[dev] = true;
   }
   PanelArgs a = {};
   a.count = count;
+  a.ppc = ppc;
   a.pf = pf;
-  int panels = 0, nbp_max = 0;
+  int ctas = 0, nbp_max = 0;
   for (int j = 0; j < count; ++j) {
     const q1_product& pr = prods[j];
     const Layout L = F::layout(pr.rows, pr.n);
@@ -271,31 +296,39 @@ int launch_panel_w(const q1_product* prods, int count, cudaStream_t s, const cha
     d.rows = int(pr.rows);
     d.nb = int(L.nb);
     d.nbp = int(L.nbp);
-    d.panel_begin = panels;
-    panels += int(L.panels);
+    d.panels = int(L.panels);
+    d.panel_begin = ctas;
+    ctas += (d.panels + ppc - 1) / ppc;
     nbp_max = nbp_max > d.nbp ? nbp_max : d.nbp;
   }
+  if (panel_smem_bytes(nbp_max, ppc) > kPanelSmemMax)
+    return fail(Q1_ERR_ARG, "%s: %d panels of %d blocks a CTA exceed the shared memory", who, ppc, nbp_max);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(panels));
+  cfg.gridDim = dim3(unsigned(ctas));
   cfg.blockDim = dim3(unsigned(32 * W));
-  cfg.dynamicSmemBytes = size_t(panel_smem_bytes(nbp_max));
+  cfg.dynamicSmemBytes = size_t(panel_smem_bytes(nbp_max, ppc));
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_panel<F, W, PF, UB>, a), who);
+  return cuda_status(cudaLaunchKernelEx(&cfg, k_q1_panel<F, W, PF, UB, MP>, a), who);
 }
 
 // The kernel's shape for a list of products, or {0, 0}: the most warps W
 // (16, 8, 4; starting from the longest row's quads rounded up) whose grid of
 // one CTA per panel of every product is one wave; then half-quad units, and
 // twice the warps where that still fits, when they lower the work of the
-// busiest warp.  A list that no shape runs in one wave takes the panel kernel
-// in two waves when it has more than one product (gate and up together), at
-// the W with the least work per SM; a single product, or more panels than two
-// waves, goes to the streaming kernel.
+// busiest warp.  When no such shape fits one wave, one CTA of 16 warps per SM
+// takes P consecutive panels of a product and builds the activation table
+// once for them: the smallest P from ceil(panels / SMs) (at most 8) whose grid
+// (ceil(panels_j / P) over the products) is one wave of one CTA per SM and
+// whose shared memory fits, with half-quad units when they lower the work of
+// the busiest warp (gate and up together: 896 panels, six a CTA).  Failing
+// that, a list of two or more products runs one CTA per panel in two waves,
+// at the W with the least work per SM; a single product, or more panels than
+// two waves, goes to the streaming kernel.
 template <class F>
 PanelConfig panel_config_for(const q1_product* prods, int count, int sms) {
   if (count < 1 || count > kPanelMaxProducts) return {};
@@ -322,6 +355,14 @@ PanelConfig panel_config_for(const q1_product* prods, int count, int sms) {
   for (int Wc = W0; Wc >= 4 && !W; Wc >>= 1)
     if (fits(Wc)) W = Wc;
   if (!W) {
+    for (int P = int((panels + sms - 1) / sms); P <= kPanelMaxPpc; ++P) {
+      if (panel_smem_bytes(nbp, P) > kPanelSmemMax) break;
+      int64_t ctas = 0;
+      for (int j = 0; j < count; ++j) ctas += (layout_of(prods[j].rows, prods[j].n).panels + P - 1) / P;
+      if (ctas > sms) continue;
+      const int b4 = (P * nbp / 4 + 15) / 16 * 2, b2 = (P * nbp / 2 + 15) / 16;  // busiest warp's half quads
+      return PanelConfig{16, b2 < b4 ? 2 : 4, P};
+    }
     if (count < 2) return {};
     int64_t best = 0;
     for (int Wc = W0; Wc >= 4; Wc >>= 1) {
@@ -329,11 +370,11 @@ PanelConfig panel_config_for(const q1_product* prods, int count, int sms) {
       const int64_t work = (panels + sms - 1) / sms * busiest(Wc, 4) * Wc;  // warp half-quads per SM
       if (!W || work < best) W = Wc, best = work;
     }
-    return W ? PanelConfig{W, 4} : PanelConfig{};
+    return W ? PanelConfig{W, 4, 1} : PanelConfig{};
   }
-  PanelConfig c{W, 4};
+  PanelConfig c{W, 4, 1};
   if (busiest(W, 2) < busiest(W, 4)) c.unit = 2;
-  if (2 * W <= 16 && fits(2 * W) && busiest(2 * W, 2) < busiest(c.warps, c.unit)) c = PanelConfig{2 * W, 2};
+  if (2 * W <= 16 && fits(2 * W) && busiest(2 * W, 2) < busiest(c.warps, c.unit)) c = PanelConfig{2 * W, 2, 1};
   return c;
 }
 
@@ -350,13 +391,20 @@ template <class F>
 int launch_panel(const q1_product* prods, int count, PanelConfig c, cudaStream_t s, const char* who,
                  const L2Ranges& pf) {
   if (count < 1 || count > kPanelMaxProducts) return fail(Q1_ERR_ARG, "%s: %d products for the panel kernel", who, count);
+  if (c.ppc > 1) {  // several panels a CTA: 16 warps
+    switch (c.warps * 10 + c.unit) {
+      case 164: return launch_panel_w<F, 16, 4, true>(prods, count, c.ppc, s, who, pf);
+      case 162: return launch_panel_w<F, 16, 2, true>(prods, count, c.ppc, s, who, pf);
+      default: return fail(Q1_ERR_ARG, "%s: %d warps x %d-block units for %d panels a CTA", who, c.warps, c.unit, c.ppc);
+    }
+  }
   switch (c.warps * 10 + c.unit) {
-    case 164: return launch_panel_w<F, 16, 4>(prods, count, s, who, pf);
-    case 162: return launch_panel_w<F, 16, 2>(prods, count, s, who, pf);
-    case 84: return launch_panel_w<F, 8, 4>(prods, count, s, who, pf);
-    case 82: return launch_panel_w<F, 8, 2>(prods, count, s, who, pf);
-    case 44: return launch_panel_w<F, 4, 4>(prods, count, s, who, pf);
-    case 42: return launch_panel_w<F, 4, 2>(prods, count, s, who, pf);
+    case 164: return launch_panel_w<F, 16, 4, false>(prods, count, 1, s, who, pf);
+    case 162: return launch_panel_w<F, 16, 2, false>(prods, count, 1, s, who, pf);
+    case 84: return launch_panel_w<F, 8, 4, false>(prods, count, 1, s, who, pf);
+    case 82: return launch_panel_w<F, 8, 2, false>(prods, count, 1, s, who, pf);
+    case 44: return launch_panel_w<F, 4, 4, false>(prods, count, 1, s, who, pf);
+    case 42: return launch_panel_w<F, 4, 2, false>(prods, count, 1, s, who, pf);
     default: return fail(Q1_ERR_ARG, "%s: %d warps x %d-block units per panel", who, c.warps, c.unit);
   }
 }

@@ -364,7 +364,7 @@ extern "C" int q1_0_verify(int flags, char* report, size_t report_len) {
       {"q1_0_gemm_small", 200, 4096, 16, false}, {"q1_0_gemm_small", 64, 512, 64, true},
       {"q2_0_gemv", 64, 128, 1, true},    {"q2_0_gemv", 1000, 4096, 1, false}, {"q2_0_gemv", 33, 14336, 1, true},
       // more panels than one wave of the panel kernel holds: the streaming kernel
-      {"q1_0_gemv", 40000, 256, 1, true},    {"q2_0_gemv", 20000, 256, 1, false},
+      {"q1_0_gemv", 40000, 256, 1, true},    {"q2_0_gemv", 40000, 256, 1, false},
   };
   if (flags & 4) {  // the failure path first; the shape cases after it show the context still works
     if (int e = run_wait_probe(rep)) {

@@ -191,11 +191,17 @@ typedef struct q1_multi_plan {
   int64_t max_range_cost; /* largest tile cost owned by one CTA                     */
   int panel_warps;        /* 0: the streaming kernel above.  Else the call (up to
                              8 products of few rows in total) runs as one CTA per
-                             32-row panel of each product, whose panel_warps
-                             warps share out the panel's blocks in units of
-                             panel_unit_blocks (grid = panels of all products,
-                             rows_per_thread = 4, both costs 0, no cuts) */
+                             panel_panels consecutive 32-row panels of a
+                             product, whose panel_warps warps share out those
+                             panels' blocks in units of panel_unit_blocks (grid
+                             = ceil(panels / panel_panels) summed over the
+                             products, rows_per_thread = 4, both costs 0, no
+                             cuts) */
   int panel_unit_blocks;  /* 4 (quads) or 2 (half quads); 0 with the streaming kernel */
+  int panel_panels;       /* panels a CTA takes: 1, or 2..8 when one CTA per panel
+                             would put two or more panels on an SM (the CTA then
+                             builds the activation table once for all of them);
+                             0 with the streaming kernel */
 } q1_multi_plan;
 
 int q1_0_gemv_multi_plan(const q1_product *products, int count, int sms, q1_multi_plan *plan, int64_t *cuts,

@@ -242,10 +242,44 @@ def _busiest(nbp, warps, unit):
     return -(-(nbp // unit) // warps) * (unit // 2)
 
 
+SMEM_MAX = 233472 - 1024  # a CTA's dynamic shared memory at most
+
+
+def _panel_smem(nbp, ppc):
+    return nbp * 320 + ppc * nbp * 1152
+
+
+def _expected_ppc(panel_counts, nbp, sms=152):
+    """The panels-per-CTA rule, for lists that no one-panel shape runs in one
+    wave: the smallest P >= ceil(panels / SMs) (at most 8) whose grid of
+    ceil(panels_j / P) CTAs is one CTA per SM and whose shared memory fits;
+    then 16 warps, and half-quad units when they lower the busiest warp's
+    work.  None when no P qualifies."""
+    total = sum(panel_counts)
+    for P in range(-(-total // sms), 9):
+        if _panel_smem(nbp, P) > SMEM_MAX:
+            return None
+        if sum(-(-c // P) for c in panel_counts) <= sms:
+            b4 = -(-(P * nbp // 4) // 16) * 2
+            b2 = -(-(P * nbp // 2) // 16)
+            return 16, (2 if b2 < b4 else 4), P
+    return None
+
+
+def _one_wave_widths(panels, nbp, regs):
+    return [w for w in (4, 8, 16) if panels <= max(1, min(_panel_per_sm(w, nbp, regs), 2048 // (32 * w))) * 152]
+
+
 def _check_panel_choice(plan, rows, n, regs):
     warps, unit = plan["panel_warps"], plan["panel_unit_blocks"]
     panels = -(-rows // 256) * 8
     nbp = -(-(n // 128) // 4) * 4
+    exp = None if _one_wave_widths(panels, nbp, regs) else _expected_ppc([panels], nbp)
+    if exp:
+        assert (warps, unit, plan["panel_panels"]) == exp
+        assert plan["grid"] == -(-panels // exp[2]) <= 152 and plan["rows_per_thread"] == 4
+        return
+    assert plan["panel_panels"] == 1
     assert plan["grid"] == panels and plan["rows_per_thread"] == 4 and plan["cuts"] == []
     assert panels <= _panel_per_sm(warps, nbp, regs) * 152 and nbp <= 156
     # no other (warps, unit) that fits one wave gives the busiest warp less work
@@ -256,19 +290,22 @@ def _check_panel_choice(plan, rows, n, regs):
                 assert _busiest(nbp, warps, unit) <= _busiest(nbp, w2, u2)
 
 
-@pytest.mark.parametrize("rows,n,warps,unit", [
-    (4096, 4096, 16, 2), (1024, 4096, 16, 2), (4096, 14336, 16, 4), (14336, 4096, 8, 4), (256, 1024, 4, 2),
-    (1, 128, 4, 2), (300, 384, 4, 2), (300, 1536, 8, 2), (8192, 8192, 8, 4), (18000, 4096, 4, 4),
-    (4096, 19968, 16, 2), (5000, 19968, 0, 0), (4096, 20096, 0, 0), (128256, 4096, 0, 0), (40000, 256, 0, 0)])
-def test_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
-    """A single product of few rows goes to the one-CTA-per-panel kernel:
-    W = 16, 8 or 4 warps sharing out the panel's blocks in quads or half
-    quads, the grid of one CTA per panel one wave (80 registers a thread,
-    2048 threads, 228 KB of shared memory at 1472 bytes per block plus 1 KB
-    per CTA), n at most 156 blocks, and the busiest warp as lightly loaded as
-    those limits allow."""
+@pytest.mark.parametrize("rows,n,warps,unit,ppc", [
+    (4096, 4096, 16, 2, 1), (1024, 4096, 16, 2, 1), (4096, 14336, 16, 4, 1), (14336, 4096, 8, 4, 1),
+    (256, 1024, 4, 2, 1), (1, 128, 4, 2, 1), (300, 384, 4, 2, 1), (300, 1536, 8, 2, 1), (8192, 8192, 8, 4, 1),
+    (18000, 4096, 4, 4, 1), (20000, 256, 4, 2, 1), (22000, 4096, 16, 2, 5), (30000, 1024, 16, 4, 7),
+    (4096, 19968, 16, 2, 1), (5000, 19968, 0, 0, 0), (4096, 20096, 0, 0, 0), (128256, 4096, 0, 0, 0),
+    (40000, 256, 0, 0, 0)])
+def test_multi_plan_one_product_kernel(lib, rows, n, warps, unit, ppc):
+    """A single product of few rows goes to the panel kernel: W = 16, 8 or 4
+    warps sharing out the panel's blocks in quads or half quads, the grid of
+    one CTA per panel one wave (80 registers a thread, 2048 threads, 228 KB of
+    shared memory at 1472 bytes per block plus 1 KB per CTA), n at most 156
+    blocks, and the busiest warp as lightly loaded as those limits allow; or,
+    when no such grid fits one wave, one CTA of 16 warps per SM taking several
+    consecutive panels (at most 8)."""
     plan = binding.multi_plan([(rows, n)], sms=152)
-    assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
+    assert (plan["panel_warps"], plan["panel_unit_blocks"], plan["panel_panels"]) == (warps, unit, ppc)
     if warps:
         _check_panel_choice(plan, rows, n, 80 if warps < 16 else 128)
     else:
@@ -277,14 +314,16 @@ def test_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
     assert binding.multi_plan([(rows, n), (32, 20096)], sms=152)["panel_warps"] == 0
 
 
-@pytest.mark.parametrize("rows,n,warps,unit", [
-    (4096, 4096, 16, 2), (1024, 4096, 16, 2), (4096, 14336, 16, 4), (14336, 4096, 4, 4), (1, 128, 4, 2),
-    (8192, 8192, 8, 4), (18000, 4096, 4, 4), (20000, 4096, 0, 0), (4096, 20096, 0, 0)])
-def test_q2_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
+@pytest.mark.parametrize("rows,n,warps,unit,ppc", [
+    (4096, 4096, 16, 2, 1), (1024, 4096, 16, 2, 1), (4096, 14336, 16, 4, 1), (14336, 4096, 4, 4, 1),
+    (1, 128, 4, 2, 1), (8192, 8192, 8, 4, 1), (18000, 4096, 4, 4, 1), (20000, 4096, 16, 2, 5),
+    (40000, 4096, 0, 0, 0), (4096, 20096, 0, 0, 0)])
+def test_q2_multi_plan_one_product_kernel(lib, rows, n, warps, unit, ppc):
     """The Q2_0 panel kernel keeps up to 128 registers a thread: 4 CTAs of
-    4 warps, 2 of 8 or 1 of 16 an SM by registers."""
+    4 warps, 2 of 8 or 1 of 16 an SM by registers; several panels a CTA as for
+    Q1_0."""
     plan = binding.multi_plan([(rows, n)], sms=152, fmt="q2")
-    assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
+    assert (plan["panel_warps"], plan["panel_unit_blocks"], plan["panel_panels"]) == (warps, unit, ppc)
     if warps:
         _check_panel_choice(plan, rows, n, 128)
     q1 = binding.multi_plan([(rows, n), (32, 20096)], sms=152)
@@ -292,21 +331,25 @@ def test_q2_multi_plan_one_product_kernel(lib, rows, n, warps, unit):
     assert q2 == q1 and q1["panel_warps"] == 0  # the streaming split depends on the shapes only
 
 
-@pytest.mark.parametrize("shapes,warps,unit", [
-    ([(4096, 4096), (1024, 4096), (1024, 4096)], 8, 4),     # q, k, v of one layer
-    ([(2048, 4096), (1000, 14336), (33, 128)], 16, 4),      # unequal rows and n
-    ([(300, 1024)] * 8, 4, 2),                               # eight products
-    ([(14336, 4096), (14336, 4096)], 8, 4),                  # gate and up: 896 panels, two waves
-    ([(14336, 4096)] * 3, 0, 0),                             # more than two waves
-    ([(32, 128)] * 9, 0, 0),                                 # more than eight products
-    ([(64, 4096), (32, 20096)], 0, 0)])                      # a row longer than 156 blocks
-def test_multi_plan_panel_lists(lib, shapes, warps, unit):
-    """Lists of up to 8 products whose panels together fit one wave, or two
-    waves when no shape fits one, take the panel kernel, sized by the longest
-    row and the total panels."""
+@pytest.mark.parametrize("shapes,warps,unit,ppc", [
+    ([(4096, 4096), (1024, 4096), (1024, 4096)], 8, 4, 1),   # q, k, v of one layer: 192 panels
+    ([(2048, 4096), (1000, 14336), (33, 128)], 16, 4, 1),   # unequal rows and n
+    ([(300, 1024)] * 8, 4, 2, 1),                            # eight products
+    ([(14336, 4096), (14336, 4096)], 16, 4, 6),              # gate and up: 896 panels, 6 a CTA
+    ([(20000, 1024), (20000, 1024)], 4, 4, 1),               # 1264 panels: two waves
+    ([(14336, 4096)] * 3, 0, 0, 0),                          # more than 8 panels a CTA, two waves
+    ([(32, 128)] * 9, 0, 0, 0),                              # more than eight products
+    ([(64, 4096), (32, 20096)], 0, 0, 0)])                   # a row longer than 156 blocks
+def test_multi_plan_panel_lists(lib, shapes, warps, unit, ppc):
+    """Lists of up to 8 products whose panels together fit one wave, or that
+    several panels a CTA fit in one wave of one CTA per SM, or two waves when
+    neither does, take the panel kernel, sized by the longest row and the
+    total panels."""
     plan = binding.multi_plan(shapes, sms=152)
-    assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
-    if warps:
+    assert (plan["panel_warps"], plan["panel_unit_blocks"], plan["panel_panels"]) == (warps, unit, ppc)
+    if ppc > 1:
+        assert plan["grid"] == sum(-(-(-(-r // 256) * 8) // ppc) for r, _ in shapes) <= 152
+    elif warps:
         panels = sum(-(-r // 256) * 8 for r, _ in shapes)
         nbp = max(-(-(n // 128) // 4) * 4 for _, n in shapes)
         waves = 1 if panels <= _panel_per_sm(4, nbp, 80) * 152 else 2
@@ -318,10 +361,11 @@ def test_multi_plan_panel_lists(lib, shapes, warps, unit):
 def test_multi_plan_panel_rules_random_lists(lib, fmt, regs, seed):
     """Random lists of 1-10 products: the launcher's kernel choice follows its
     stated rules.  The panel kernel only for at most 8 products with rows of at
-    most 156 blocks; one wave when any shape fits one (the busiest warp then
-    no more loaded than under any other one-wave shape); two waves only for
-    lists of two or more that fit no shape in one; the streaming kernel
-    otherwise."""
+    most 156 blocks; several panels a CTA when one CTA per panel would put two
+    or more on an SM and some P fits; else one wave when any shape fits one
+    (the busiest warp then no more loaded than under any other one-wave
+    shape); two waves only for lists of two or more that fit no shape in one;
+    the streaming kernel otherwise."""
     import random
     rnd = random.Random(1000 + seed)
     for _ in range(60):
@@ -335,10 +379,16 @@ def test_multi_plan_panel_rules_random_lists(lib, fmt, regs, seed):
         one_wave = [w for w in (4, 8, 16) if panels <= per_sm(w) * 152]
         two_wave = [w for w in (4, 8, 16) if panels <= 2 * per_sm(w) * 152]
         eligible = count <= 8 and nbp <= 156
+        exp = _expected_ppc([-(-r // 256) * 8 for r, _ in shapes], nbp) if eligible and not one_wave else None
+        if exp:
+            assert (plan["panel_warps"], plan["panel_unit_blocks"], plan["panel_panels"]) == exp, (shapes, plan)
+            assert plan["grid"] == sum(-(-(-(-r // 256) * 8) // exp[2]) for r, _ in shapes) <= 152
+            continue
         if not eligible or (not one_wave and (count < 2 or not two_wave)):
             assert plan["panel_warps"] == 0, (shapes, plan)
             continue
         assert plan["panel_warps"] in (4, 8, 16) and plan["grid"] == panels, (shapes, plan)
+        assert plan["panel_panels"] == 1, (shapes, plan)
         w, u = plan["panel_warps"], plan["panel_unit_blocks"]
         if one_wave:
             assert panels <= per_sm(w) * 152

@@ -8,8 +8,9 @@ streaming kernel.  Both must
 give the oracle's bits: every output of the two launches is compared with the
 other, and every output with the (threaded) oracle.  The shapes cover every warp
 count (16, 8, 4) with quad and half-quad work units, fewer units than warps,
-warps with several units, ragged rows, and the longest row the kernel takes
-(156 blocks).
+warps with several units, ragged rows, the longest row the kernel takes
+(156 blocks), and CTAs that take several consecutive panels of a product
+(5 and 7, with a last CTA of fewer), whose table is built once by the CTA.
 """
 import numpy as np
 import pytest
@@ -42,12 +43,13 @@ def bits_equal(got, want):
                             f"got {got.ravel()[diff[:5]]} want {want.ravel()[diff[:5]]}")
 
 
-# (rows, n, Q1_0 warps per CTA and blocks per work unit on a 152-SM GB300);
-# the test also requires that the launcher on the device it runs on picks the
-# panel kernel.
-SHAPES = [(1, 128, 4, 2), (33, 384, 4, 2), (256, 1024, 4, 2), (300, 1536, 8, 2), (3000, 2048, 8, 2),
-          (1000, 640, 4, 2), (1024, 4096, 16, 2), (4096, 4096, 16, 2), (14336, 4096, 8, 4),
-          (18000, 4096, 4, 4), (8192, 8192, 8, 4), (4096, 14336, 16, 4), (300, 19968, 16, 2)]
+# (rows, n, Q1_0 warps per CTA, blocks per work unit and panels per CTA on a
+# 152-SM GB300); the test also requires that the launcher on the device it
+# runs on picks the panel kernel.
+SHAPES = [(1, 128, 4, 2, 1), (33, 384, 4, 2, 1), (256, 1024, 4, 2, 1), (300, 1536, 8, 2, 1),
+          (3000, 2048, 8, 2, 1), (1000, 640, 4, 2, 1), (1024, 4096, 16, 2, 1), (4096, 4096, 16, 2, 1),
+          (14336, 4096, 8, 4, 1), (18000, 4096, 4, 4, 1), (8192, 8192, 8, 4, 1), (9000, 2048, 8, 2, 1),
+          (22000, 4096, 16, 2, 5), (30000, 1024, 16, 4, 7), (4096, 14336, 16, 4, 1), (300, 19968, 16, 2, 1)]
 
 
 def _run(fmt, packed, rows, n, x, q, d):
@@ -72,11 +74,11 @@ def _run(fmt, packed, rows, n, x, q, d):
     return alone.cpu().numpy(), paired.cpu().numpy()
 
 
-@pytest.mark.parametrize("rows,n,warps,unit", SHAPES)
+@pytest.mark.parametrize("rows,n,warps,unit,ppc", SHAPES)
 @pytest.mark.parametrize("act", ["f32", "q8"])
-def test_panel_q1_equals_streaming_and_oracle(rows, n, warps, unit, act):
+def test_panel_q1_equals_streaming_and_oracle(rows, n, warps, unit, ppc, act):
     plan = binding.multi_plan([(rows, n)], sms=152)
-    assert (plan["panel_warps"], plan["panel_unit_blocks"]) == (warps, unit)
+    assert (plan["panel_warps"], plan["panel_unit_blocks"], plan["panel_panels"]) == (warps, unit, ppc)
     assert binding.multi_plan([(rows, n)])["panel_warps"] > 0, "this device's launcher takes the streaming kernel"
     rng = synth.rng_for(501, rows, n, len(act))
     blocks = synth.weight_blocks(rng, rows, n, "lognormal" if rows % 2 else "halfnormal")
@@ -93,9 +95,9 @@ def test_panel_q1_equals_streaming_and_oracle(rows, n, warps, unit, act):
     bits_equal(alone, oracle.gemm_threaded(blocks, q, d)[0])
 
 
-@pytest.mark.parametrize("rows,n,warps,unit", [s for s in SHAPES if s[0] * s[1] <= 4096 * 14336])
+@pytest.mark.parametrize("rows,n,warps,unit,ppc", [s for s in SHAPES if s[0] * s[1] <= 4096 * 14336])
 @pytest.mark.parametrize("act", ["f32", "q8"])
-def test_panel_q2_equals_streaming_and_oracle(rows, n, warps, unit, act):
+def test_panel_q2_equals_streaming_and_oracle(rows, n, warps, unit, ppc, act):
     """Q2_0 keeps up to 128 registers a thread, so its warp counts can be
     lower than Q1_0's; every shape here stays within its one-wave limit."""
     assert binding.multi_plan([(rows, n)], fmt="q2")["panel_warps"] > 0
@@ -149,15 +151,17 @@ def test_panel_in_graph_with_dependent_launches():
 
 
 @pytest.mark.parametrize("shapes", [
-    [(4096, 4096), (1024, 4096), (1024, 4096)],
-    [(14336, 4096), (14336, 4096)],  # gate and up: two waves
+    [(4096, 4096), (1024, 4096), (1024, 4096)],  # q, k, v
+    [(14336, 4096), (14336, 4096)],              # gate and up: six panels a CTA
+    [(14336, 4096), (6000, 2048)],               # five a CTA, products of different n
+    [(20000, 1024), (20000, 1024)],              # one panel a CTA, two waves
     [(2048, 4096), (1000, 14336), (33, 128)],
     [(300, 1024), (7, 384), (256, 1152), (1, 128), (100, 2048), (32, 640), (500, 1024), (64, 4096)]])
 def test_panel_product_lists(shapes):
     """Several products in one panel launch (one CTA per panel of each, in
-    one wave or, for gate and up, two), f32 and q8_0 activations mixed: every
-    output against the oracle and against the same products launched one at
-    a time."""
+    one wave or two, or one CTA per several consecutive panels of a product),
+    f32 and q8_0 activations mixed: every output against the oracle and
+    against the same products launched one at a time."""
     plan = binding.multi_plan(shapes)
     assert plan["panel_warps"] > 0
     items, want, alone = [], [], []
@@ -185,11 +189,11 @@ def test_panel_product_lists(shapes):
         bits_equal(one.cpu().numpy(), w)
 
 
-def test_panel_q2_two_wave_list():
-    """Two Q2_0 products whose 752 panels need two waves of the Q2_0 panel
-    kernel (one wave of the Q1_0 one): every output against the oracle."""
+def test_panel_q2_list_several_panels_a_cta():
+    """Two Q2_0 products of 752 panels in all: five consecutive panels a CTA,
+    152 CTAs, with Q2_0's two sign planes; every output against the oracle."""
     shapes = [(12000, 2048), (12000, 2048)]
-    assert binding.multi_plan(shapes, sms=152, fmt="q2")["panel_warps"] > 0
+    assert binding.multi_plan(shapes, sms=152, fmt="q2")["panel_panels"] == 5
     assert binding.multi_plan(shapes, fmt="q2")["panel_warps"] > 0
     items, want = [], []
     for i, (rows, n) in enumerate(shapes):
