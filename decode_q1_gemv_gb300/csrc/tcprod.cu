@@ -34,14 +34,15 @@
 //
 // Structure (one persistent CTA per SM, 29 warps, stages that run
 // concurrently on different blocks):
-//   warps 16-19 A builders: warp q owns rows 32q..32q+31 of the 128-row tile
-//               (tensor-memory lanes) and turns their four sign words into the
-//               +-1 f16 A operand of all eight lanes (tensor memory), up to
-//               two blocks ahead of the MMAs.
-//   warps 20-27 MMA issuers: warp 20 + l issues the hi and lo MMAs of lane l
-//               of every block (a warp issues its MMAs one after the other,
-//               a hundred or more cycles each; separate warps issue in
-//               parallel) and commits them twice: D ready, A slot free.
+//   warps 16-23 A builders: warp 16 + 4h + q owns rows 32q..32q+31 of the
+//               128-row tile (tensor-memory lanes) and turns their sign words
+//               2h and 2h + 1 into the +-1 f16 A operand of those words' four
+//               lanes (tensor memory), up to two blocks ahead of the MMAs.
+//   warps 24-27 MMA issuers: warp 24 + l issues the hi and lo MMAs of lanes
+//               2l and 2l + 1 of every block (a warp issues its MMAs one
+//               after the other, a hundred or more cycles each; separate
+//               warps issue in parallel) and commits them twice: D ready, A
+//               slot free.
 //   warps 0-15  epilogue: warp (quarter q, word w) takes lanes w, w+4 of its
 //               32 rows from tensor memory into acc = fma(d0, ab, acc) (or runs
 //               the dp4a chain on a table block); at the end of a tile the four
@@ -75,8 +76,8 @@ constexpr int kRecBytes = 8192;          // per (group, block): 16 B tiles of 51
 constexpr int kSlowBytes = kTcV * 320;   // 16 vectors' one-block dp4a tables (table.cuh, kc = 1)
 constexpr int kEpiWarps = 16;            // warps 0-15
 constexpr int kEpi = kEpiWarps * 32;
-constexpr int kBuildWarp0 = 16, kBuildWarps = 4;
-constexpr int kIssuerWarp0 = 20, kIssuers = 8;
+constexpr int kBuildWarp0 = 16, kBuildWarps = 8;
+constexpr int kIssuerWarp0 = 24, kIssuers = 4;
 constexpr int kProducerWarp = 28;
 constexpr int kTcThreads = 29 * 32;
 constexpr int kASlots = 2, kDSlots = 3;
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     }
   } else if (warp >= kIssuerWarp0) {
     // ---------------------------------------------------------- issuers --
-    // Warp kIssuerWarp0 + l, lane 0: lane l of every block.
+    // Warp kIssuerWarp0 + l, lane 0: lanes 2l and 2l + 1 of every block.
     const int l = warp - kIssuerWarp0;
     const uint32_t idesc = idesc_f16(kTcRows, kTcV);
     int it = 0, last = -1, last_dsl = 0;
@@ -384,11 +385,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
           }
           tc_fence_after();
           if (bflag[s2]) {
-            const uint32_t bst = smem_addr(smem + kOffB + s2 * kRecBytes) + uint32_t(2 * l) * 512u;
-            const uint32_t dcol = tbase + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(l & 3) + 16u * uint32_t(l >> 2);
-            const uint32_t acol = tbase + 64u * uint32_t(asl) + 16u * uint32_t(l & 3) + 8u * uint32_t(l >> 2);
-            mma_f16_ts(dcol, acol, smem_desc(bst, 128, 256), idesc, 0u);
-            mma_f16_ts(dcol, acol, smem_desc(bst + 512, 128, 256), idesc, 1u);
+            for (int ll = 2 * l; ll < 2 * l + 2; ++ll) {  // this issuer's two lanes
+              const uint32_t bst = smem_addr(smem + kOffB + s2 * kRecBytes) + uint32_t(2 * ll) * 512u;
+              const uint32_t dcol =
+                  tbase + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(ll & 3) + 16u * uint32_t(ll >> 2);
+              const uint32_t acol = tbase + 64u * uint32_t(asl) + 16u * uint32_t(ll & 3) + 8u * uint32_t(ll >> 2);
+              mma_f16_ts(dcol, acol, smem_desc(bst, 128, 256), idesc, 0u);
+              mma_f16_ts(dcol, acol, smem_desc(bst + 512, 128, 256), idesc, 1u);
+            }
           }
           mma_commit(bar(kBarDFull + dsl));
           mma_commit(bar(kBarAFree + asl));
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     __syncwarp();
   } else if (warp >= kBuildWarp0) {
     // ------------------------------------------------------- A builders --
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, half = (warp - kBuildWarp0) >> 2;  // words 2 half, 2 half + 1
     const uint32_t lrow = tbase + (uint32_t(quarter * 32) << 16);
     int it = 0, ws = 0, asl = 0;
     uint32_t wph = 0, aph = 0;
@@ -436,7 +440,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
         }
         tc_fence_after();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * half + jj;
           uint32_t av[16];
           signs_to_f16(word_of(wq4[j], bq), av);
           tmem_st16(lrow + 64u * uint32_t(asl) + 16u * uint32_t(j), av);
