@@ -41,8 +41,8 @@
 //   warps 24-27 MMA issuers: warp 24 + l issues the hi and lo MMAs of lanes
 //               2l and 2l + 1 of every block (a warp issues its MMAs one
 //               after the other, a hundred or more cycles each; separate
-//               warps issue in parallel) and commits them twice: D ready, A
-//               slot free.
+//               warps issue in parallel) and commits them once to the
+//               block's completion barrier (D ready, A slot free).
 //   warps 0-15  epilogue: warp (quarter q, word w) takes lanes w, w+4 of its
 //               32 rows from tensor memory into acc = fma(d0, ab, acc) (or runs
 //               the dp4a chain on a table block); at the end of a tile the four
@@ -81,6 +81,7 @@ constexpr int kIssuerWarp0 = 24, kIssuers = 4;
 constexpr int kProducerWarp = 28;
 constexpr int kTcThreads = 29 * 32;
 constexpr int kASlots = 2, kDSlots = 3;
+constexpr int kMSlots = 6;  // MMA-completion barriers: block i on i % 6, a multiple of both slot counts
 constexpr int kWStages = 4;
 constexpr int kBStages = 6;
 constexpr int kWStageBytes = 4 * 2048 + 4 * 256;   // one quad of the tile's 4 panels: bits + scales
@@ -89,10 +90,10 @@ constexpr int kOffB = kOffW + kWStages * kWStageBytes;
 constexpr int kOffPart = kOffB + kBStages * kRecBytes;
 constexpr int kPartBytes = 4 * kTcV * kTcRows * 4;
 constexpr int kOffBars = kOffPart + kPartBytes;
-// barriers: wfull, wempty, bfull, bempty, afull, afree, dfull, dempty, partfull, partfree
+// barriers: wfull, wempty, bfull, bempty, afull, mdone, dempty, partfull, partfree
 constexpr int kBarWFull = 0, kBarWEmpty = kBarWFull + kWStages, kBarBFull = kBarWEmpty + kWStages,
-              kBarBEmpty = kBarBFull + kBStages, kBarAFull = kBarBEmpty + kBStages, kBarAFree = kBarAFull + kASlots,
-              kBarDFull = kBarAFree + kASlots, kBarDEmpty = kBarDFull + kDSlots,
+              kBarBEmpty = kBarBFull + kBStages, kBarAFull = kBarBEmpty + kBStages, kBarMDone = kBarAFull + kASlots,
+              kBarDEmpty = kBarMDone + kMSlots,
               kBarPartFull = kBarDEmpty + kDSlots, kBarPartFree = kBarPartFull + 1, kNumBars = kBarPartFree + 1;
 constexpr int kOffFlag = kOffBars + kNumBars * 8;
 constexpr int kOffMisc = kOffFlag + kBStages * 4;
@@ -237,6 +238,26 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   if (!done) done = tc_wait_slow(bar, parity, abort_flag);
   return __all_sync(0xffffffffu, done);
 }
+// Whether the phases with the given parities of three barriers have all
+// completed, tested side by side without waiting: each test is a round trip
+// to the barrier unit of about a hundred cycles, which an MMA issuer would
+// otherwise pay three times a block.
+__device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
+                                           uint32_t p2) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred a, b, c;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 a, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 b, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 c, [%5], %6;\n\t"
+      "and.pred a, a, b;\n\t"
+      "and.pred a, a, c;\n\t"
+      "selp.u32 %0, 1, 0, a; }"
+      : "=r"(done)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return done != 0;
+}
 // Slot index and phase bit of a ring of N, advanced one position.
 template <int N>
 __device__ __forceinline__ void ring_next(int& slot, uint32_t& phase) {
@@ -299,14 +320,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
       mbar_init(bar(kBarBFull + s), 1);
       mbar_init(bar(kBarBEmpty + s), 32 * kEpiWarps);
     }
-    for (int s = 0; s < kASlots; ++s) {
-      mbar_init(bar(kBarAFull + s), 32 * kBuildWarps);
-      mbar_init(bar(kBarAFree + s), kIssuers);
-    }
-    for (int s = 0; s < kDSlots; ++s) {
-      mbar_init(bar(kBarDFull + s), kIssuers);
-      mbar_init(bar(kBarDEmpty + s), 32 * kEpiWarps);
-    }
+    for (int s = 0; s < kASlots; ++s) mbar_init(bar(kBarAFull + s), 32 * kBuildWarps);
+    for (int s = 0; s < kMSlots; ++s) mbar_init(bar(kBarMDone + s), kIssuers);
+    for (int s = 0; s < kDSlots; ++s) mbar_init(bar(kBarDEmpty + s), 32 * kEpiWarps);
     // Barriers the row workers release are arrived on by every lane of their
     // warps (each lane after its own accesses), the others by one thread.
     mbar_init(bar(kBarPartFull), 32 * kEpiWarps);
@@ -369,17 +385,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     // Warp kIssuerWarp0 + l, lane 0: lanes 2l and 2l + 1 of every block.
     const int l = warp - kIssuerWarp0;
     const uint32_t idesc = idesc_f16(kTcRows, kTcV);
-    int it = 0, last = -1, last_dsl = 0;
-    uint32_t last_dph = 0;
+    int it = 0, last = -1, last_msl = 0;
+    uint32_t last_mph = 0;
     bool ok = true;
     if (lane == 0) {
-      int asl = 0, dsl = 0, s2 = 0;
-      uint32_t aph = 0, dph = 0, bph = 0;
+      int asl = 0, dsl = 0, s2 = 0, msl = 0;
+      uint32_t aph = 0, dph = 0, bph = 0, mph = 0;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         for (int b = 0; b < a.nb; ++b, ++it) {
-          if (!tc_wait(bar(kBarAFull + asl), aph, abort_flag) ||
-              (it >= kDSlots && !tc_wait(bar(kBarDEmpty + dsl), dph ^ 1u, abort_flag)) ||
-              !tc_wait(bar(kBarBFull + s2), bph, abort_flag)) {
+          // The A slot is built, the D slot is free (a fresh barrier counts
+          // its phase of parity 1 as complete: the first kDSlots blocks pass)
+          // and the B record has landed.
+          if (!mbar_test3(bar(kBarAFull + asl), aph, bar(kBarDEmpty + dsl), dph ^ 1u, bar(kBarBFull + s2), bph) &&
+              (!tc_wait(bar(kBarAFull + asl), aph, abort_flag) ||
+               !tc_wait(bar(kBarDEmpty + dsl), dph ^ 1u, abort_flag) ||
+               !tc_wait(bar(kBarBFull + s2), bph, abort_flag))) {
             ok = false;
             break;
           }
@@ -394,11 +414,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
               mma_f16_ts(dcol, acol, smem_desc(bst + 512, 128, 256), idesc, 1u);
             }
           }
-          mma_commit(bar(kBarDFull + dsl));
-          mma_commit(bar(kBarAFree + asl));
+          mma_commit(bar(kBarMDone + msl));  // D ready and A slot free
           last = it;
-          last_dsl = dsl;
-          last_dph = dph;
+          last_msl = msl;
+          last_mph = mph;
+          ring_next<kMSlots>(msl, mph);
           ring_next<kASlots>(asl, aph);
           ring_next<kDSlots>(dsl, dph);
           ring_next<kBStages>(s2, bph);
@@ -406,15 +426,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
       }
       // After an abort, this issuer's MMAs may still be running: let them
       // finish (bounded) before the tensor memory is released.
-      if (!ok && last >= 0) mbar_wait(bar(kBarDFull + last_dsl), last_dph, 100000000ull);
+      if (!ok && last >= 0) mbar_wait(bar(kBarMDone + last_msl), last_mph, 100000000ull);
     }
     __syncwarp();
   } else if (warp >= kBuildWarp0) {
     // ------------------------------------------------------- A builders --
     const int quarter = warp & 3, half = (warp - kBuildWarp0) >> 2;  // words 2 half, 2 half + 1
     const uint32_t lrow = tbase + (uint32_t(quarter * 32) << 16);
-    int it = 0, ws = 0, asl = 0;
-    uint32_t wph = 0, aph = 0;
+    int it = 0, ws = 0, asl = 0, msl = 0;  // msl, mph: MMA-completion barrier of block it - kASlots
+    uint32_t wph = 0, aph = 0, mph = 0;
     bool ok = true;
     uint4 wq4[4];
 #pragma unroll
@@ -434,9 +454,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
           ring_next<kWStages>(ws, wph);
         }
         // The slot's previous block must be through its MMAs.
-        if (it >= kASlots && !warp_wait(bar(kBarAFree + asl), aph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
+        if (it >= kASlots) {
+          if (!warp_wait(bar(kBarMDone + msl), mph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ring_next<kMSlots>(msl, mph);
         }
         tc_fence_after();
 #pragma unroll
@@ -458,8 +481,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     const int rt = quarter * 32 + lane;               // row within the tile = tensor-memory lane
     const uint32_t lrow = tbase + (uint32_t(quarter * 32) << 16);
     float* part = reinterpret_cast<float*>(smem + kOffPart);  // [word][vector][row]
-    int ws = 0, dsl = 0, s2 = 0, units_done = 0;
-    uint32_t wph = 0, dph = 0, bph = 0;
+    int ws = 0, dsl = 0, s2 = 0, msl = 0, units_done = 0;
+    uint32_t wph = 0, dph = 0, bph = 0, mph = 0;
     bool ok = true;
     uint4 wv = make_uint4(0u, 0u, 0u, 0u);
     uint2 sc = make_uint2(0u, 0u);
@@ -483,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
           ring_next<kWStages>(ws, wph);
         }
         const uint32_t W = word_of(wv, bq), D0 = scale_of(sc, bq);
-        if (!warp_wait(bar(kBarDFull + dsl), dph, abort_flag) || !warp_wait(bar(kBarBFull + s2), bph, abort_flag)) {
+        if (!warp_wait(bar(kBarMDone + msl), mph, abort_flag) || !warp_wait(bar(kBarBFull + s2), bph, abort_flag)) {
           ok = false;
           break;
         }
@@ -519,6 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
         }
         mbar_arrive(bar(kBarBEmpty + s2));
         ring_next<kDSlots>(dsl, dph);
+        ring_next<kMSlots>(msl, mph);
         ring_next<kBStages>(s2, bph);
       }
       if (!ok) break;
