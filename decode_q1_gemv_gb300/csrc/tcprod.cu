@@ -84,6 +84,8 @@ constexpr int kASlots = 2, kDSlots = 3;
 constexpr int kMSlots = 6;  // MMA-completion barriers: block i on i % 6, a multiple of both slot counts
 constexpr int kWStages = 4;
 constexpr int kBStages = 6;
+static_assert(kBStages == kMSlots && kMSlots == 2 * kDSlots && kMSlots == 3 * kASlots,
+              "one position (i % 6, (i / 6) & 1) gives block i's slot in every per-block ring");
 constexpr int kWStageBytes = 4 * 2048 + 4 * 256;   // one quad of the tile's 4 panels: bits + scales
 constexpr int kOffW = 0;
 constexpr int kOffB = kOffW + kWStages * kWStageBytes;
@@ -258,6 +260,28 @@ __device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1
       : "memory");
   return done != 0;
 }
+// Block i's slot and phase in the per-block rings, from m = i % 6 and
+// ph = (i / 6) & 1 (the MMA-completion ring and the B ring are both six
+// long): the D ring (three) and the A ring (two) follow.
+__device__ __forceinline__ int d_slot(int m) { return m >= 3 ? m - 3 : m; }
+__device__ __forceinline__ uint32_t d_phase(int m) { return m >= 3 ? 1u : 0u; }
+__device__ __forceinline__ int a_slot(int m) { return m & 1; }
+__device__ __forceinline__ uint32_t a_phase(int m, uint32_t ph) { return ph ^ uint32_t((m >> 1) & 1); }
+// Whether the phases with the given parities of two barriers have both
+// completed (tested side by side, without waiting).
+__device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred a, b;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 a, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 b, [%3], %4;\n\t"
+      "and.pred a, a, b;\n\t"
+      "selp.u32 %0, 1, 0, a; }"
+      : "=r"(done)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1)
+      : "memory");
+  return done != 0;
+}
 // Slot index and phase bit of a ring of N, advanced one position.
 template <int N>
 __device__ __forceinline__ void ring_next(int& slot, uint32_t& phase) {
@@ -389,10 +413,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     uint32_t last_mph = 0;
     bool ok = true;
     if (lane == 0) {
-      int asl = 0, dsl = 0, s2 = 0, msl = 0;
-      uint32_t aph = 0, dph = 0, bph = 0, mph = 0;
+      int msl = 0;
+      uint32_t mph = 0;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         for (int b = 0; b < a.nb; ++b, ++it) {
+          const int asl = a_slot(msl), dsl = d_slot(msl), s2 = msl;
+          const uint32_t aph = a_phase(msl, mph), dph = d_phase(msl), bph = mph;
           // The A slot is built, the D slot is free (a fresh barrier counts
           // its phase of parity 1 as complete: the first kDSlots blocks pass)
           // and the B record has landed.
@@ -419,9 +445,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
           last_msl = msl;
           last_mph = mph;
           ring_next<kMSlots>(msl, mph);
-          ring_next<kASlots>(asl, aph);
-          ring_next<kDSlots>(dsl, dph);
-          ring_next<kBStages>(s2, bph);
         }
       }
       // After an abort, this issuer's MMAs may still be running: let them
@@ -436,43 +459,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     int it = 0, ws = 0, asl = 0, msl = 0;  // msl, mph: MMA-completion barrier of block it - kASlots
     uint32_t wph = 0, aph = 0, mph = 0;
     bool ok = true;
-    uint4 wq4[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) wq4[j] = make_uint4(0u, 0u, 0u, 0u);
     for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-      for (int b = 0; b < a.nb; ++b, ++it) {
-        const int bq = b & 3;
-        if (bq == 0) {
-          if (!warp_wait(bar(kBarWFull + ws), wph, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const unsigned char* st = smem + kOffW + ws * kWStageBytes + quarter * 2048 + lane * 64;
+      for (int b0 = 0; b0 < a.nb; b0 += 4) {
+        // A weight quad: this warp's two sign words (each holds the word of
+        // the quad's four blocks) for its 32 rows.
+        if (!warp_wait(bar(kBarWFull + ws), wph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const unsigned char* st = smem + kOffW + ws * kWStageBytes + quarter * 2048 + lane * 64;
+        const uint4 wq0 = *reinterpret_cast<const uint4*>(st + 2 * half * 16);
+        const uint4 wq1 = *reinterpret_cast<const uint4*>(st + (2 * half + 1) * 16);
+        mbar_arrive(bar(kBarWEmpty + ws));
+        ring_next<kWStages>(ws, wph);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) wq4[j] = *reinterpret_cast<const uint4*>(st + j * 16);
-          mbar_arrive(bar(kBarWEmpty + ws));
-          ring_next<kWStages>(ws, wph);
-        }
-        // The slot's previous block must be through its MMAs.
-        if (it >= kASlots) {
-          if (!warp_wait(bar(kBarMDone + msl), mph, abort_flag)) {
-            ok = false;
-            break;
+        for (int bq = 0; bq < 4; ++bq) {  // the quad's blocks, unrolled: word and slot arithmetic fold
+          if (b0 + bq >= a.nb) break;
+          // The slot's previous block must be through its MMAs.
+          if (it >= kASlots) {
+            if (!warp_wait(bar(kBarMDone + msl), mph, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ring_next<kMSlots>(msl, mph);
           }
-          ring_next<kMSlots>(msl, mph);
-        }
-        tc_fence_after();
+          tc_fence_after();
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * half + jj;
-          uint32_t av[16];
-          signs_to_f16(word_of(wq4[j], bq), av);
-          tmem_st16(lrow + 64u * uint32_t(asl) + 16u * uint32_t(j), av);
+          for (int jj = 0; jj < 2; ++jj) {
+            uint32_t av[16];
+            signs_to_f16(word_of(jj ? wq1 : wq0, bq), av);
+            tmem_st16(lrow + 64u * uint32_t(asl) + 16u * uint32_t(2 * half + jj), av);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(kBarAFull + asl));
+          ring_next<kASlots>(asl, aph);
+          ++it;
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(kBarAFull + asl));
-        ring_next<kASlots>(asl, aph);
+        if (!ok) break;
       }
     }
   } else {
@@ -481,69 +505,71 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     const int rt = quarter * 32 + lane;               // row within the tile = tensor-memory lane
     const uint32_t lrow = tbase + (uint32_t(quarter * 32) << 16);
     float* part = reinterpret_cast<float*>(smem + kOffPart);  // [word][vector][row]
-    int ws = 0, dsl = 0, s2 = 0, msl = 0, units_done = 0;
-    uint32_t wph = 0, dph = 0, bph = 0, mph = 0;
+    int ws = 0, msl = 0, units_done = 0;
+    uint32_t wph = 0, mph = 0;
     bool ok = true;
-    uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-    uint2 sc = make_uint2(0u, 0u);
     for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++units_done) {
       if (u + int(gridDim.x) >= a.units && threadIdx.x == 0) pdl_launch_dependents();
       const int t = u / a.groups, g = u % a.groups;
       float accE[kTcV], accO[kTcV];
 #pragma unroll
       for (int v = 0; v < kTcV; ++v) accE[v] = accO[v] = 0.0f;
-      for (int b = 0; b < a.nb; ++b) {
-        const int bq = b & 3;
-        if (bq == 0) {
-          if (!warp_wait(bar(kBarWFull + ws), wph, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const unsigned char* st = smem + kOffW + ws * kWStageBytes;
-          wv = *reinterpret_cast<const uint4*>(st + quarter * 2048 + (lane * 16 + w * 4) * 4);
-          sc = *reinterpret_cast<const uint2*>(st + 4 * 2048 + quarter * 256 + lane * 8);
-          mbar_arrive(bar(kBarWEmpty + ws));
-          ring_next<kWStages>(ws, wph);
-        }
-        const uint32_t W = word_of(wv, bq), D0 = scale_of(sc, bq);
-        if (!warp_wait(bar(kBarMDone + msl), mph, abort_flag) || !warp_wait(bar(kBarBFull + s2), bph, abort_flag)) {
+      for (int b0 = 0; b0 < a.nb && ok; b0 += 4) {
+        // A weight quad: the row's word w and block scales of four blocks.
+        if (!warp_wait(bar(kBarWFull + ws), wph, abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (bflag[s2]) {
-          // The accumulator holds -ab (signs_to_f16).
-          const float d0 = -__half2float(__ushort_as_half(uint16_t(D0)));
-          uint32_t dv[16];
-          tmem_ld16(lrow + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(w), dv);
-          tmem_wait_ld16(dv);
+        const unsigned char* st = smem + kOffW + ws * kWStageBytes;
+        const uint4 wv = *reinterpret_cast<const uint4*>(st + quarter * 2048 + (lane * 16 + w * 4) * 4);
+        const uint2 sc = *reinterpret_cast<const uint2*>(st + 4 * 2048 + quarter * 256 + lane * 8);
+        mbar_arrive(bar(kBarWEmpty + ws));
+        ring_next<kWStages>(ws, wph);
 #pragma unroll
-          for (int v = 0; v < kTcV; ++v) accE[v] = __fmaf_rn(d0, __uint_as_float(dv[v]), accE[v]);
-          tmem_ld16(lrow + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(w) + 16u, dv);
-          tmem_wait_ld16(dv);
-          tc_fence_before();
-          mbar_arrive(bar(kBarDEmpty + dsl));   // D slot free for the next block
-#pragma unroll
-          for (int v = 0; v < kTcV; ++v) accO[v] = __fmaf_rn(d0, __uint_as_float(dv[v]), accO[v]);
-        } else {
-          tc_fence_before();
-          mbar_arrive(bar(kBarDEmpty + dsl));
-          const unsigned char* tabs = smem + kOffB + s2 * kRecBytes;
-          const uint4 wv1[1] = {make_uint4(W, 0u, 0u, 0u)};
-          const uint2 sc1[1] = {make_uint2(D0, 0u)};
-#pragma unroll
-          for (int v = 0; v < kTcV; ++v) {
-            float aE[1] = {accE[v]}, aO[1] = {accO[v]};
-            quad_block<1, 0>(wv1, sc1, reinterpret_cast<const uint4*>(tabs + v * 320),
-                             reinterpret_cast<const float4*>(tabs + v * 320 + 256), w, aE, aO);
-            accE[v] = aE[0];
-            accO[v] = aO[0];
+        for (int bq = 0; bq < 4; ++bq) {  // the quad's blocks, unrolled
+          if (b0 + bq >= a.nb) break;
+          const uint32_t W = word_of(wv, bq), D0 = scale_of(sc, bq);
+          const int dsl = d_slot(msl), s2 = msl;
+          // The block's MMAs are done and its B record has landed.
+          const bool ready = mbar_test2(bar(kBarMDone + msl), mph, bar(kBarBFull + s2), mph);
+          if (!__all_sync(0xffffffffu, ready) &&
+              (!warp_wait(bar(kBarMDone + msl), mph, abort_flag) || !warp_wait(bar(kBarBFull + s2), mph, abort_flag))) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          if (bflag[s2]) {
+            // The accumulator holds -ab (signs_to_f16).
+            const float d0 = -__half2float(__ushort_as_half(uint16_t(D0)));
+            uint32_t dv[16];
+            tmem_ld16(lrow + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(w), dv);
+            tmem_wait_ld16(dv);
+#pragma unroll
+            for (int v = 0; v < kTcV; ++v) accE[v] = __fmaf_rn(d0, __uint_as_float(dv[v]), accE[v]);
+            tmem_ld16(lrow + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(w) + 16u, dv);
+            tmem_wait_ld16(dv);
+            tc_fence_before();
+            mbar_arrive(bar(kBarDEmpty + dsl));   // D slot free for the next block
+#pragma unroll
+            for (int v = 0; v < kTcV; ++v) accO[v] = __fmaf_rn(d0, __uint_as_float(dv[v]), accO[v]);
+          } else {
+            tc_fence_before();
+            mbar_arrive(bar(kBarDEmpty + dsl));
+            const unsigned char* tabs = smem + kOffB + s2 * kRecBytes;
+            const uint4 wv1[1] = {make_uint4(W, 0u, 0u, 0u)};
+            const uint2 sc1[1] = {make_uint2(D0, 0u)};
+#pragma unroll
+            for (int v = 0; v < kTcV; ++v) {
+              float aE[1] = {accE[v]}, aO[1] = {accO[v]};
+              quad_block<1, 0>(wv1, sc1, reinterpret_cast<const uint4*>(tabs + v * 320),
+                               reinterpret_cast<const float4*>(tabs + v * 320 + 256), w, aE, aO);
+              accE[v] = aE[0];
+              accO[v] = aO[0];
+            }
+          }
+          mbar_arrive(bar(kBarBEmpty + s2));
+          ring_next<kMSlots>(msl, mph);
         }
-        mbar_arrive(bar(kBarBEmpty + s2));
-        ring_next<kDSlots>(dsl, dph);
-        ring_next<kMSlots>(msl, mph);
-        ring_next<kBStages>(s2, bph);
       }
       if (!ok) break;
       // Horizontal sum: word w holds (a_w, a_w+4); the four words meet in
