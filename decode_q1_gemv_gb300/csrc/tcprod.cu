@@ -312,8 +312,13 @@ __device__ __forceinline__ void signs_to_f16(uint32_t W, uint32_t (&av)[16]) {
 #pragma unroll
     for (int par = 0; par < 2; ++par) {
       const int pl = 2 * k + par;
-      av[8 * par + 2 * k] = imad(W & (0x00010001u << pl), 1u << (15 - pl), 0x3C003C00u);
-      av[8 * par + 2 * k + 1] = imad(W & (0x01000100u << pl), 1u << (7 - pl), 0x3C003C00u);
+      // Each multiplier carries a second term that moves both masked bits
+      // past bit 31, where they vanish: not a power of two, it stays an
+      // integer multiply-add on the FMA pipe instead of a shift-add on the
+      // ALU pipe, which the masks and the control code already load.
+      av[8 * par + 2 * k] =
+          imad(W & (0x00010001u << pl), (1u << (15 - pl)) + (pl > 0 ? 1u << ((32 - pl) & 31) : 0u), 0x3C003C00u);
+      av[8 * par + 2 * k + 1] = imad(W & (0x01000100u << pl), (1u << (7 - pl)) + (1u << (24 - pl)), 0x3C003C00u);
     }
   }
 }
