@@ -112,6 +112,24 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a, uint64_t bdes
       : "memory");
 }
 
+// The same MMA issued by one elected lane of a converged warp: the whole warp
+// runs the issuing code, so its operands are warp-uniform values.
+__device__ __forceinline__ void mma_f16_ts_elect(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The commit of the MMAs that the elected lane (the lowest, as above) issued.
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+      : "memory");
+}
+
 // Arrives once on the mbarrier when every tcgen05.mma this thread issued
 // before it has completed (with none outstanding, at once).
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

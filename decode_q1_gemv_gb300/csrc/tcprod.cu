@@ -411,51 +411,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     }
   } else if (warp >= kIssuerWarp0) {
     // ---------------------------------------------------------- issuers --
-    // Warp kIssuerWarp0 + l, lane 0: lanes 2l and 2l + 1 of every block.
+    // Warp kIssuerWarp0 + l: lanes 2l and 2l + 1 of every block.  The whole
+    // warp runs the loop and one elected lane issues: the slot and address
+    // arithmetic stays warp-uniform.
     const int l = warp - kIssuerWarp0;
     const uint32_t idesc = idesc_f16(kTcRows, kTcV);
-    int it = 0, last = -1, last_msl = 0;
-    uint32_t last_mph = 0;
+    int it = 0, last = -1, last_msl = 0, msl = 0;
+    uint32_t last_mph = 0, mph = 0;
     bool ok = true;
-    if (lane == 0) {
-      int msl = 0;
-      uint32_t mph = 0;
-      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-        for (int b = 0; b < a.nb; ++b, ++it) {
-          const int asl = a_slot(msl), dsl = d_slot(msl), s2 = msl;
-          const uint32_t aph = a_phase(msl, mph), dph = d_phase(msl), bph = mph;
-          // The A slot is built, the D slot is free (a fresh barrier counts
-          // its phase of parity 1 as complete: the first kDSlots blocks pass)
-          // and the B record has landed.
-          if (!mbar_test3(bar(kBarAFull + asl), aph, bar(kBarDEmpty + dsl), dph ^ 1u, bar(kBarBFull + s2), bph) &&
-              (!tc_wait(bar(kBarAFull + asl), aph, abort_flag) ||
-               !tc_wait(bar(kBarDEmpty + dsl), dph ^ 1u, abort_flag) ||
-               !tc_wait(bar(kBarBFull + s2), bph, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (bflag[s2]) {
-            for (int ll = 2 * l; ll < 2 * l + 2; ++ll) {  // this issuer's two lanes
-              const uint32_t bst = smem_addr(smem + kOffB + s2 * kRecBytes) + uint32_t(2 * ll) * 512u;
-              const uint32_t dcol =
-                  tbase + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(ll & 3) + 16u * uint32_t(ll >> 2);
-              const uint32_t acol = tbase + 64u * uint32_t(asl) + 16u * uint32_t(ll & 3) + 8u * uint32_t(ll >> 2);
-              mma_f16_ts(dcol, acol, smem_desc(bst, 128, 256), idesc, 0u);
-              mma_f16_ts(dcol, acol, smem_desc(bst + 512, 128, 256), idesc, 1u);
-            }
-          }
-          mma_commit(bar(kBarMDone + msl));  // D ready and A slot free
-          last = it;
-          last_msl = msl;
-          last_mph = mph;
-          ring_next<kMSlots>(msl, mph);
+    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+      for (int b = 0; b < a.nb; ++b, ++it) {
+        const int asl = a_slot(msl), dsl = d_slot(msl), s2 = msl;
+        const uint32_t aph = a_phase(msl, mph), dph = d_phase(msl), bph = mph;
+        // The A slot is built, the D slot is free (a fresh barrier counts
+        // its phase of parity 1 as complete: the first kDSlots blocks pass)
+        // and the B record has landed.
+        const bool ready =
+            mbar_test3(bar(kBarAFull + asl), aph, bar(kBarDEmpty + dsl), dph ^ 1u, bar(kBarBFull + s2), bph);
+        if (!__all_sync(0xffffffffu, ready) &&
+            (!warp_wait(bar(kBarAFull + asl), aph, abort_flag) ||
+             !warp_wait(bar(kBarDEmpty + dsl), dph ^ 1u, abort_flag) ||
+             !warp_wait(bar(kBarBFull + s2), bph, abort_flag))) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        if (bflag[s2]) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {  // this issuer's two lanes
+            const int ll = 2 * l + j;
+            const uint32_t bst = smem_addr(smem + kOffB + s2 * kRecBytes) + uint32_t(2 * ll) * 512u;
+            const uint32_t dcol =
+                tbase + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(ll & 3) + 16u * uint32_t(ll >> 2);
+            const uint32_t acol = tbase + 64u * uint32_t(asl) + 16u * uint32_t(ll & 3) + 8u * uint32_t(ll >> 2);
+            mma_f16_ts_elect(dcol, acol, smem_desc(bst, 128, 256), idesc, 0u);
+            mma_f16_ts_elect(dcol, acol, smem_desc(bst + 512, 128, 256), idesc, 1u);
+          }
+        }
+        mma_commit_elect(bar(kBarMDone + msl));  // D ready and A slot free
+        last = it;
+        last_msl = msl;
+        last_mph = mph;
+        ring_next<kMSlots>(msl, mph);
       }
-      // After an abort, this issuer's MMAs may still be running: let them
-      // finish (bounded) before the tensor memory is released.
-      if (!ok && last >= 0) mbar_wait(bar(kBarMDone + last_msl), last_mph, 100000000ull);
     }
+    // After an abort, this issuer's MMAs may still be running: let them
+    // finish (bounded) before the tensor memory is released.
+    if (!ok && last >= 0 && lane == 0) mbar_wait(bar(kBarMDone + last_msl), last_mph, 100000000ull);
     __syncwarp();
   } else if (warp >= kBuildWarp0) {
     // ------------------------------------------------------- A builders --
