@@ -219,12 +219,14 @@ __device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity, 
 // phase's completion.
 static __device__ __noinline__ bool tc_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const uint64_t t0 = globaltimer();
-  for (;;) {
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_suspend(bar, parity, 20000u)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > uint64_t(kMaxWaitNs)) {
-      *abort_flag = 1;
-      return false;
+    if ((i & 7) == 0) {  // the flag and the clock every eighth round: fewer instructions a round
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > uint64_t(kMaxWaitNs)) {
+        *abort_flag = 1;
+        return false;
+      }
     }
   }
 }
