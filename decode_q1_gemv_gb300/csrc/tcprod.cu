@@ -42,7 +42,14 @@
 //               2l and 2l + 1 of every block (a warp issues its MMAs one
 //               after the other, a hundred or more cycles each; separate
 //               warps issue in parallel) and commits them once to the
-//               block's completion barrier (D ready, A slot free).
+//               block's completion barrier (D ready, A slot free).  The
+//               whole warp runs the loop and one elected lane issues.
+// Each block's slot in every ring (A 2, D 3, B records 6, completion 6)
+// follows from one counter of the block index modulo 6.  The four schedulers
+// of the SM carry all 29 warps' instructions, and the non-issuing roles'
+// control code competes with the issuers for them and for the ALU pipe: the
+// quad loops are unrolled and the builders' multiply-adds kept on the FMA
+// pipe for that reason.
 //   warps 0-15  epilogue: warp (quarter q, word w) takes lanes w, w+4 of its
 //               32 rows from tensor memory into acc = fma(d0, ab, acc) (or runs
 //               the dp4a chain on a table block); at the end of a tile the four
