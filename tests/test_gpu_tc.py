@@ -178,5 +178,28 @@ def test_tensor_kernel_rejects_oversized_scratch():
         binding.gemm_small_kernel("auto")
 
 
+@pytest.mark.parametrize("kernel", ["dp4a", "tensor"])
+def test_outputs_written_once_and_guard_untouched(kernel):
+    """Ragged rows (the last 128-row tile holds 44) and a ragged vector group
+    (19 vectors: the second group of 16 holds 3): every output is written
+    with the oracle's bits and nothing past the output array changes."""
+    rows, n, nvec = 300, 1024, 19
+    rng = synth.rng_for(606)
+    blocks = synth.weight_blocks(rng, rows, n, "lognormal")
+    q, d = activations_q(rng, nvec, n, "quantized")
+    packed = binding.pack(dev(blocks), rows, n)
+    guard = 512
+    buf = torch.full((nvec * rows + guard,), float("nan"), device="cuda")
+    prev = binding.gemm_small_kernel(kernel)
+    try:
+        binding.gemm_small(packed, rows, n, dev(q), dev(d.view(np.int16)), out=buf[:nvec * rows])
+    finally:
+        binding.gemm_small_kernel(prev)
+    host = buf.cpu().numpy()
+    assert not np.any(np.isnan(host[:nvec * rows]))
+    assert np.all(np.isnan(host[nvec * rows:]))
+    bits_equal(host[:nvec * rows].reshape(nvec, rows), oracle.gemm_threaded(blocks, q, d))
+
+
 def test_device_status_clean():
     assert binding.device_status() == 0
