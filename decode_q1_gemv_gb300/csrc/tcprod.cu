@@ -378,7 +378,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
   if (warp == kProducerWarp) {
     // ------------------------------------------------------- producer --
     if (lane == 0) {
-      // The records are written by the prologue kernel.
+      auto copy_quad = [&](int s, int64_t p0, int qd) {
+        const uint32_t wf = bar(kBarWFull + s);
+        mbar_arrive_expect_tx(wf, uint32_t(kWStageBytes));
+        const uint32_t dst = smem_addr(smem + kOffW + s * kWStageBytes);
+        bulk_g2s(dst, a.bits + quad_bits_offset(p0, qd, a.nbp), 4 * 2048, wf);
+        bulk_g2s(dst + 4 * 2048, a.scales + quad_scales_offset(p0, qd, a.nbp), 4 * 256, wf);
+      };
+      // The weights do not depend on the prologue kernel: the first unit's
+      // first quads go out before waiting for it (the builders can start on
+      // them); the records and their flags are the prologue's output.
+      const int pre = blockIdx.x < unsigned(a.units) ? min(nq, kWStages) : 0;
+      for (int qd = 0; qd < pre; ++qd)
+        copy_quad(qd, int64_t(int(blockIdx.x) / a.groups) * (kTcRows / kPanel), qd);
       pdl_wait();
       int wq = 0, it = 0;
       bool ok = true;
@@ -387,15 +399,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
         const int64_t p0 = int64_t(t) * (kTcRows / kPanel);
         for (int qd = 0; qd < nq && ok; ++qd, ++wq) {
           const int s = wq % kWStages;
-          if (wq >= kWStages && !tc_wait(bar(kBarWEmpty + s), uint32_t(wq / kWStages - 1) & 1u, abort_flag)) {
-            ok = false;
-            break;
+          if (wq >= pre) {
+            if (wq >= kWStages && !tc_wait(bar(kBarWEmpty + s), uint32_t(wq / kWStages - 1) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            copy_quad(s, p0, qd);
           }
-          const uint32_t wf = bar(kBarWFull + s);
-          mbar_arrive_expect_tx(wf, uint32_t(kWStageBytes));
-          const uint32_t dst = smem_addr(smem + kOffW + s * kWStageBytes);
-          bulk_g2s(dst, a.bits + quad_bits_offset(p0, qd, a.nbp), 4 * 2048, wf);
-          bulk_g2s(dst + 4 * 2048, a.scales + quad_scales_offset(p0, qd, a.nbp), 4 * 256, wf);
           for (int bq = 0; bq < 4 && qd * 4 + bq < a.nb; ++bq, ++it) {
             const int b = qd * 4 + bq, s2 = it % kBStages;
             if (it >= kBStages && !tc_wait(bar(kBarBEmpty + s2), uint32_t(it / kBStages - 1) & 1u, abort_flag)) {
