@@ -114,7 +114,7 @@ uint16_t scale_bits(Rng& r, bool layer) {
 }
 
 struct Case {
-  const char* kernel;  // "q1_0_gemv", "q1_0_gemm_small" or "q2_0_gemv"
+  const char* kernel;  // "q1_0_gemv", "q1_0_gemm_small", "q1_0_gemm_small_noalloc" or "q2_0_gemv"
   int64_t rows, n, nvec;
   bool layer;          // layer-shaped regime: raw quants (with -128), log-normal scales
 };
@@ -242,6 +242,8 @@ int run_case(const Case& c, uint64_t seed, bool corrupt, Report& rep) {
   int e = ternary ? q2_0_gemv(d_packed, c.rows, c.n, d_q, d_d, d_out, nullptr)
           : (std::strcmp(c.kernel, "q1_0_gemv") == 0)
               ? q1_0_gemv(d_packed, c.rows, c.n, d_q, d_d, d_out, nullptr)
+          : (std::strcmp(c.kernel, "q1_0_gemm_small_noalloc") == 0)  // always the tensor-core kernel
+              ? q1_0_gemm_small_noalloc(d_packed, c.rows, c.n, c.nvec, d_q, d_d, d_out, nullptr)
               : q1_0_gemm_small(d_packed, c.rows, c.n, c.nvec, d_q, d_d, d_out, nullptr);
   if (e) return e;
   std::vector<float> out(size_t(c.nvec * c.rows));
@@ -362,6 +364,9 @@ extern "C" int q1_0_verify(int flags, char* report, size_t report_len) {
       {"q1_0_gemv", 1000, 4096, 1, true},    {"q1_0_gemv", 33, 14336, 1, true},   {"q1_0_gemv", 4096, 4096, 1, false},
       {"q1_0_gemv", 9999, 1152, 1, true},    {"q1_0_gemm_small", 300, 1024, 3, true},
       {"q1_0_gemm_small", 200, 4096, 16, false}, {"q1_0_gemm_small", 64, 512, 64, true},
+      // the tensor-core kernel on a ragged row tile and vector group, and on the layer-shaped
+      // regime, whose -128 quants send blocks to its dp4a tables
+      {"q1_0_gemm_small_noalloc", 300, 1024, 19, false}, {"q1_0_gemm_small_noalloc", 200, 4096, 16, true},
       {"q2_0_gemv", 64, 128, 1, true},    {"q2_0_gemv", 1000, 4096, 1, false}, {"q2_0_gemv", 33, 14336, 1, true},
       // more panels than one wave of the panel kernel holds: the streaming kernel
       {"q1_0_gemv", 40000, 256, 1, true},    {"q2_0_gemv", 40000, 256, 1, false},

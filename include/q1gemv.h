@@ -333,9 +333,11 @@ int q1_device_status(int clear);
  * compiled into the library.
  *   flags  : 0 = default shape set (small products for the panel kernel, two
  *            with too many rows for it that take the streaming kernel, and
- *            the batched product), preceded by an exhaustive check of the
- *            kernels' quantizer rounding (every float |t| < 2^22 against the
- *            device's roundf); bit 0 (1) = quick set (three small shapes, no
+ *            the batched product through q1_0_gemm_small and, for its
+ *            tensor-core kernel, q1_0_gemm_small_noalloc), preceded by an
+ *            exhaustive check of the kernels' quantizer rounding (every
+ *            float |t| < 2^22 against the device's roundf); bit 0 (1) =
+ *            quick set (three small shapes, no
  *            rounding check);
  *            bit 1 (2) = negative control: in every one-vector case the
  *            packed scales of one row (nonzero reference output, about the

@@ -63,12 +63,12 @@ def test_library_self_check():
     # first the exhaustive check of the kernels' quantizer rounding (all floats |t| < 2^22)
     assert lines[0] == "q8 rounding by adds: all 2499805184 floats with |t| < 2^22 equal roundf", report
     lines = lines[1:]
-    assert len(lines) == 15 and all(line.endswith("bit-exact") for line in lines), report
+    assert len(lines) == 17 and all(line.endswith("bit-exact") for line in lines), report
     # both matrix-vector kernels: the last two shapes have too many rows for the panel kernel
     assert binding.multi_plan([(40000, 256)])["panel_warps"] == 0
     assert binding.multi_plan([(40000, 256)], fmt="q2")["panel_warps"] == 0
     assert binding.multi_plan([(9999, 1152)])["panel_warps"] > 0
-    for kernel in ("q1_0_gemv ", "q1_0_gemm_small ", "q2_0_gemv "):
+    for kernel in ("q1_0_gemv ", "q1_0_gemm_small ", "q1_0_gemm_small_noalloc ", "q2_0_gemv "):
         assert any(line.startswith(kernel) for line in lines), (kernel, report)
 
 
