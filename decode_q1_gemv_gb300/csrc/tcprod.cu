@@ -537,9 +537,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++units_done) {
       if (u + int(gridDim.x) >= a.units && threadIdx.x == 0) pdl_launch_dependents();
       const int t = u / a.groups, g = u % a.groups;
-      float accE[kTcV], accO[kTcV];
+      // Vectors 2i and 2i + 1 side by side: the paired fma (two single
+      // roundings in one instruction) halves the epilogue's issue slots.
+      float2 accE[kTcV / 2], accO[kTcV / 2];
 #pragma unroll
-      for (int v = 0; v < kTcV; ++v) accE[v] = accO[v] = 0.0f;
+      for (int i = 0; i < kTcV / 2; ++i) accE[i] = accO[i] = make_float2(0.0f, 0.0f);
       for (int b0 = 0; b0 < a.nb && ok; b0 += 4) {
         // A weight quad: the row's word w and block scales of four blocks.
         if (!warp_wait(bar(kBarWFull + ws), wph, abort_flag)) {
@@ -571,13 +573,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
             tmem_ld16(lrow + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(w), dv);
             tmem_wait_ld16(dv);
 #pragma unroll
-            for (int v = 0; v < kTcV; ++v) accE[v] = __fmaf_rn(d0, __uint_as_float(dv[v]), accE[v]);
+            for (int i = 0; i < kTcV / 2; ++i)
+              accE[i] = __ffma2_rn(make_float2(d0, d0),
+                                   make_float2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1])), accE[i]);
             tmem_ld16(lrow + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(w) + 16u, dv);
             tmem_wait_ld16(dv);
             tc_fence_before();
             mbar_arrive(bar(kBarDEmpty + dsl));   // D slot free for the next block
 #pragma unroll
-            for (int v = 0; v < kTcV; ++v) accO[v] = __fmaf_rn(d0, __uint_as_float(dv[v]), accO[v]);
+            for (int i = 0; i < kTcV / 2; ++i)
+              accO[i] = __ffma2_rn(make_float2(d0, d0),
+                                   make_float2(__uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1])), accO[i]);
           } else {
             tc_fence_before();
             mbar_arrive(bar(kBarDEmpty + dsl));
@@ -586,11 +592,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
             const uint2 sc1[1] = {make_uint2(D0, 0u)};
 #pragma unroll
             for (int v = 0; v < kTcV; ++v) {
-              float aE[1] = {accE[v]}, aO[1] = {accO[v]};
+              float aE[1] = {(v & 1) ? accE[v / 2].y : accE[v / 2].x}, aO[1] = {(v & 1) ? accO[v / 2].y : accO[v / 2].x};
               quad_block<1, 0>(wv1, sc1, reinterpret_cast<const uint4*>(tabs + v * 320),
                                reinterpret_cast<const float4*>(tabs + v * 320 + 256), w, aE, aO);
-              accE[v] = aE[0];
-              accO[v] = aO[0];
+              if (v & 1) {
+                accE[v / 2].y = aE[0];
+                accO[v / 2].y = aO[0];
+              } else {
+                accE[v / 2].x = aE[0];
+                accO[v / 2].x = aO[0];
+              }
             }
           }
           mbar_arrive(bar(kBarBEmpty + s2));
@@ -605,7 +616,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
         break;
       }
 #pragma unroll
-      for (int v = 0; v < kTcV; ++v) part[(w * kTcV + v) * kTcRows + rt] = __fadd_rn(accE[v], accO[v]);
+      for (int v = 0; v < kTcV; ++v)
+        part[(w * kTcV + v) * kTcRows + rt] = (v & 1) ? __fadd_rn(accE[v / 2].y, accO[v / 2].y)
+                                                      : __fadd_rn(accE[v / 2].x, accO[v / 2].x);
       mbar_arrive(bar(kBarPartFull));
       if (!warp_wait(bar(kBarPartFull), uint32_t(units_done) & 1u, abort_flag)) {
         ok = false;
