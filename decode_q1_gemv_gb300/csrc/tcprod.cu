@@ -435,6 +435,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     // arithmetic stays warp-uniform.
     const int l = warp - kIssuerWarp0;
     const uint32_t idesc = idesc_f16(kTcRows, kTcV);
+    // Loop-invariant parts of the operands.  A descriptor's start address is
+    // its low 14 bits in 16-byte units, and every B tile lies well inside that
+    // range, so a tile's descriptor is the region's plus its offset / 16.
+    const uint64_t bdesc0 = smem_desc(smem_addr(smem + kOffB), 128, 256);
+    uint32_t dlane[2], alane[2];
+    uint64_t blane[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int ll = 2 * l + j;
+      dlane[j] = tbase + kColD + 32u * uint32_t(ll & 3) + 16u * uint32_t(ll >> 2);
+      alane[j] = tbase + 16u * uint32_t(ll & 3) + 8u * uint32_t(ll >> 2);
+      blane[j] = bdesc0 + uint64_t((2 * ll * 512) >> 4);
+    }
     int it = 0, last = -1, last_msl = 0, msl = 0;
     uint32_t last_mph = 0, mph = 0;
     bool ok = true;
@@ -456,15 +469,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
         }
         tc_fence_after();
         if (bflag[s2]) {
+          const uint32_t doff = 128u * uint32_t(dsl), aoff = 64u * uint32_t(asl);
+          const uint64_t boff = uint64_t(s2 * (kRecBytes >> 4));
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {  // this issuer's two lanes
-            const int ll = 2 * l + j;
-            const uint32_t bst = smem_addr(smem + kOffB + s2 * kRecBytes) + uint32_t(2 * ll) * 512u;
-            const uint32_t dcol =
-                tbase + kColD + 128u * uint32_t(dsl) + 32u * uint32_t(ll & 3) + 16u * uint32_t(ll >> 2);
-            const uint32_t acol = tbase + 64u * uint32_t(asl) + 16u * uint32_t(ll & 3) + 8u * uint32_t(ll >> 2);
-            mma_f16_ts_elect(dcol, acol, smem_desc(bst, 128, 256), idesc, 0u);
-            mma_f16_ts_elect(dcol, acol, smem_desc(bst + 512, 128, 256), idesc, 1u);
+          for (int j = 0; j < 2; ++j) {  // this issuer's two lanes: hi tile, then lo tile 512 B on
+            mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff, idesc, 0u);
+            mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff + (512 >> 4), idesc, 1u);
           }
         }
         mma_commit_elect(bar(kBarMDone + msl));  // D ready and A slot free
