@@ -448,13 +448,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
       alane[j] = tbase + 16u * uint32_t(ll & 3) + 8u * uint32_t(ll >> 2);
       blane[j] = bdesc0 + uint64_t((2 * ll * 512) >> 4);
     }
-    int it = 0, last = -1, last_msl = 0, msl = 0;
+    // The CTA's blocks in order, six at a time: a block's slot in every ring
+    // is its index modulo 6, a compile-time constant in the unrolled loop, and
+    // only the phase bit of the six-block round varies.
+    const int total = (a.units - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) * a.nb;
+    int last = -1, last_msl = 0;
     uint32_t last_mph = 0, mph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-      for (int b = 0; b < a.nb; ++b, ++it) {
-        const int asl = a_slot(msl), dsl = d_slot(msl), s2 = msl;
-        const uint32_t aph = a_phase(msl, mph), dph = d_phase(msl), bph = mph;
+    for (int it0 = 0; it0 < total && ok; it0 += kMSlots, mph ^= 1u) {
+#pragma unroll
+      for (int m = 0; m < kMSlots; ++m) {
+        const int it = it0 + m;
+        if (it >= total) break;
+        const int asl = a_slot(m), dsl = d_slot(m), s2 = m;
+        const uint32_t aph = a_phase(m, mph), dph = d_phase(m), bph = mph;
         // The A slot is built, the D slot is free (a fresh barrier counts
         // its phase of parity 1 as complete: the first kDSlots blocks pass)
         // and the B record has landed.
@@ -477,11 +484,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
             mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff + (512 >> 4), idesc, 1u);
           }
         }
-        mma_commit_elect(bar(kBarMDone + msl));  // D ready and A slot free
+        mma_commit_elect(bar(kBarMDone + m));  // D ready and A slot free
         last = it;
-        last_msl = msl;
+        last_msl = m;
         last_mph = mph;
-        ring_next<kMSlots>(msl, mph);
       }
     }
     // After an abort, this issuer's MMAs may still be running: let them
