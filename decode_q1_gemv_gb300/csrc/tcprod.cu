@@ -68,6 +68,7 @@
 // abort flag and the device status word, and every role winds down.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 #include <cuda_fp16.h>
 
 #include "table.cuh"
@@ -99,11 +100,12 @@ constexpr int kOffB = kOffW + kWStages * kWStageBytes;
 constexpr int kOffPart = kOffB + kBStages * kRecBytes;
 constexpr int kPartBytes = 4 * kTcV * kTcRows * 4;
 constexpr int kOffBars = kOffPart + kPartBytes;
-// barriers: wfull, wempty, bfull, bempty, afull, mdone, dempty, partfull, partfree
+// barriers: wfull, wempty, bfull, bempty, afull, mdone, dempty, partfull, partfree, drain
 constexpr int kBarWFull = 0, kBarWEmpty = kBarWFull + kWStages, kBarBFull = kBarWEmpty + kWStages,
               kBarBEmpty = kBarBFull + kBStages, kBarAFull = kBarBEmpty + kBStages, kBarMDone = kBarAFull + kASlots,
               kBarDEmpty = kBarMDone + kMSlots,
-              kBarPartFull = kBarDEmpty + kDSlots, kBarPartFree = kBarPartFull + 1, kNumBars = kBarPartFree + 1;
+              kBarPartFull = kBarDEmpty + kDSlots, kBarPartFree = kBarPartFull + 1, kBarDrain = kBarPartFree + 1,
+              kNumBars = kBarDrain + kIssuers;
 constexpr int kOffFlag = kOffBars + kNumBars * 8;
 constexpr int kOffMisc = kOffFlag + kBStages * 4;
 constexpr int kTcSmem = kOffMisc + 16;
@@ -365,6 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     // warps (each lane after its own accesses), the others by one thread.
     mbar_init(bar(kBarPartFull), 32 * kEpiWarps);
     mbar_init(bar(kBarPartFree), 32 * kEpiWarps);
+    for (int i = 0; i < kIssuers; ++i) mbar_init(bar(kBarDrain + i), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -452,47 +455,62 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     // is its index modulo 6, a compile-time constant in the unrolled loop, and
     // only the phase bit of the six-block round varies.
     const int total = (a.units - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) * a.nb;
-    int last = -1, last_msl = 0;
-    uint32_t last_mph = 0, mph = 0;
+    uint32_t mph = 0;
     bool ok = true;
-    for (int it0 = 0; it0 < total && ok; it0 += kMSlots, mph ^= 1u) {
+    int it0 = 0;
+    // Block m of a round (phase bit mph): false when a wait gave up.
+    auto issue = [&](auto mc) -> bool {
+      constexpr int m = decltype(mc)::value;
+      constexpr int asl = m & 1, dsl = m >= 3 ? m - 3 : m, s2 = m;
+      const uint32_t aph = mph ^ uint32_t((m >> 1) & 1), dph = m >= 3 ? 1u : 0u, bph = mph;
+      // The A slot is built, the D slot is free (a fresh barrier counts its
+      // phase of parity 1 as complete: the first kDSlots blocks pass) and the
+      // B record has landed.
+      const bool ready =
+          mbar_test3(bar(kBarAFull + asl), aph, bar(kBarDEmpty + dsl), dph ^ 1u, bar(kBarBFull + s2), bph);
+      if (!__all_sync(0xffffffffu, ready) &&
+          (!warp_wait(bar(kBarAFull + asl), aph, abort_flag) ||
+           !warp_wait(bar(kBarDEmpty + dsl), dph ^ 1u, abort_flag) ||
+           !warp_wait(bar(kBarBFull + s2), bph, abort_flag)))
+        return false;
+      tc_fence_after();
+      if (bflag[s2]) {
+        constexpr uint32_t doff = 128u * dsl, aoff = 64u * asl;
+        constexpr uint64_t boff = uint64_t(s2 * (kRecBytes >> 4));
 #pragma unroll
-      for (int m = 0; m < kMSlots; ++m) {
-        const int it = it0 + m;
-        if (it >= total) break;
-        const int asl = a_slot(m), dsl = d_slot(m), s2 = m;
-        const uint32_t aph = a_phase(m, mph), dph = d_phase(m), bph = mph;
-        // The A slot is built, the D slot is free (a fresh barrier counts
-        // its phase of parity 1 as complete: the first kDSlots blocks pass)
-        // and the B record has landed.
-        const bool ready =
-            mbar_test3(bar(kBarAFull + asl), aph, bar(kBarDEmpty + dsl), dph ^ 1u, bar(kBarBFull + s2), bph);
-        if (!__all_sync(0xffffffffu, ready) &&
-            (!warp_wait(bar(kBarAFull + asl), aph, abort_flag) ||
-             !warp_wait(bar(kBarDEmpty + dsl), dph ^ 1u, abort_flag) ||
-             !warp_wait(bar(kBarBFull + s2), bph, abort_flag))) {
-          ok = false;
-          break;
+        for (int j = 0; j < 2; ++j) {  // this issuer's two lanes: hi tile, then lo tile 512 B on
+          mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff, idesc, 0u);
+          mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff + (512 >> 4), idesc, 1u);
         }
-        tc_fence_after();
-        if (bflag[s2]) {
-          const uint32_t doff = 128u * uint32_t(dsl), aoff = 64u * uint32_t(asl);
-          const uint64_t boff = uint64_t(s2 * (kRecBytes >> 4));
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {  // this issuer's two lanes: hi tile, then lo tile 512 B on
-            mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff, idesc, 0u);
-            mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff + (512 >> 4), idesc, 1u);
-          }
-        }
-        mma_commit_elect(bar(kBarMDone + m));  // D ready and A slot free
-        last = it;
-        last_msl = m;
-        last_mph = mph;
       }
+      mma_commit_elect(bar(kBarMDone + m));  // D ready and A slot free
+      return true;
+    };
+    // Whole rounds without bounds checks, then the last partial round.
+    using I0 = std::integral_constant<int, 0>;
+    using I1 = std::integral_constant<int, 1>;
+    using I2 = std::integral_constant<int, 2>;
+    using I3 = std::integral_constant<int, 3>;
+    using I4 = std::integral_constant<int, 4>;
+    using I5 = std::integral_constant<int, 5>;
+    const int whole = total - total % kMSlots;
+    for (; it0 < whole && ok; it0 += kMSlots, mph ^= 1u)
+      ok = issue(I0{}) && issue(I1{}) && issue(I2{}) && issue(I3{}) && issue(I4{}) && issue(I5{});
+    if (ok && it0 < total) {
+      const int rest = total - it0;  // 1 to 5 blocks
+      ok = issue(I0{});
+      if (ok && rest > 1) ok = issue(I1{});
+      if (ok && rest > 2) ok = issue(I2{});
+      if (ok && rest > 3) ok = issue(I3{});
+      if (ok && rest > 4) ok = issue(I4{});
     }
-    // After an abort, this issuer's MMAs may still be running: let them
-    // finish (bounded) before the tensor memory is released.
-    if (!ok && last >= 0 && lane == 0) mbar_wait(bar(kBarMDone + last_msl), last_mph, 100000000ull);
+    // After an abort, this issuer's MMAs may still be running: a commit to its
+    // own drain barrier arrives once they are all through (at once if there
+    // are none); wait for it (bounded) before the tensor memory is released.
+    if (!ok) {
+      mma_commit_elect(bar(kBarDrain + l));
+      if (lane == 0) mbar_wait(bar(kBarDrain + l), 0u, 100000000ull);
+    }
     __syncwarp();
   } else if (warp >= kBuildWarp0) {
     // ------------------------------------------------------- A builders --
