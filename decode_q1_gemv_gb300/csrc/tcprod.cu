@@ -85,8 +85,11 @@ constexpr int kSlowBytes = kTcV * 320;   // 16 vectors' one-block dp4a tables (t
 constexpr int kEpiWarps = 16;            // warps 0-15
 constexpr int kEpi = kEpiWarps * 32;
 constexpr int kBuildWarp0 = 16, kBuildWarps = 8;
-constexpr int kIssuerWarp0 = 24, kIssuers = 4;
-constexpr int kProducerWarp = 28;
+constexpr int kIssuerWarp0 = kBuildWarp0 + kBuildWarps, kIssuers = 4;
+constexpr int kBuildWords = 16 / kBuildWarps;  // sign words a builder warp turns into A, for its 32 rows
+constexpr int kIssuerLanes = 8 / kIssuers;     // lanes whose MMAs an issuer warp issues
+static_assert(kBuildWarps % 4 == 0 && 16 % kBuildWarps == 0 && 8 % kIssuers == 0, "role split");
+constexpr int kProducerWarp = kIssuerWarp0 + kIssuers;
 constexpr int kTcThreads = 29 * 32;
 constexpr int kASlots = 2, kDSlots = 3;
 constexpr int kMSlots = 6;  // MMA-completion barriers: block i on i % 6, a multiple of both slot counts
@@ -442,11 +445,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     // its low 14 bits in 16-byte units, and every B tile lies well inside that
     // range, so a tile's descriptor is the region's plus its offset / 16.
     const uint64_t bdesc0 = smem_desc(smem_addr(smem + kOffB), 128, 256);
-    uint32_t dlane[2], alane[2];
-    uint64_t blane[2];
+    uint32_t dlane[kIssuerLanes], alane[kIssuerLanes];
+    uint64_t blane[kIssuerLanes];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int ll = 2 * l + j;
+    for (int j = 0; j < kIssuerLanes; ++j) {
+      const int ll = kIssuerLanes * l + j;
       dlane[j] = tbase + kColD + 32u * uint32_t(ll & 3) + 16u * uint32_t(ll >> 2);
       alane[j] = tbase + 16u * uint32_t(ll & 3) + 8u * uint32_t(ll >> 2);
       blane[j] = bdesc0 + uint64_t((2 * ll * 512) >> 4);
@@ -478,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
         constexpr uint32_t doff = 128u * dsl, aoff = 64u * asl;
         constexpr uint64_t boff = uint64_t(s2 * (kRecBytes >> 4));
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {  // this issuer's two lanes: hi tile, then lo tile 512 B on
+        for (int j = 0; j < kIssuerLanes; ++j) {  // this issuer's lanes: hi tile, then lo tile 512 B on
           mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff, idesc, 0u);
           mma_f16_ts_elect(dlane[j] + doff, alane[j] + aoff, blane[j] + boff + (512 >> 4), idesc, 1u);
         }
@@ -514,7 +517,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
     __syncwarp();
   } else if (warp >= kBuildWarp0) {
     // ------------------------------------------------------- A builders --
-    const int quarter = warp & 3, half = (warp - kBuildWarp0) >> 2;  // words 2 half, 2 half + 1
+    const int quarter = warp & 3, grp = (warp - kBuildWarp0) >> 2;  // words kBuildWords grp ... + kBuildWords - 1
     const uint32_t lrow = tbase + (uint32_t(quarter * 32) << 16);
     int it = 0, ws = 0, asl = 0, msl = 0;  // msl, mph: MMA-completion barrier of block it - kASlots
     uint32_t wph = 0, aph = 0, mph = 0;
@@ -528,8 +531,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
           break;
         }
         const unsigned char* st = smem + kOffW + ws * kWStageBytes + quarter * 2048 + lane * 64;
-        const uint4 wq0 = *reinterpret_cast<const uint4*>(st + 2 * half * 16);
-        const uint4 wq1 = *reinterpret_cast<const uint4*>(st + (2 * half + 1) * 16);
+        uint4 wq[kBuildWords];
+#pragma unroll
+        for (int jj = 0; jj < kBuildWords; ++jj)
+          wq[jj] = *reinterpret_cast<const uint4*>(st + (kBuildWords * grp + jj) * 16);
         mbar_arrive(bar(kBarWEmpty + ws));
         ring_next<kWStages>(ws, wph);
 #pragma unroll
@@ -545,10 +550,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_q1_tc(const __grid_constant__
           }
           tc_fence_after();
 #pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
+          for (int jj = 0; jj < kBuildWords; ++jj) {
             uint32_t av[16];
-            signs_to_f16(word_of(jj ? wq1 : wq0, bq), av);
-            tmem_st16(lrow + 64u * uint32_t(asl) + 16u * uint32_t(2 * half + jj), av);
+            signs_to_f16(word_of(wq[jj], bq), av);
+            tmem_st16(lrow + 64u * uint32_t(asl) + 16u * uint32_t(kBuildWords * grp + jj), av);
           }
           tmem_wait_st();
           tc_fence_before();
