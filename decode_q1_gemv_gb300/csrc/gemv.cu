@@ -260,14 +260,14 @@ static int scratch_pool(cudaMemPool_t* out) {
 // Which kernel is faster for a product, from a cost model of both measured on
 // a GB300 (cold L2, one launch between events; 14336x4096 to 128256x4096,
 // 8 to 64 vectors): the tensor-core kernel keeps one 128-row x 16-vector
-// unit per SM in flight at about 0.59 us per block of 128 weights, plus
+// unit per SM in flight at about 0.51 us per block of 128 weights, plus
 // about 12 us of prologue and ramp; the dp4a kernel streams about 2.2e13
 // weight-vector products per second plus about 5 us.
 static bool tc_faster(int64_t rows, int64_t n, int64_t nvec) {
   const double sms = double(num_sms());
   const double units = double((rows + 127) / 128) * double((nvec + 15) / 16);
   const double waves = std::ceil(units / sms);
-  const double t_tc = waves * double(n / kBlock) * 0.59 + 12.0;
+  const double t_tc = waves * double(n / kBlock) * 0.51 + 12.0;
   const double t_dp4a = double(rows) * double(n) * double(nvec) / 2.2e7 + 5.0;
   return t_tc < t_dp4a;
 }
