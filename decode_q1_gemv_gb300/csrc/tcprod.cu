@@ -34,6 +34,11 @@
 //
 // Structure (one persistent CTA per SM, 29 warps, stages that run
 // concurrently on different blocks):
+//   warps 0-15  epilogue: warp (quarter q, word w) takes lanes w, w+4 of its
+//               32 rows from tensor memory into acc = fma(d0, ab, acc), two
+//               vectors an instruction (or runs the dp4a chain on a table
+//               block); at the end of a tile the four words' partial sums
+//               meet in shared memory for the horizontal sum.
 //   warps 16-23 A builders: warp 16 + 4h + q owns rows 32q..32q+31 of the
 //               128-row tile (tensor-memory lanes) and turns their sign words
 //               2h and 2h + 1 into the +-1 f16 A operand of those words' four
@@ -44,19 +49,14 @@
 //               warps issue in parallel) and commits them once to the
 //               block's completion barrier (D ready, A slot free).  The
 //               whole warp runs the loop and one elected lane issues.
-// Each block's slot in every ring (A 2, D 3, B records 6, completion 6)
-// follows from one counter of the block index modulo 6.  The four schedulers
-// of the SM carry all 29 warps' instructions, and the non-issuing roles'
-// control code competes with the issuers for them and for the ALU pipe: the
-// quad loops are unrolled and the builders' multiply-adds kept on the FMA
-// pipe for that reason.
-//   warps 0-15  epilogue: warp (quarter q, word w) takes lanes w, w+4 of its
-//               32 rows from tensor memory into acc = fma(d0, ab, acc) (or runs
-//               the dp4a chain on a table block); at the end of a tile the four
-//               words' partial sums meet in shared memory for the horizontal
-//               sum.
 //   warp 28     producer: 1-D bulk copies of the tile's weight quads (4
 //               blocks x 128 rows) and of each block's B record into rings.
+// Each block's slot in every ring (A 2, D 3, B records 6, completion 6)
+// follows from the block index modulo 6; the issuers walk their blocks six
+// at a time, so their slots are compile-time constants.  The issuers' own
+// instruction stream sets the pace, and all 29 warps share the SM's four
+// schedulers and its ALU pipe: the roles' loops are unrolled, the builders'
+// multiply-adds kept on the FMA pipe and the epilogue's fmas paired.
 // Tensor memory: two A slots of 64 columns (8 lanes x 8 f16 pairs) and three
 // D slots of 128 columns (8 lanes x 16 vectors).  Within a slot the two lanes
 // of sign word w sit side by side (A: lane w at 16w, lane w+4 at 16w + 8;
