@@ -98,6 +98,7 @@ def activations_q(rng, nvec, n, regime):
     (777, 2048, 16, "layer"),
     (2000, 4096, 20, "mixed"),
     (1, 128, 17, "quantized"),
+    (260, 1408, 16, "quantized"),   # 11 blocks: the issuers' last round holds five
 ])
 def test_tensor_kernel_equals_dp4a_and_oracle(rows, n, nvec, regime):
     rng = synth.rng_for(601, rows, n, nvec, len(regime))
