@@ -209,17 +209,21 @@ def unpack(packed: torch.Tensor, rows: int, n: int, blocks: torch.Tensor | None 
 
 
 def quantize(x: torch.Tensor, q: torch.Tensor | None = None, d: torch.Tensor | None = None, stream=None):
-    """q8_0 quantization of x [nvec, n] (or [n]).  Returns (q int8, d int16 fp16 bits)."""
+    """q8_0 quantization of x [nvec, n] (or [n]).  Returns (q int8, d int16 fp16 bits).
+    x, q and d may be pinned host tensors (the kernel addresses them directly);
+    q and d are allocated on the GPU when not given."""
     n = x.shape[-1]
     nvec = x.numel() // n if n else 0
+    dev = x.device if x.is_cuda else torch.device("cuda")
     if q is None:
-        q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+        q = torch.empty(x.shape, dtype=torch.int8, device=dev)
     if d is None:
-        d = torch.empty(x.shape[:-1] + (n // 32,), dtype=torch.int16, device=x.device)
+        d = torch.empty(x.shape[:-1] + (n // 32,), dtype=torch.int16, device=dev)
     if q.numel() != nvec * n or d.numel() != nvec * (n // 32):
         raise ValueError("q/d sizes do not match x")
-    _check(load().q8_quantize_act(_dev(x, "x", (torch.float32,)), nvec, n, _dev(q, "q", (torch.int8,)),
-                                  _dev(d, "d", _SCALE_DTYPES), _stream_ptr(stream)), "q8_quantize_act")
+    _check(load().q8_quantize_act(_dev(x, "x", (torch.float32,), True), nvec, n,
+                                  _dev(q, "q", (torch.int8,), True), _dev(d, "d", _SCALE_DTYPES, True),
+                                  _stream_ptr(stream)), "q8_quantize_act")
     return q, d
 
 

@@ -83,7 +83,7 @@ class DecodeSet:
             self.out_off.append(nout)
             nx += _round_up(n, 256)
             nout += _round_up(rows, 64)
-        self.x_all = torch.empty(nx, dtype=torch.float32, device=self.device)
+        self.x_all = torch.zeros(nx, dtype=torch.float32, device=self.device)  # padding stays 0
         self.q_all = torch.empty(nx, dtype=torch.int8, device=self.device)
         self.d_all = torch.empty(nx // 32, dtype=torch.int16, device=self.device)
         self.out_all = torch.empty(nout, dtype=torch.float32, device=self.device)

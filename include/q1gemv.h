@@ -91,7 +91,9 @@ int q1_0_unpack(const void *packed, int64_t rows, int64_t n, uint8_t *blocks, vo
  * q = roundf(x*id) (half away from zero), scale stored as fp16 (round to
  * nearest even) of d.
  *   x : device f32 [nvec][n]; q : device int8 [nvec][n];
- *   d : device fp16 bits [nvec][n/32].
+ *   d : device fp16 bits [nvec][n/32].  Each of the three may instead be
+ *   pinned host memory, under the same rule as the products' activations
+ *   (one launch then reads x over the host link, in full 512-byte requests).
  * n is a multiple of 32 here (128 for use with the products), 1 <= nvec <= 65535.
  * Inputs must be finite and max|x| <= 65504*127 for the scale to stay finite. */
 int q8_quantize_act(const float *x, int64_t nvec, int64_t n, int8_t *q, uint16_t *d, void *stream);

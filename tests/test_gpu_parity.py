@@ -174,6 +174,41 @@ def test_quantize_parity(case):
     assert np.array_equal(d.cpu().numpy().view(np.uint16), want_d)
 
 
+@pytest.mark.parametrize("nvec,n", [(5, 1184), (1, 96), (2, 32 * 33)])
+def test_quantize_ragged_block_counts_guard_untouched(nvec, n):
+    """Block counts that are not a multiple of a warp's four blocks or a CTA's
+    32 (185, 3 and 66): every block quantized, nothing written past the end."""
+    rng = synth.rng_for(103, nvec, n)
+    x = synth.activations(rng, nvec, n, outliers=0.01)
+    q_big = torch.full((nvec * n + 512,), 77, dtype=torch.int8, device="cuda")
+    d_big = torch.full((nvec * (n // 32) + 256,), 0x7E00, dtype=torch.int16, device="cuda")
+    binding.quantize(dev(x), q_big[:nvec * n], d_big[:nvec * (n // 32)])
+    want_q, want_d = oracle.q8_quantize(x)
+    got_q, got_d = q_big.cpu().numpy(), d_big.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got_q[:nvec * n].reshape(nvec, n), want_q)
+    assert np.array_equal(got_d[:nvec * (n // 32)].reshape(nvec, n // 32), want_d)
+    assert np.all(got_q[nvec * n:] == 77) and np.all(got_d[nvec * (n // 32):] == 0x7E00)
+
+
+def test_quantize_from_pinned_host_activations():
+    """x in pinned host memory, read by the kernel over the host link; q and d
+    on the device and, in a second call, in pinned host memory too."""
+    rng = synth.rng_for(104)
+    nvec, n = 2, 14336
+    x = synth.activations(rng, nvec, n, outliers=0.01)
+    hx = torch.from_numpy(x).pin_memory()
+    want_q, want_d = oracle.q8_quantize(x)
+    q, d = binding.quantize(hx)
+    torch.cuda.synchronize()
+    assert q.is_cuda and np.array_equal(q.cpu().numpy(), want_q)
+    assert np.array_equal(d.cpu().numpy().view(np.uint16), want_d)
+    hq = torch.empty((nvec, n), dtype=torch.int8).pin_memory()
+    hd = torch.empty((nvec, n // 32), dtype=torch.int16).pin_memory()
+    binding.quantize(hx, hq, hd)
+    torch.cuda.synchronize()
+    assert np.array_equal(hq.numpy(), want_q) and np.array_equal(hd.numpy().view(np.uint16), want_d)
+
+
 def test_quantize_hand_derived_fixture():
     import json
     import os
