@@ -86,6 +86,19 @@ def test_shape_limits_rejected_on_host(lib):
     assert lib.q8_quantize_act(fake, 1, 48, fake, fake, None) == binding.Q1_ERR_ARG
 
 
+def test_kernel_choice_knob_rejects_bad_values_and_round_trips(lib):
+    """The batched product's kernel choice is a host setting: a bad value is
+    refused with a message, a good one returns the previous choice."""
+    assert lib.q1_gemm_small_kernel(3) == binding.Q1_ERR_ARG
+    assert "choice" in binding.last_error()
+    assert lib.q1_gemm_small_kernel(-1) == binding.Q1_ERR_ARG
+    assert binding.gemm_small_kernel("tensor") == "auto"
+    assert binding.gemm_small_kernel("dp4a") == "tensor"
+    assert binding.gemm_small_kernel("auto") == "dp4a"
+    with pytest.raises(ValueError):
+        binding.gemm_small_kernel("cuda")
+
+
 def test_misaligned_pointers_rejected_on_host(lib):
     ok = ctypes.c_void_p(0x10000)
     bad = ctypes.c_void_p(0x10004)
