@@ -174,10 +174,11 @@ def test_quantize_parity(case):
     assert np.array_equal(d.cpu().numpy().view(np.uint16), want_d)
 
 
-@pytest.mark.parametrize("nvec,n", [(5, 1184), (1, 96), (2, 32 * 33)])
+@pytest.mark.parametrize("nvec,n", [(5, 1184), (1, 96), (2, 32 * 33), (5, 32 * 3333)])
 def test_quantize_ragged_block_counts_guard_untouched(nvec, n):
     """Block counts that are not a multiple of a warp's four blocks or a CTA's
-    32 (185, 3 and 66): every block quantized, nothing written past the end."""
+    32 (185, 3, 66 and 16665): every block quantized, nothing written past the
+    end."""
     rng = synth.rng_for(103, nvec, n)
     x = synth.activations(rng, nvec, n, outliers=0.01)
     q_big = torch.full((nvec * n + 512,), 77, dtype=torch.int8, device="cuda")
@@ -190,11 +191,12 @@ def test_quantize_ragged_block_counts_guard_untouched(nvec, n):
     assert np.all(got_q[nvec * n:] == 77) and np.all(got_d[nvec * (n // 32):] == 0x7E00)
 
 
-def test_quantize_from_pinned_host_activations():
+@pytest.mark.parametrize("nvec,n", [(2, 14336), (40, 16384)])
+def test_quantize_from_pinned_host_activations(nvec, n):
     """x in pinned host memory, read by the kernel over the host link; q and d
-    on the device and, in a second call, in pinned host memory too."""
-    rng = synth.rng_for(104)
-    nvec, n = 2, 14336
+    on the device and, in a second call, in pinned host memory too (one
+    activation, and 40 side by side)."""
+    rng = synth.rng_for(104, nvec)
     x = synth.activations(rng, nvec, n, outliers=0.01)
     hx = torch.from_numpy(x).pin_memory()
     want_q, want_d = oracle.q8_quantize(x)
