@@ -62,3 +62,27 @@ def test_reference_arm_rank_above_zero_does_no_work(monkeypatch):
     with redirect_stdout(buf):
         assert bench.run_reference(A()) == 0
     assert buf.getvalue() == ""
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` runs the oracle on the host cores (no GPU
+    needed) and prints one JSON line with the keys the benchmark contract
+    names: the same metric and unit as the CUDA arm, its cpu_baseline and an
+    e2e object that moves no bytes to or from a device."""
+    import json
+    import subprocess
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"]
